@@ -1,0 +1,143 @@
+"""Pins for the oracle's stratified selection.
+
+Stratified Sparse Attention news page, "How SSA splits the cache into
+strata": top-k stratum read deterministically; the remainder sampled with
+probability proportional to approximate attention; top-k and the top-k +
+uniform hybrid are special cases ("The idea is close to classical stratified
+sampling").
+"""
+import math
+
+import numpy as np
+import pytest
+
+
+def _order(s):
+    # brute force: descending value with -0 below +0, ties by ascending index
+    key = [(-(float(v)), -math.copysign(1.0, float(v)) if v == 0 else 0.0, i) for i, v in enumerate(s)]
+    return [k[2] for k in sorted(key)]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_matches_brute_force_with_ties(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(1, 400))
+    s = np.round(rng.standard_normal(N) * 3) / 2       # many exact ties
+    s[rng.random(N) < 0.1] = 0.0
+    s[rng.random(N) < 0.1] = -0.0
+    s = s.astype(np.float32)
+    for k in sorted({0, 1, N // 3, N - 1, N, N + 5}):
+        if k < 0:
+            continue
+        idx, p, m, Z = oracle_mod.select_unit(s, k, 0.0, 0, 0, 0)
+        want = sorted(_order(s)[:k])
+        assert idx.tolist() == want
+        assert np.all(p == 1.0)
+        if 0 < N and k <= N:
+            assert m == s[_order(s)[max(k, 1) - 1]]
+
+
+def test_budget_infinite_selects_everything(oracle_mod):
+    s = np.random.default_rng(0).standard_normal(333).astype(np.float32)
+    idx, p, m, Z = oracle_mod.select_unit(s, 17, math.inf, 5, 0, 0)
+    assert idx.tolist() == list(range(333)) and np.all(p == 1.0)
+
+
+def test_k_at_least_n_is_dense(oracle_mod):
+    s = np.random.default_rng(1).standard_normal(50).astype(np.float32)
+    idx, p, m, Z = oracle_mod.select_unit(s, 50, 10.0, 5, 0, 0)
+    assert idx.tolist() == list(range(50)) and np.all(p == 1.0) and Z == 0.0
+
+
+def test_k_zero_uses_the_maximum_as_reference(oracle_mod):
+    s = np.random.default_rng(2).standard_normal(100).astype(np.float32)
+    idx, p, m, Z, p_all = oracle_mod.select_unit(s, 0, 10.0, 5, 0, 0, want_p_all=True)
+    assert m == s.max()
+    assert Z >= 1.0  # the arg-max term is exp(0) = 1
+    assert np.all(p_all < 1.0 + 1e-7)
+
+
+def test_inclusion_probabilities_sum_to_budget(oracle_mod):
+    # sum_R B e_j / Z = B when no p is clipped
+    rng = np.random.default_rng(3)
+    s = (rng.standard_normal(5000) * 0.3).astype(np.float32)
+    k, B = 50, 40.0
+    idx, p, m, Z, p_all = oracle_mod.select_unit(s, k, B, 1, 0, 0, want_p_all=True)
+    top = set(_order(s)[:k])
+    R = [j for j in range(s.size) if j not in top]
+    assert np.all(p_all[list(top)] == 1.0)
+    assert p_all[R].max() < 1.0
+    assert abs(p_all[R].astype(np.float64).sum() - B) < 1e-4 * B
+    # proportional to exp(s): the ratio of two p's is the ratio of their exponentials
+    a, b = R[0], R[1]
+    assert abs(p_all[a] / p_all[b] - math.exp(float(s[a]) - float(s[b]))) < 1e-5
+
+
+def test_clipping_keeps_sum_below_budget(oracle_mod):
+    s = np.zeros(100, np.float32)
+    s[:5] = 10.0
+    idx, p, m, Z, p_all = oracle_mod.select_unit(s, 0, 50.0, 1, 0, 0, want_p_all=True)
+    assert np.all(p_all[:5] == 1.0)
+    assert p_all.sum() <= 50.0 + 1e-4
+
+
+def test_constant_scores_give_the_uniform_hybrid(oracle_mod):
+    # constant estimates: T = first k indices, every other token has p = B/(N-k)
+    N, k, B = 1000, 30, 70.0
+    s = np.full(N, 0.25, np.float32)
+    idx, p, m, Z, p_all = oracle_mod.select_unit(s, k, B, 9, 0, 0, want_p_all=True)
+    assert np.all(p_all[:k] == 1.0)
+    assert Z == np.float32(N - k)
+    assert np.all(p_all[k:] == np.float32(B) / np.float32(N - k))
+    assert set(range(k)) <= set(idx.tolist())
+
+
+def test_budget_zero_is_pure_topk(oracle_mod):
+    s = np.random.default_rng(4).standard_normal(777).astype(np.float32)
+    idx, p, m, Z = oracle_mod.select_unit(s, 40, 0.0, 3, 0, 0)
+    assert idx.tolist() == sorted(_order(s)[:40])
+
+
+def test_selection_frequency_matches_p(oracle_mod):
+    # Poisson sampling: token j is drawn with probability p_j, independently of the others
+    rng = np.random.default_rng(5)
+    N, k, B = 64, 4, 12.0
+    s = (rng.standard_normal(N) * 1.2).astype(np.float32)
+    _, _, _, _, p_all = oracle_mod.select_unit(s, k, B, 0, 0, 0, want_p_all=True)
+    trials = 4000
+    hits = np.zeros(N)
+    counts = []
+    for seed in range(trials):
+        idx, _, _, _ = oracle_mod.select_unit(s, k, B, seed, 1, 2)
+        hits[idx] += 1
+        counts.append(idx.size)
+    freq = hits / trials
+    sd = np.sqrt(np.maximum(p_all * (1 - p_all), 1e-12) / trials)
+    assert np.all(np.abs(freq - p_all) <= 5 * sd + 1e-9)
+    assert abs(np.mean(counts) - p_all.astype(np.float64).sum()) < 5 * np.sqrt(p_all.sum() / trials) + 1e-6
+
+
+def test_selection_is_deterministic_per_seed_and_unit(oracle_mod):
+    s = np.random.default_rng(6).standard_normal(4000).astype(np.float32)
+    a = oracle_mod.select_unit(s, 20, 100.0, 11, 0, 0)[0]
+    b = oracle_mod.select_unit(s, 20, 100.0, 11, 0, 0)[0]
+    c = oracle_mod.select_unit(s, 20, 100.0, 12, 0, 0)[0]
+    d = oracle_mod.select_unit(s, 20, 100.0, 11, 0, 1)[0]
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, c) and not np.array_equal(a, d)
+
+
+def test_non_finite_scores_are_rejected(oracle_mod):
+    s = np.zeros(10, np.float32)
+    s[3] = np.nan
+    with pytest.raises(FloatingPointError):
+        oracle_mod.select_unit(s, 2, 1.0, 0, 0, 0)
+    s[3] = np.inf
+    with pytest.raises(FloatingPointError):
+        oracle_mod.select_unit(s, 2, 1.0, 0, 0, 0)
+
+
+def test_cap_overflow_is_reported(oracle_mod):
+    s = np.zeros(10, np.float32)
+    with pytest.raises(OverflowError):
+        oracle_mod.select_unit(s, 5, 0.0, 0, 0, 0, cap=3)
