@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark: microseconds per Stratified Sparse Attention decode step.
+
+Default workload: the Ministral-8B-shaped layer at 128K context (batch 2,
+32 query / 8 KV heads, d = 128, d_sel = 32, 50x sparsity: top-k 1311,
+budget 1310), seeded synthetic inputs resident in HBM.  A step is one
+ssa_decode call (score -> select -> corrected attention, one kernel launch);
+the seed changes every step.  L2 is flushed (a 256 MiB write) before every
+timed step and each step is timed alone with CUDA events on its stream.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle
+instead (the reference arm for this method has no runnable upstream code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per sparse decode step at 128K/1M ctx; achieved HBM GB/s vs B300 peak"
+UNIT = "us/step"
+FLUSH_BYTES = 256 << 20
+CSRC = os.path.join(ROOT, "long_context_decode_subset_b300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ministral8b_128k")
+    ap.add_argument("--secondary", default="ministral8b_1m", help="second workload reported beside ('' = none)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clocks"}
+
+    def __init__(self, index: int, period: float = 0.01):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._period = period
+        self._handle = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._handle = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._handle, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self._handle = None
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._nvml.nvmlDeviceGetClockInfo(self._handle, self._nvml.NVML_CLOCK_SM))
+                try:
+                    r = self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._handle)
+                except AttributeError:
+                    r = self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self._handle)
+                self.reasons |= int(r) & ~0x1
+            except Exception:
+                pass
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self._handle is not None:
+            self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._handle is not None:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b], "samples": len(self.samples)}
+
+
+def algorithmic_bytes(cfg, rows_selected: float) -> float:
+    """Key summary + selected K and V rows + q in + out/lse out (bytes per step)."""
+    summary = cfg.batch * cfg.n_kv_heads * cfg.ctx_len * cfg.d_sel * 2
+    rows = rows_selected * cfg.head_dim * 2 * 2
+    io = cfg.batch * cfg.n_q_heads * (cfg.head_dim * 2 + cfg.head_dim * 4 + 4)
+    return float(summary + rows + io)
+
+
+def traffic_for(workload: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_sha") == source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def u16(t):
+    import numpy as np
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def host_inputs(w, Ks):
+    return dict(q=u16(w["q"]), K=u16(w["K"]), V=u16(w["V"]), Ks=u16(Ks), sel=w["sel_ch"].cpu().numpy())
+
+
+def time_oracle(h, cfg, seconds: float, max_steps: int | None = None):
+    """Time oracle.decode steps (all units, all host threads) for about `seconds`."""
+    import oracle
+    times = []
+    t_end = time.perf_counter() + seconds
+    step = 0
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode(h["q"], h["K"], h["V"], h["Ks"], h["sel"], cfg.top_k, cfg.budget, step, cfg.scale,
+                      want_lists=False)
+        times.append(time.perf_counter() - t0)
+        step += 1
+        if (max_steps is not None and step >= max_steps) or (max_steps is None and time.perf_counter() > t_end):
+            break
+    return times, oracle.num_threads()
+
+
+def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    w = workloads.generate(cfg, 0, dev)
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    q, K, V, sel = w["q"], w["K"], w["V"], w["sel_ch"]
+    shape = ssa.shape_of(q, K, Ks)
+    ws = ssa.workspace(shape, 0, dev)
+    units = cfg.batch * cfg.n_kv_heads
+    out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((cfg.batch, cfg.n_q_heads), dtype=torch.float32, device=dev)
+    counts = torch.zeros((steps, units), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, count_buf=None):
+        ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out=out, lse=lse,
+                       count=count_buf, ws=ws, stream=stream)
+
+    for i in range(warmup):
+        flush.fill_(i & 0xff)
+        step(1_000_000 + i)
+    torch.cuda.synchronize()
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(50_000_000)  # give the host a head start so launches queue up
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            step(i, counts[i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    times_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    rows = counts.sum(dim=1).double().mean().item()
+    res = dict(times_us=times_us, rows=rows, clocks=clk.summary(), w=w, Ks=Ks)
+
+    if with_e2e:
+        q_host = q.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(warmup):
+            ssa.ssa_decode_host(q_host, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out_h, lse_h, ws,
+                                stream=stream)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(50_000_000)
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev2[i][0].record(stream)
+            ssa.ssa_decode_host(q_host, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out_h, lse_h, ws,
+                                stream=stream)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        res["e2e_us"] = [a.elapsed_time(b) * 1e3 for a, b in ev2]
+        res["h2d"] = q_host.numel() * 2
+        res["d2h"] = out_h.numel() * 4 + lse_h.numel() * 4
+    del flush
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    cfg = workloads.CONFIGS[args.workload]
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    m = measure_ours(cfg, args.steps, args.warmup, dev)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+
+    mean_us = statistics.fmean(m["times_us"])
+    e2e_us = statistics.fmean(m["e2e_us"])
+    if world > 1:
+        tt = torch.tensor([mean_us, e2e_us], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_us, e2e_us = tt.tolist()
+    peak, peak_kind = measured_peaks()
+    abytes = algorithmic_bytes(cfg, m["rows"])
+    achieved = abytes / (mean_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(mean_us / world, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_us / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; shapes of a Ministral-8B layer, generator in workloads/)",
+        "config": {
+            "workload": cfg.name, "batch": cfg.batch, "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads,
+            "head_dim": cfg.head_dim, "ctx_len": cfg.ctx_len, "d_sel": cfg.d_sel, "top_k": cfg.top_k,
+            "budget": cfg.budget, "inputs": "bf16 q/K/V/summary, fp32 scores and accumulation",
+            "l2": "flushed before every timed step (256 MiB write)", "seed": "step index",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_step_median": round(statistics.median(m["times_us"]), 3),
+        "us_per_step_p10_p90": [round(sorted(m["times_us"])[len(m["times_us"]) // 10], 3),
+                                round(sorted(m["times_us"])[(9 * len(m["times_us"])) // 10], 3)],
+        "rows_selected_per_step": round(m["rows"], 1),
+        "algorithmic_bytes_per_step": int(abytes),
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+            "frac_of_8000": round(achieved / 8000.0, 4),
+            "traffic": traffic_for(cfg.name),
+            "kernel": "ssa::unit_kernel (decode: score+select+attend, one launch per step)",
+        },
+        "e2e": {"value": round(e2e_us / world, 3), "unit": UNIT, "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"], "api": "ssa_decode_host (pinned host q in, out/lse back)"},
+        "gpu_launches": args.steps,
+        "clocks": m["clocks"],
+        "wall_s": round(wall, 2),
+    }
+    if rank == 0 and args.secondary:
+        cfg2 = workloads.CONFIGS[args.secondary]
+        del m
+        torch.cuda.empty_cache()
+        steps2 = max(20, min(args.steps, 300))
+        m2 = measure_ours(cfg2, steps2, max(3, min(args.warmup, 10)), dev, with_e2e=False)
+        us2 = statistics.fmean(m2["times_us"])
+        ab2 = algorithmic_bytes(cfg2, m2["rows"])
+        line["secondary"] = {
+            "workload": cfg2.name, "value": round(us2, 3), "unit": UNIT, "steps": steps2,
+            "algorithmic_bytes_per_step": int(ab2), "achieved_gbs": round(ab2 / (us2 * 1e-6) / 1e9, 1),
+            "frac": round(ab2 / (us2 * 1e-6) / 1e9 / peak, 4),
+            "frac_of_8000": round(ab2 / (us2 * 1e-6) / 1e9 / 8000.0, 4),
+            "traffic": traffic_for(cfg2.name), "clocks": m2["clocks"],
+        }
+        del m2
+        torch.cuda.empty_cache()
+        m = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle as it stands, on this host's cores, on a bounded sample of the same workload
+        w = workloads.generate(cfg, 0, dev)
+        import long_context_decode_subset_b300 as ssa
+        Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+        h = host_inputs(w, Ks)
+        del w, Ks
+        times, cores = time_oracle(h, cfg, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": round(statistics.fmean(times) * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} full decode steps of {cfg.name} (all {cfg.units} units), seeds 0..{len(times) - 1}",
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    import workloads
+
+    cfg = workloads.CONFIGS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = workloads.generate(cfg, 0, dev)
+    if dev == "cuda":
+        import long_context_decode_subset_b300 as ssa
+        Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    else:
+        import oracle
+        Ks = torch.from_numpy(oracle.pack_summary(u16(w["K"]), w["sel_ch"].numpy(), cfg.d_sel).view("int16"))
+        Ks = Ks.view(torch.bfloat16)
+    h = host_inputs(w, Ks)
+    del w, Ks
+    import oracle
+    oracle.build()
+    # one untimed step to estimate the cost, then K timed steps within a few minutes:
+    # if K full steps would take too long, each step runs the oracle on a subset of
+    # units and is scaled to the full step.
+    t_est, cores = time_oracle(h, cfg, 0.0, max_steps=1)
+    budget_s = 150.0
+    n_units = cfg.units
+    units_per_step = n_units
+    if t_est[0] * (args.steps + args.warmup) > budget_s:
+        units_per_step = max(1, int(n_units * budget_s / (t_est[0] * (args.steps + args.warmup))))
+    G = cfg.group
+    sub = []
+    for u in range(units_per_step):
+        b, hh = divmod(u, cfg.n_kv_heads)
+        sub.append(dict(q=h["q"][b:b + 1, hh * G:(hh + 1) * G], K=h["K"][b:b + 1, hh:hh + 1],
+                        V=h["V"][b:b + 1, hh:hh + 1], Ks=h["Ks"][b:b + 1, hh:hh + 1], sel=h["sel"][hh:hh + 1]))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if units_per_step == n_units:
+            oracle.decode(h["q"], h["K"], h["V"], h["Ks"], h["sel"], cfg.top_k, cfg.budget, i, cfg.scale,
+                          want_lists=False)
+        else:
+            for s in sub:
+                oracle.decode(s["q"], s["K"], s["V"], s["Ks"], s["sel"], cfg.top_k, cfg.budget, i, cfg.scale,
+                              want_lists=False)
+        dt = (time.perf_counter() - t0) * n_units / units_per_step
+        if i >= args.warmup:
+            times.append(dt)
+    us = statistics.fmean(times) * 1e6
+    sample = (f"full steps (all {n_units} units)" if units_per_step == n_units else
+              f"{units_per_step} of {n_units} units per step, scaled to the full step (one unit per thread at most)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "n_q_heads": cfg.n_q_heads,
+                   "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "ctx_len": cfg.ctx_len,
+                   "d_sel": cfg.d_sel, "top_k": cfg.top_k, "budget": cfg.budget},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "no runnable upstream implementation exists; the reference arm is the CPU oracle (C, OpenMP)",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

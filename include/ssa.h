@@ -1,0 +1,190 @@
+/*
+ * ssa.h -- libssa: Stratified Sparse Attention single-token decode on one
+ * B300 (sm_103a).  Plain C ABI: raw pointers, sizes and a CUDA stream; no
+ * framework types.
+ *
+ * One decode step for every (batch b, KV head h_kv) "unit" has three parts
+ * (sources cited by page title and section):
+ *
+ *  (a) score  -- an approximate score s_i for every cached token i from the
+ *      key summary: a fixed per-KV-head subset of d_sel channels S_ch,
+ *      stored contiguously at append time ("FASA: Frequency-Aware Sparse
+ *      Attention", section 3, Stage 1 "Token Importance Prediction": online
+ *      scoring from the pre-calibrated dominant frequency chunks only).
+ *      The G query heads of a GQA group are combined by max:
+ *          s_i = fl32(scale * max_g sum_j q_g[S_ch[j]] * Ks[i][j]).
+ *  (b) select -- ("Stratified Sparse Attention speeds up decoding 2.96x on a
+ *      1M context", section "How SSA splits the cache into strata") the
+ *      top-k tokens by s (ties to the lower index) are taken
+ *      deterministically (stratum T); every other token j (the remainder R)
+ *      is drawn independently with inclusion probability
+ *          p_j = min(1, B * exp(s_j - m) / sum_{l in R} exp(s_l - m)),
+ *      m = the k-th largest s (the largest when k = 0), the normaliser summed
+ *      exactly and rounded once to fp32, using the uniform
+ *          u_j = (x0 >> 8) * 2^-24,  x0 = word 0 of Philox4x32-10 with
+ *          key (seed & 0xffffffff, seed >> 32), counter (j, h_kv, b, 0)
+ *      (Salmon et al., SC'11); j is selected iff u_j < p_j.  p = 1 on T.
+ *  (c) attend -- exact softmax attention over the selected rows at their
+ *      original positions ("FASA", section 3, Stage 2 "Focused Attention
+ *      Computation"), with the inclusion correction 1/p_i folded into the
+ *      logit as -log p_i so that numerator and denominator are both
+ *      corrected (SSA strata section: the correction recovers the attention
+ *      mass outside the chosen set); split across CTAs and merged through
+ *      the online-softmax state (m, l, acc) ("S2O", technical summary,
+ *      Method section 3).
+ *
+ * Layouts (row-major, element strides; bf16 values are passed as their raw
+ * 16-bit patterns, type ssa_bf16):
+ *   q      [batch][n_q_heads][head_dim]                     contiguous
+ *   K, V   [batch][n_kv_heads][ctx_len][head_dim]           token stride head_dim,
+ *          batch / head strides kv_stride_b / kv_stride_h
+ *   Ks     [batch][n_kv_heads][ctx_len][d_sel]              token stride d_sel,
+ *          batch / head strides ks_stride_b / ks_stride_h
+ *   sel_ch [n_kv_heads][d_sel] int32 channel ids in [0, head_dim)
+ *   s_hat  [batch][n_kv_heads][ctx_len] fp32                contiguous
+ *   idx, p [batch][n_kv_heads][list_cap]  selected token ids (ascending) and
+ *          their inclusion probabilities; count [batch][n_kv_heads] int32
+ *   out    [batch][n_q_heads][head_dim] fp32;  lse [batch][n_q_heads] fp32
+ *          (natural log of the corrected softmax denominator; -inf and a
+ *          zero output when nothing is selected)
+ * Query head g of KV head h_kv is q head h_kv * G + g, G = n_q_heads / n_kv_heads.
+ *
+ * Supported: head_dim in {64, 128}; d_sel in {16, 32} (d_sel <= head_dim);
+ * G in {1, 2, 4, 8}; 0 <= ctx_len < 2^31; top_k >= 0; budget >= 0 or +inf
+ * (+inf: every token is kept with p = 1, i.e. dense attention).
+ * Alignment: q, K, V, Ks and the workspace must be 16-byte aligned (the
+ * workspace 256-byte aligned) and kv/ks strides multiples of 8 elements.
+ *
+ * Memory and ownership: every buffer, the workspace included, is allocated
+ * and owned by the caller.  Device pointers unless stated otherwise.  The
+ * library allocates no device memory and keeps no state between calls;
+ * calls on different streams need different workspaces.
+ *
+ * Errors: every entry point validates its arguments on the host and returns
+ * a status before launching anything.  All launches are asynchronous on the
+ * given stream.  Problems only the device can see (a non-finite score, a
+ * list longer than list_cap, an index out of range, a wait that timed out)
+ * set bits in a status word inside the workspace; ssa_get_device_status()
+ * synchronises the stream, reads and clears them.
+ */
+#ifndef LIBSSA_SSA_H
+#define LIBSSA_SSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ssa_bf16; /* raw bfloat16 bit pattern */
+
+typedef enum {
+    SSA_OK = 0,
+    SSA_ERR_INVALID_ARG = 1,     /* null pointer, bad size, bad stride, bad scalar */
+    SSA_ERR_UNSUPPORTED = 2,     /* head_dim / d_sel / group size not built */
+    SSA_ERR_WORKSPACE = 3,       /* workspace too small or misaligned */
+    SSA_ERR_CUDA = 4,            /* a CUDA runtime call failed (no device, launch error) */
+    SSA_ERR_OVERFLOW = 5,        /* device: a unit selected more than list_cap rows */
+    SSA_ERR_NONFINITE = 6,       /* device: a score was NaN or infinite */
+    SSA_ERR_DEVICE_TIMEOUT = 7,  /* device: an asynchronous copy did not arrive in time */
+    SSA_ERR_BAD_INDEX = 8        /* device: a selected index or summary channel out of range */
+} ssa_status;
+
+/* Device status bits (ssa_get_device_status). */
+#define SSA_DEV_NONFINITE 0x1u
+#define SSA_DEV_OVERFLOW 0x2u
+#define SSA_DEV_TIMEOUT 0x4u
+#define SSA_DEV_BAD_INDEX 0x8u
+
+typedef struct {
+    int32_t batch;        /* B_t >= 0 */
+    int32_t n_q_heads;    /* H_q, a multiple of n_kv_heads */
+    int32_t n_kv_heads;   /* H_kv >= 1 */
+    int32_t head_dim;     /* d: 64 or 128 */
+    int32_t d_sel;        /* summary channels: 16 or 32 */
+    int32_t reserved;     /* must be 0 */
+    int64_t ctx_len;      /* N: cached tokens, all visible */
+    int64_t kv_stride_b;  /* K/V elements between batches (>= n_kv_heads*kv_stride_h) */
+    int64_t kv_stride_h;  /* K/V elements between KV heads (>= ctx_len*head_dim) */
+    int64_t ks_stride_b;  /* Ks elements between batches */
+    int64_t ks_stride_h;  /* Ks elements between KV heads (>= ctx_len*d_sel) */
+} ssa_shape;
+
+/* Human-readable name of a status code (static string). */
+const char* ssa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int ssa_version(void);
+
+/* Bytes of device workspace every entry point below needs for this shape
+ * and list capacity (list_cap <= 0 means ctx_len).  Independent of the
+ * stream; 0 on invalid input. */
+size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap);
+
+/* Append-time key summary (step a0): Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]]
+ * for all i < ctx_len.  An out-of-range channel sets SSA_DEV_BAD_INDEX (the
+ * channel is clamped).  Not part of the timed step. */
+ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* Ks,
+                            void* ws, size_t ws_bytes, const ssa_shape* shape,
+                            cudaStream_t stream);
+
+/* Step (a): s_hat[b][h][i] for every token (FASA section 3, Stage 1). */
+ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_ch, float scale,
+                     float* s_hat, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                     cudaStream_t stream);
+
+/* Step (b): stratified selection from given scores.  Writes idx / p (the
+ * first count[u] entries of each unit's row of length list_cap, ascending
+ * token order) and count.  A unit whose count exceeds list_cap keeps the
+ * first list_cap entries and sets SSA_DEV_OVERFLOW; count still holds the
+ * true number. */
+ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t seed,
+                      int32_t* idx, float* p, int32_t* count, int64_t list_cap,
+                      void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
+
+/* Step (c): corrected attention over given selections (rows idx[u][0..min(count[u],
+ * list_cap)) with probabilities p > 0). */
+ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                      const int32_t* idx, const float* p, const int32_t* count, int64_t list_cap,
+                      float scale, float* out, float* lse,
+                      void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
+
+/* The whole step, (a) -> (b) -> (c), as one launch.  s_hat_opt, idx_opt,
+ * p_opt, count_opt may be NULL; when given they receive the intermediate
+ * results (idx_opt / p_opt need list_cap entries per unit). */
+ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                      const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
+                      uint64_t seed, float scale, float* out, float* lse,
+                      float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
+                      int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                      cudaStream_t stream);
+
+/* ssa_decode with the step's query read from, and its result written to,
+ * HOST memory (pinned for asynchrony): copies q_host to a device staging
+ * area inside the workspace, runs the step, and copies out / lse back to
+ * out_host / lse_host, all enqueued on `stream`.  The caller synchronises.
+ * The KV cache (K, V, Ks, sel_ch) stays resident on the device. */
+ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_bf16* V,
+                           const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
+                           uint64_t seed, float scale, float* out_host, float* lse_host,
+                           void* ws, size_t ws_bytes, const ssa_shape* shape,
+                           cudaStream_t stream);
+
+/* Synchronises `stream`, ORs the device status bits (SSA_DEV_*) into
+ * *flags_out (may be NULL), clears them, and returns the status code of the
+ * most serious one (SSA_OK if none). */
+ssa_status ssa_get_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);
+
+/* Launch geometry the library would use for a shape: CTAs per unit (the
+ * thread-block cluster size), whether the unit's scores stay in shared
+ * memory, and the dynamic shared memory per CTA.  For tests and tuning. */
+ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* cluster_size, int32_t* scores_resident,
+                          int32_t* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSSA_SSA_H */

@@ -1,0 +1,122 @@
+"""The C-ABI library loads, exports every symbol include/ssa.h declares, and
+rejects bad arguments on the host (no GPU needed: validation precedes any
+CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import long_context_decode_subset_b300 as ssa
+from long_context_decode_subset_b300 import ssa as binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ssa.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", ssa.LIB_PATH], capture_output=True, text=True).stdout
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), f"{name} not exported"
+
+
+def test_library_is_built_for_sm_103a():
+    out = subprocess.run(["cuobjdump", "--list-elf", ssa.LIB_PATH], capture_output=True, text=True).stdout
+    assert "sm_103a" in out
+
+
+def test_status_strings_and_version():
+    lib = ssa.load_library()
+    assert lib.ssa_status_string(0) == b"ok"
+    assert lib.ssa_status_string(3).startswith(b"workspace")
+    assert ssa.ssa_version() >= 100
+
+
+def _shape(**kw):
+    base = dict(batch=2, n_q_heads=32, n_kv_heads=8, head_dim=128, d_sel=32, ctx_len=4096)
+    base.update(kw)
+    return ssa.make_shape(**base)
+
+
+def test_workspace_bytes():
+    s = _shape()
+    n = ssa.ssa_workspace_bytes(s)
+    units, N = 16, 4096
+    assert n >= units * N * 4 * 3
+    assert ssa.ssa_workspace_bytes(s, 100) < n
+    assert ssa.ssa_workspace_bytes(_shape(head_dim=96)) == 0
+    assert ssa.ssa_workspace_bytes(_shape(n_q_heads=24)) == 0      # G = 3
+    assert ssa.ssa_workspace_bytes(_shape(ctx_len=-1)) == 0
+
+
+P = ctypes.c_void_p
+
+
+def _decode(lib, shape, **over):
+    fake = 1 << 20  # never dereferenced: every call below must fail validation first
+    args = dict(q=fake, K=fake, V=fake, Ks=fake, sel=fake, k=10, B=10.0, seed=0, scale=0.1, out=fake, lse=fake,
+                ws=fake, ws_bytes=1 << 40)
+    args.update(over)
+    return lib.ssa_decode(P(args["q"]), P(args["K"]), P(args["V"]), P(args["Ks"]), P(args["sel"]), args["k"],
+                          args["B"], args["seed"], args["scale"], P(args["out"]), P(args["lse"]), None, None, None,
+                          None, 0, P(args["ws"]), args["ws_bytes"], ctypes.byref(shape), None)
+
+
+def test_decode_validation_statuses():
+    lib = ssa.load_library()
+    s = _shape()
+    assert _decode(lib, s, q=0) == 1
+    assert _decode(lib, s, k=-1) == 1
+    assert _decode(lib, s, B=-1.0) == 1
+    assert _decode(lib, s, B=float("nan")) == 1
+    assert _decode(lib, s, scale=0.0) == 1
+    assert _decode(lib, s, K=(1 << 20) + 2) == 1                    # misaligned
+    assert _decode(lib, _shape(head_dim=80)) == 2
+    assert _decode(lib, _shape(d_sel=24)) == 2
+    assert _decode(lib, _shape(n_q_heads=48, n_kv_heads=4)) == 2   # G = 12
+    assert _decode(lib, s, ws_bytes=1000) == 3
+    assert _decode(lib, s, ws=(1 << 20) + 16) == 3                  # workspace not 256-aligned
+    bad = _shape()
+    bad.kv_stride_h = 100
+    assert _decode(lib, bad) == 1
+    bad = _shape()
+    bad.reserved = 1
+    assert _decode(lib, bad) == 1
+
+
+def test_other_entry_points_validate():
+    lib = ssa.load_library()
+    s = _shape()
+    f = P(1 << 20)
+    cap = 0
+    assert lib.ssa_select(None, 5, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_select(f, -5, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_select(f, 5, 1.0, 0, f, f, f, cap, f, 16, ctypes.byref(s), None) == 3
+    assert lib.ssa_score(f, f, f, 0.1, None, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_score(f, f, f, float("inf"), f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_attend(f, f, f, f, f, None, cap, 0.1, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_pack_summary(None, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_decode_host(None, f, f, f, f, 5, 1.0, 0, 0.1, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_get_device_status(None, None, None) == 3
+    assert lib.ssa_query_plan(None, None, None, None) == 1
+
+
+def test_binding_requires_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        binding.load_library()

@@ -1,0 +1,140 @@
+"""GPU end-to-end decode parity at small sizes, every plan, and the special
+cases the pages name (dense limit, pure top-k, uniform hybrid)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_decode_subset_b300 as ssa
+import workloads
+from gpu_e2e import check_unit, gpu_decode
+from test_gpu_stages import SMALL, case, oracle_inputs, plan_env
+from _util import u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("plan", [(None, False), (1, False), (4, True), (16, False)])
+def test_decode_parity(oracle_mod, name, plan):
+    w = case(name)
+    cfg = w["cfg"]
+    with plan_env(*plan):
+        g = gpu_decode(w, cfg.top_k, cfg.budget, 1)
+    assert g["status"] == 0, hex(g["flags"])
+    stats = {}
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            check_unit(oracle_mod, w, g, b, h, cfg.top_k, cfg.budget, 1, stats)
+    assert stats.get("units_differing", 0) <= max(1, stats["units"] // 8), stats
+
+
+@pytest.mark.parametrize("name", ["tiny", "g4_d128", "g8_d128"])
+def test_dense_limit_equals_dense_attention(oracle_mod, name):
+    w = case(name)
+    cfg = w["cfg"]
+    g = gpu_decode(w, cfg.top_k, math.inf, 0)
+    q, K, V, Ks, sel = oracle_inputs(w)
+    d_out, d_lse = oracle_mod.dense_attention(q, K, V, cfg.scale)
+    assert np.all(g["count"].cpu().numpy() == cfg.ctx_len)
+    assert np.allclose(g["out"].cpu().numpy(), d_out, atol=2e-3, rtol=2e-3)
+    assert np.allclose(g["lse"].cpu().numpy(), d_lse, atol=2e-3, rtol=2e-3)
+
+
+def test_budget_zero_is_pure_topk(oracle_mod):
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    g = gpu_decode(w, cfg.top_k, 0.0, 0)
+    assert np.all(g["count"].cpu().numpy() == cfg.top_k)
+    assert torch.all(g["p"][..., :cfg.top_k] == 1.0)
+    stats = {}
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            check_unit(oracle_mod, w, g, b, h, cfg.top_k, 0.0, 0, stats)
+
+
+def test_zero_query_on_summary_is_uniform_hybrid(oracle_mod):
+    w = dict(case("g4_d128"))
+    cfg = w["cfg"]
+    q = w["q"].clone()
+    G = cfg.group
+    for h in range(cfg.n_kv_heads):
+        q[:, h * G:(h + 1) * G, w["sel_ch"][h].long()] = 0
+    w["q"] = q
+    g = gpu_decode(w, cfg.top_k, cfg.budget, 2)
+    assert torch.all(g["s_hat"] == 0)
+    N, k = cfg.ctx_len, cfg.top_k
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            n = int(g["count"][b, h])
+            idx = g["idx"][b, h, :n].cpu().numpy()
+            p = g["p"][b, h, :n].cpu().numpy()
+            assert set(range(k)) <= set(idx.tolist())
+            assert np.all(p[idx >= k] == np.float32(cfg.budget) / np.float32(N - k))
+    stats = {}
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            check_unit(oracle_mod, w, g, b, h, k, cfg.budget, 2, stats)
+
+
+def test_k_at_least_n_and_empty_context(oracle_mod):
+    w = case("tiny")
+    cfg = w["cfg"]
+    g = gpu_decode(w, cfg.ctx_len + 3, 5.0, 0)
+    assert int(g["count"][0, 0]) == cfg.ctx_len
+    q, K, V, Ks, sel = oracle_inputs(w)
+    d_out, d_lse = oracle_mod.dense_attention(q, K, V, cfg.scale)
+    assert np.allclose(g["out"].cpu().numpy(), d_out, atol=2e-3, rtol=2e-3)
+    # N = 0: nothing to attend to
+    K0 = w["K"][:, :, :0]
+    Ks0 = w["Ks"][:, :, :0]
+    out, lse = ssa.ssa_decode(w["q"], K0, K0, Ks0, w["sel_ch"], 3, 3.0, 0, cfg.scale)
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_decode_is_deterministic_and_seed_dependent():
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    a = gpu_decode(w, cfg.top_k, cfg.budget, 42)
+    b = gpu_decode(w, cfg.top_k, cfg.budget, 42)
+    c = gpu_decode(w, cfg.top_k, cfg.budget, 43)
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["idx"], b["idx"]) and torch.equal(a["lse"], b["lse"])
+    assert not torch.equal(a["idx"], c["idx"])
+
+
+def test_decode_host_matches_device_path():
+    w = case("g8_d128")
+    cfg = w["cfg"]
+    g = gpu_decode(w, cfg.top_k, cfg.budget, 9)
+    q_host = w["q"].cpu().pin_memory()
+    out_h = torch.empty(g["out"].shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(g["lse"].shape, dtype=torch.float32).pin_memory()
+    shape = ssa.shape_of(w["q"], w["K"], w["Ks"])
+    ws = ssa.workspace(shape)
+    ssa.ssa_decode_host(q_host, w["K"], w["V"], w["Ks"], w["sel_ch"], cfg.top_k, cfg.budget, 9, cfg.scale,
+                        out_h, lse_h, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, g["out"].cpu()) and torch.equal(lse_h, g["lse"].cpu())
+
+
+def test_strided_cache_layout(oracle_mod):
+    # K / V / Ks inside larger caches (capacity > N): batch and head strides differ from the packed ones
+    w = case("g1_d64")
+    cfg = w["cfg"]
+    cap_tokens = cfg.ctx_len + 77 * 8
+    Bt, Hkv, N, d = w["K"].shape
+    bigK = torch.zeros((Bt, Hkv, cap_tokens, d), dtype=torch.bfloat16, device=DEV)
+    bigV = torch.zeros_like(bigK)
+    bigK[:, :, :N] = w["K"]
+    bigV[:, :, :N] = w["V"]
+    K = bigK[:, :, :N]
+    V = bigV[:, :, :N]
+    bigKs = torch.zeros((Bt, Hkv, cap_tokens, cfg.d_sel), dtype=torch.bfloat16, device=DEV)
+    Ks = bigKs[:, :, :N]
+    ssa.ssa_pack_summary(K, w["sel_ch"], Ks=Ks)
+    assert torch.equal(Ks, w["Ks"])
+    ref = gpu_decode(w, cfg.top_k, cfg.budget, 4)
+    out, lse = ssa.ssa_decode(w["q"], K, V, Ks, w["sel_ch"], cfg.top_k, cfg.budget, 4, cfg.scale)
+    assert torch.equal(out, ref["out"]) and torch.equal(lse, ref["lse"])

@@ -1,0 +1,210 @@
+"""GPU parity, stage by stage, against the CPU oracle (small sizes that span
+several tiles, ragged tails and every cluster size).
+
+Tolerances:
+  * pack: bit-exact.
+  * score: |s_gpu - s_oracle| <= 1e-5 * scale * max_g sum_j |q_g[S_j] Ks_ij|
+    (fp32 accumulation vs. the oracle's double; the plain relative form fails
+    where s ~ 0).
+  * select (given the oracle's scores): index sets identical except tokens
+    with |u - p| <= 1e-6 (expf vs. a correctly rounded exp may move p by an
+    ulp or two); p within 4 ulp.
+  * attend (given the oracle's lists): out and lse within 2e-3 abs + 2e-3 rel.
+"""
+import contextlib
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_decode_subset_b300 as ssa
+import workloads
+from _util import compare_unit_lists, score_bound, u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@contextlib.contextmanager
+def plan_env(cluster=None, global_scores=False):
+    old = {k: os.environ.get(k) for k in ("SSA_FORCE_CLUSTER", "SSA_FORCE_GLOBAL_SCORES")}
+    if cluster:
+        os.environ["SSA_FORCE_CLUSTER"] = str(cluster)
+    else:
+        os.environ.pop("SSA_FORCE_CLUSTER", None)
+    if global_scores:
+        os.environ["SSA_FORCE_GLOBAL_SCORES"] = "1"
+    else:
+        os.environ.pop("SSA_FORCE_GLOBAL_SCORES", None)
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+SMALL = {
+    "tiny": workloads.CONFIGS["tiny"],
+    "g4_d128": workloads.make_config("ministral8b_32k", batch=2, n_q_heads=8, n_kv_heads=2, ctx_len=5000,
+                                     top_k=50, budget=50.0, n_needles=8),
+    "g8_d128": workloads.make_config("ministral8b_32k", batch=1, n_q_heads=16, n_kv_heads=2, ctx_len=3001,
+                                     top_k=30, budget=31.0, n_needles=4),
+    "g1_d64": workloads.make_config("ministral8b_32k", batch=2, n_q_heads=2, n_kv_heads=2, head_dim=64,
+                                    ctx_len=1500, top_k=20, budget=20.0, n_needles=4),
+    "g2_d128_s16": workloads.make_config("27b_128k_50x", batch=1, n_q_heads=4, n_kv_heads=2, ctx_len=4100,
+                                         d_sel=16, top_k=41, budget=41.0, n_needles=4),
+    "g8_d64_s16": workloads.make_config("ministral8b_32k", batch=1, n_q_heads=8, n_kv_heads=1, head_dim=64,
+                                        d_sel=16, ctx_len=2600, top_k=26, budget=26.0, n_needles=4),
+}
+
+_cache = {}
+
+
+def case(name, seed=0):
+    key = (name, seed)
+    if key not in _cache:
+        cfg = SMALL[name]
+        w = workloads.generate(cfg, seed, DEV)
+        w["Ks"] = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+        torch.cuda.synchronize()
+        _cache[key] = w
+    return _cache[key]
+
+
+def oracle_inputs(w):
+    return u16(w["q"]), u16(w["K"]), u16(w["V"]), u16(w["Ks"]), w["sel_ch"].cpu().numpy()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_pack_summary_bit_exact(oracle_mod, name):
+    w = case(name)
+    cfg = w["cfg"]
+    want = oracle_mod.pack_summary(u16(w["K"]), w["sel_ch"].cpu().numpy(), cfg.d_sel)
+    assert np.array_equal(u16(w["Ks"]), want)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_score_parity(oracle_mod, name):
+    w = case(name)
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    s_gpu = ssa.ssa_score(w["q"], w["Ks"], w["sel_ch"], cfg.scale).cpu().numpy()
+    s_ora = oracle_mod.score(q, Ks, sel, cfg.scale)
+    tol = score_bound(q, Ks, sel, cfg.scale)
+    assert np.all(np.abs(s_gpu - s_ora) <= tol), np.max(np.abs(s_gpu - s_ora) / tol)
+
+
+def _select_and_compare(oracle_mod, s_np, k, B, seed, cluster=None, global_scores=False, cap=None):
+    s = torch.from_numpy(s_np).to(DEV)
+    Bt, Hkv, N = s_np.shape
+    with plan_env(cluster, global_scores):
+        idx, p, count = ssa.ssa_select(s, k, B, seed, list_cap=cap or 0)
+        ws = None
+    torch.cuda.synchronize()
+    idx, p, count = idx.cpu().numpy(), p.cpu().numpy(), count.cpu().numpy()
+    nb = 0
+    for b in range(Bt):
+        for h in range(Hkv):
+            o_idx, o_p, m, Z, p_all = oracle_mod.select_unit(s_np[b, h], k, B, seed, b, h, want_p_all=True)
+            n = int(count[b, h])
+            nd, _ = compare_unit_lists(idx[b, h, :n], p[b, h, :n], o_idx, o_p, p_all,
+                                       lambda j: oracle_mod.uniform(seed, j, h, b))
+            nb += nd
+            assert np.all(np.diff(idx[b, h, :n]) > 0), "selection not in ascending token order"
+    return nb
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("global_scores", [False, True])
+def test_select_parity_cluster_sizes(oracle_mod, cluster, global_scores):
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
+    nb = _select_and_compare(oracle_mod, s_np, cfg.top_k, cfg.budget, 7, cluster, global_scores)
+    assert nb <= 2
+
+
+@pytest.mark.parametrize("cluster", [1, 4, 16])
+def test_select_edge_cases(oracle_mod, cluster):
+    rng = np.random.default_rng(11)
+    Bt, Hkv = 1, 2
+    for N, k, B, kind in [
+        (3000, 40, 40.0, "ties"),            # heavy exact ties at the threshold
+        (3000, 40, 40.0, "constant"),        # uniform hybrid: all scores equal
+        (2500, 0, 30.0, "normal"),           # no top-k stratum: m = max
+        (2500, 25, 0.0, "normal"),           # pure top-k
+        (2500, 25, math.inf, "normal"),      # dense limit
+        (700, 700, 10.0, "normal"),          # k >= N
+        (700, 699, 10.0, "normal"),          # k = N - 1
+        (1, 0, 5.0, "normal"),               # single token
+        (513, 5, 5.0, "signed_zero"),        # -0 / +0 ordering
+        (4097, 60, 1e6, "normal"),           # clipping: most p = 1
+        (2000, 30, 30.0, "wide"),            # scores spanning many octaves
+    ]:
+        if kind == "ties":
+            s = np.round(rng.standard_normal((Bt, Hkv, N)) * 2) / 4
+        elif kind == "constant":
+            s = np.full((Bt, Hkv, N), 0.375)
+        elif kind == "signed_zero":
+            s = np.where(rng.random((Bt, Hkv, N)) < 0.5, 0.0, -0.0) * np.ones((Bt, Hkv, N))
+            s[..., ::7] = rng.standard_normal(s[..., ::7].shape)
+        elif kind == "wide":
+            s = rng.standard_normal((Bt, Hkv, N)) * np.exp2(rng.integers(-20, 6, (Bt, Hkv, N)))
+        else:
+            s = rng.standard_normal((Bt, Hkv, N)) * 1.5
+        s = s.astype(np.float32)
+        nb = _select_and_compare(oracle_mod, s, k, B, 3, cluster)
+        assert nb <= 2, (N, k, B, kind)
+
+
+def test_select_overflow_flag(oracle_mod):
+    s = torch.zeros((1, 1, 1000), device=DEV)
+    idx, p, count = ssa.ssa_select(s, 100, math.inf, 0, list_cap=10)
+    shape = ssa.make_shape(1, 1, 1, 64, 16, 1000)
+    # the binding allocated its own workspace; re-run with one we can inspect
+    ws = ssa.workspace(shape, 10)
+    idx2, p2, c2 = ssa.ssa_select(s, 100, math.inf, 0, idx=idx, p=p, count=count, list_cap=10, ws=ws)
+    st, flags = ssa.ssa_get_device_status(ws)
+    assert flags & ssa.ssa.DEV_OVERFLOW and st == 5
+    assert int(c2[0, 0]) == 1000 and idx2[0, 0].tolist() == list(range(10))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("cluster", [None, 1, 8])
+def test_attend_parity(oracle_mod, name, cluster):
+    w = case(name)
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    r = oracle_mod.decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, 5, cfg.scale)
+    idx = torch.from_numpy(r["idx"]).to(DEV)
+    p = torch.from_numpy(r["p"]).to(DEV)
+    count = torch.from_numpy(r["count"].astype(np.int32)).to(DEV)
+    with plan_env(cluster):
+        out, lse = ssa.ssa_attend(w["q"], w["K"], w["V"], idx, p, count, cfg.scale)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.allclose(out, r["out"], atol=2e-3, rtol=2e-3), np.abs(out - r["out"]).max()
+    assert np.allclose(lse, r["lse"], atol=2e-3, rtol=2e-3), np.abs(lse - r["lse"]).max()
+
+
+def test_attend_empty_and_dense(oracle_mod):
+    w = case("tiny")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    N = cfg.ctx_len
+    idx = torch.arange(N, dtype=torch.int32, device=DEV).view(1, 1, N)
+    p = torch.ones((1, 1, N), device=DEV)
+    count = torch.tensor([[N]], dtype=torch.int32, device=DEV)
+    out, lse = ssa.ssa_attend(w["q"], w["K"], w["V"], idx, p, count, cfg.scale)
+    d_out, d_lse = oracle_mod.dense_attention(q, K, V, cfg.scale)
+    assert np.allclose(out.cpu().numpy(), d_out, atol=2e-3, rtol=2e-3)
+    assert np.allclose(lse.cpu().numpy(), d_lse, atol=2e-3, rtol=2e-3)
+    count.zero_()
+    out, lse = ssa.ssa_attend(w["q"], w["K"], w["V"], idx, p, count, cfg.scale)
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
