@@ -55,6 +55,8 @@
  * Alignment: q, K, V, Ks and the workspace must be 16-byte aligned (the
  * workspace 256-byte aligned) and kv/ks strides multiples of 8 elements.
  *
+ * K, V and Ks may be NULL when ctx_len == 0 (nothing is read).
+ *
  * Memory and ownership: every buffer, the workspace included, is allocated
  * and owned by the caller.  Device pointers unless stated otherwise.  The
  * library allocates no device memory and keeps no state between calls;

@@ -416,7 +416,7 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
 {
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    if (!q || !K || !V || !idx || !p || !count || !out || !lse) return SSA_ERR_INVALID_ARG;
+    if (!q || !idx || !p || !count || !out || !lse || (shape->ctx_len > 0 && (!K || !V))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
     if ((st = check_ws(ws, ws_bytes, *shape, list_cap)) != SSA_OK) return st;
@@ -441,7 +441,8 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
 {
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    if (!q || !K || !V || !Ks || !sel_ch || !out || !lse) return SSA_ERR_INVALID_ARG;
+    const bool empty = shape->ctx_len == 0;  // nothing is read from the cache
+    if (!q || !sel_ch || !out || !lse || (!empty && (!K || !V || !Ks))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget) || bad_scale(scale)) return SSA_ERR_INVALID_ARG;
     if ((st = check_ws(ws, ws_bytes, *shape, list_cap)) != SSA_OK) return st;
