@@ -174,6 +174,35 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
                            void* ws, size_t ws_bytes, const ssa_shape* shape,
                            cudaStream_t stream);
 
+/* Size of the library's built-in scratch array used by ssa_decode_static. */
+#define SSA_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* ssa_decode for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is a deployment convenience, not part of the
+ * method.)  Some callers own no allocator: an inference engine that reserves
+ * all HBM for its KV cache when it starts and forbids allocation inside the
+ * decode loop, or a plugin interface that hands over inputs and outputs but
+ * no workspace.  For them this entry point takes the same inputs and
+ * outputs as ssa_decode but no workspace: its scratch is one static array of
+ * SSA_STATIC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - Shapes whose scratch (ssa_workspace_bytes(shape, 0)) exceeds the array
+ *     are rejected with SSA_ERR_WORKSPACE before anything is enqueued.
+ *   - All calls share the one array and it keeps the previous call's
+ *     contents; each call clears the status word it needs.  Calls that
+ *     overlap on the GPU (different streams, or different host threads on
+ *     the same device) race on the array: serialise them.
+ *   - device_flags (device memory, may be NULL) receives this call's device
+ *     status bits (SSA_DEV_*), written on `stream` after the step. */
+ssa_status ssa_decode_static(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                             const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
+                             uint64_t seed, float scale, float* out, float* lse,
+                             uint32_t* device_flags, const ssa_shape* shape, cudaStream_t stream);
+
 /* Synchronises `stream`, ORs the device status bits (SSA_DEV_*) into
  * *flags_out (may be NULL), clears them, and returns the status code of the
  * most serious one (SSA_OK if none). */

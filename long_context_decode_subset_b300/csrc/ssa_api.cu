@@ -323,6 +323,36 @@ bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
 
 }  // namespace
 
+// Scratch for ssa_decode_static: one array per GPU that loads the library.
+// Host code must not use its name as a device address; the address comes
+// from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[SSA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+void* static_scratch_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    static std::mutex mu;
+    static std::map<int, void*> addr;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    addr[dev] = ptr;
+    return ptr;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* ssa_status_string(int status)
@@ -494,6 +524,32 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     if (cudaMemcpyAsync(out_host, out_dev, heads * shape->head_dim * 4, cudaMemcpyDeviceToHost, stream) !=
             cudaSuccess ||
         cudaMemcpyAsync(lse_host, lse_dev, heads * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSA_ERR_CUDA;
+    }
+    return SSA_OK;
+}
+
+ssa_status ssa_decode_static(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
+                             const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale,
+                             float* out, float* lse, uint32_t* device_flags, const ssa_shape* shape,
+                             cudaStream_t stream)
+{
+    const ssa_status st = check_shape(shape);
+    if (st != SSA_OK) return st;
+    if (ws_layout(*shape, 0).total > (size_t)SSA_STATIC_SCRATCH_BYTES) return SSA_ERR_WORKSPACE;
+    void* ws = static_scratch_address();
+    if (!ws) return SSA_ERR_CUDA;
+    // the status word accumulates device flags: start this call from zero
+    if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSA_ERR_CUDA;
+    }
+    const ssa_status rc = ssa_decode(q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, nullptr, nullptr,
+                                     nullptr, nullptr, 0, ws, (size_t)SSA_STATIC_SCRATCH_BYTES, shape, stream);
+    if (rc != SSA_OK) return rc;
+    if (device_flags &&
+        cudaMemcpyAsync(device_flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
         cudaGetLastError();
         return SSA_ERR_CUDA;
     }

@@ -28,7 +28,7 @@ DEV_NONFINITE, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8
 EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
-    "ssa_query_plan",
+    "ssa_query_plan", "ssa_decode_static",
 ]
 
 
@@ -74,6 +74,7 @@ def load_library():
         "ssa_decode_host": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
         "ssa_query_plan": ([SP, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], ctypes.c_int),
+        "ssa_decode_static": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, SP, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
