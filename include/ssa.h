@@ -19,8 +19,12 @@
  *      deterministically (stratum T); every other token j (the remainder R)
  *      is drawn independently with inclusion probability
  *          p_j = min(1, B * exp(s_j - m) / sum_{l in R} exp(s_l - m)),
- *      m = the k-th largest s (the largest when k = 0), the normaliser summed
- *      exactly and rounded once to fp32, using the uniform
+ *      computed in fp32 as min(1, fl32(fl32(B * e_j) / Z)) with
+ *      e_j = fl32(expf(fl32(s_j - m))) and Z the sum over R of e_j (summed
+ *      with compensated arithmetic in a fixed order, rounded once); p does
+ *      not depend on m, which is the lower edge of the 12-bit order-key
+ *      bucket holding the k-th largest s (the largest when k = 0); using
+ *      the uniform
  *          u_j = (x0 >> 8) * 2^-24,  x0 = word 0 of Philox4x32-10 with
  *          key (seed & 0xffffffff, seed >> 32), counter (j, h_kv, b, 0)
  *      (Salmon et al., SC'11); j is selected iff u_j < p_j.  p = 1 on T.
@@ -50,7 +54,7 @@
  * Query head g of KV head h_kv is q head h_kv * G + g, G = n_q_heads / n_kv_heads.
  *
  * Supported: head_dim in {64, 128}; d_sel in {16, 32} (d_sel <= head_dim);
- * G in {1, 2, 4, 8}; 0 <= ctx_len < 2^31; top_k >= 0; budget >= 0 or +inf
+ * G in {1, 2, 4, 8}; 0 <= ctx_len <= 2^31 - 4097; top_k >= 0; budget >= 0 or +inf
  * (+inf: every token is kept with p = 1, i.e. dense attention).
  * Alignment: q, K, V, Ks and the workspace must be 16-byte aligned (the
  * workspace 256-byte aligned) and kv/ks strides multiples of 8 elements.
@@ -59,7 +63,8 @@
  *
  * Memory and ownership: every buffer, the workspace included, is allocated
  * and owned by the caller.  Device pointers unless stated otherwise.  The
- * library allocates no device memory and keeps no state between calls;
+ * library allocates no device memory and keeps no state between calls (the
+ * workspace needs no initialisation: each call resets what it uses);
  * calls on different streams need different workspaces.
  *
  * Errors: every entry point validates its arguments on the host and returns
@@ -121,8 +126,10 @@ const char* ssa_status_string(int status);
 int ssa_version(void);
 
 /* Bytes of device workspace every entry point below needs for this shape
- * and list capacity (list_cap <= 0 means ctx_len).  Independent of the
- * stream; 0 on invalid input. */
+ * (about 21 bytes per cached token plus 32 KB per unit: scores, candidate
+ * and selection lists sized for the worst case, Philox bytes, histograms).
+ * Independent of the stream, the device and list_cap (kept for symmetry with
+ * the calls that take a list capacity); 0 on invalid input. */
 size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap);
 
 /* Append-time key summary (step a0): Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]]
@@ -153,9 +160,13 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       float scale, float* out, float* lse,
                       void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
 
-/* The whole step, (a) -> (b) -> (c), as one launch.  s_hat_opt, idx_opt,
+/* The whole step, (a) -> (b) -> (c), enqueued on `stream` as a chain of
+ * kernels (initialise, score, threshold bucket, decide, attend; each after
+ * the first is a programmatic dependent launch).  s_hat_opt, idx_opt,
  * p_opt, count_opt may be NULL; when given they receive the intermediate
- * results (idx_opt / p_opt need list_cap entries per unit). */
+ * results (idx_opt / p_opt need list_cap entries per unit and are given
+ * together).  A step that selects every token (top_k >= ctx_len or
+ * budget = +inf) skips the selection kernels. */
 ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
                       uint64_t seed, float scale, float* out, float* lse,
@@ -208,11 +219,12 @@ ssa_status ssa_decode_static(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
  * most serious one (SSA_OK if none). */
 ssa_status ssa_get_device_status(void* ws, cudaStream_t stream, uint32_t* flags_out);
 
-/* Launch geometry the library would use for a shape: CTAs per unit (the
- * thread-block cluster size), whether the unit's scores stay in shared
- * memory, and the dynamic shared memory per CTA.  For tests and tuning. */
-ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* cluster_size, int32_t* scores_resident,
-                          int32_t* smem_bytes);
+/* Launch geometry the library would use for a shape on the current device:
+ * CTAs of the (persistent) score kernel, selection tiles per unit, and
+ * attention CTAs per unit.  Any output pointer may be NULL.  For tests and
+ * tuning. */
+ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* tiles_per_unit,
+                          int32_t* attend_ctas_per_unit);
 
 #ifdef __cplusplus
 }

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libssa.so")
 SOURCES = ["ssa_api.cu"]
-DEPS = ["ssa_api.cu", "kernels.cuh", "ptx.cuh"]
+DEPS = ["ssa_api.cu", "common.cuh", "k_score.cuh", "k_select.cuh", "k_attend.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -1,0 +1,408 @@
+// k_attend.cuh -- K3: exact softmax attention over the selected rows with
+// the inclusion correction.
+//
+// Sources (page title, section):
+//  * "FASA: Frequency-Aware Sparse Attention", section 3, Stage 2 "Focused
+//    Attention Computation": full-precision attention over the selected
+//    tokens only, at their original positions.
+//  * "Stratified Sparse Attention speeds up decoding 2.96x on a 1M context",
+//    section "How SSA splits the cache into strata": each selected token is
+//    corrected by its inclusion probability; here the weight 1/p_i enters the
+//    logit as -log p_i, so numerator and denominator are both corrected:
+//        l_i = scale * q_g . K_i - log p_i,   o_g = sum_i softmax(l)_i V_i.
+//  * "S2O" (online permutation and early stopping), technical summary,
+//    Method section 1: rows are gathered by index arrays, the physical layout
+//    in HBM is kept; section 3: the online-softmax state (m, l, acc), merged
+//    across splits.
+//
+// P CTAs per unit each take an even share of the unit's selected list
+// (positions [r * R / P, (r + 1) * R / P)); the list is staged in shared
+// memory in chunks.  Every warp streams its rows' K and V straight from HBM
+// with cp.async (each lane copies, and later reads, its own 16- or 8-byte
+// piece of a row; NS steps in flight per warp), so the gather needs no block
+// barrier.  The CTA's (m, l, acc) partial goes to the workspace; the last CTA
+// of a unit to finish merges the P partials in a fixed order.
+#pragma once
+#include "k_select.cuh"
+
+namespace ssa {
+
+template <int G, int D>
+struct K3Cfg {
+    static constexpr int DPL = (G <= 4) ? 8 : 4;              // dims per lane (16 or 8 bytes)
+    static constexpr int LPR = D / DPL;                       // lanes per row
+    static constexpr int RPW = 32 / LPR;                      // rows per warp per step
+    static constexpr int RPS = k3Warps * RPW;                 // rows per CTA step
+    static constexpr int NS = 8;                              // steps in flight per warp
+    static constexpr uint32_t ROWB = D * 2u;
+    static constexpr uint32_t STAGE_W = (uint32_t)RPW * 2u * ROWB;    // K and V rows of one warp step
+    static constexpr uint32_t RING = (uint32_t)k3Warps * NS * STAGE_W;
+    static constexpr uint32_t MERGE = (uint32_t)k3Warps * G * D * 4u;
+    static constexpr uint32_t OFF_CHUNK = RING > MERGE ? RING : MERGE;
+    static constexpr int CHUNK = 1024;                        // list entries staged at a time
+    static constexpr uint32_t OFF_PRE = OFF_CHUNK + (uint32_t)CHUNK * 8u;
+};
+
+// Dynamic shared memory of K3 for nlists per-tile lists.
+template <int G, int D>
+constexpr uint32_t k3_smem_bytes(int nlists)
+{
+    return K3Cfg<G, D>::OFF_PRE + (uint32_t)(nlists + 1) * 4u + 128u;
+}
+
+struct K3Shared {
+    uint32_t scan[k3Warps];
+    uint32_t bcast[4];
+    float wm[k3Warps][8], wl[k3Warps][8];
+    uint32_t is_last;
+};
+
+template <int G, int D>
+__global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant__ Params p)
+{
+    using CF = K3Cfg<G, D>;
+    constexpr int DPL = CF::DPL;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                           ~static_cast<uintptr_t>(127));
+    __shared__ K3Shared ks;
+    int32_t* cidx = reinterpret_cast<int32_t*>(smem + CF::OFF_CHUNK);
+    float* clp = reinterpret_cast<float*>(smem + CF::OFF_CHUNK + CF::CHUNK * 4);
+    uint32_t* pre = reinterpret_cast<uint32_t*>(smem + CF::OFF_PRE);
+
+    const Plan& pl = p.pl;
+    const int P = pl.P;
+    const int u = blockIdx.x / P, r = blockIdx.x % P;
+    const int b = u / p.Hkv, h = u % p.Hkv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nlists = pl.ntile * kSelWarps;   // K2c writes one list per warp slice of a tile
+    const int W2 = pl.tt / kSelWarps;
+    uint32_t* status = ws_status(p);
+    grid_dep_wait();
+    SSA_MARK(7);
+
+    // the unit's list length and (per-tile lists) its prefix over the lists
+    int64_t total = 0;
+    if (p.src_mode == 0) {
+        const uint32_t* sc = ws_scount(p) + (size_t)u * nlists;
+        const int l0 = nlists * tid / k3Threads, l1 = nlists * (tid + 1) / k3Threads;
+        uint32_t mine = 0;
+        for (int l = l0; l < l1; l += 32) {
+            uint32_t c[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) c[j] = (l + j < l1) ? __ldcg(sc + l + j) : 0u;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (l + j < l1) pre[l + j] = mine;
+                mine += c[j];
+            }
+        }
+        uint32_t tot;
+        const uint32_t before = block_excl_scan<k3Threads>(mine, ks.scan, tot);
+        for (int l = l0; l < l1; ++l) pre[l] += before;
+        if (tid == 0) pre[nlists] = tot;
+        total = tot;
+    } else if (p.src_mode == 1) {
+        total = pl.N;
+    } else {
+        const int64_t c = p.count_in[u];
+        total = c < 0 ? 0 : (c > p.cap ? p.cap : c);
+    }
+    __syncthreads();
+    SSA_MARK(11);
+    const int64_t lo = total * r / P, hi = total * (r + 1) / P;
+    const uint16_t* Kb = p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
+    const uint16_t* Vb = p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
+    const int32_t* sidx = ws_sel_idx(p) + (size_t)u * pl.np;
+    const float* sp = ws_sel_p(p) + (size_t)u * pl.np;
+
+    const int sub = lane / CF::LPR, li = lane % CF::LPR;
+    float qv[G][DPL];
+    float mrun[G], lrun[G], acc[G][DPL];
+    if (p.attend) {
+        const uint16_t* qb = p.q + ((int64_t)b * p.Hq + (int64_t)h * G) * D + li * DPL;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) qv[g][c] = bf16_at(qb + (int64_t)g * D + c);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        mrun[g] = -INFINITY;
+        lrun[g] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) acc[g][c] = 0.0f;
+    }
+    unsigned char* wring = smem + (size_t)warp * CF::NS * CF::STAGE_W + (size_t)sub * 2u * CF::ROWB + li * DPL * 2;
+
+    for (int64_t c0 = lo; c0 < hi; c0 += CF::CHUNK) {
+        const int n = (int)min((int64_t)CF::CHUNK, hi - c0);
+        __syncthreads();   // the previous chunk is consumed
+        constexpr int PER = CF::CHUNK / k3Threads;   // entries per thread, loaded at once
+        int32_t jv[PER];
+        float pvv[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int i = e * k3Threads + tid;
+            const int64_t pos = c0 + i;
+            jv[e] = -1;
+            pvv[e] = 0.0f;
+            if (i < n) {
+                if (p.src_mode == 0) {
+                    int lo_l = 0, hi_l = nlists;   // pre[lo_l] <= pos < pre[hi_l]
+                    while (hi_l - lo_l > 1) {
+                        const int mid = (lo_l + hi_l) >> 1;
+                        if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
+                    }
+                    const size_t at =
+                        (size_t)(lo_l / kSelWarps) * pl.tt + (size_t)(lo_l % kSelWarps) * W2 + (pos - pre[lo_l]);
+                    jv[e] = __ldcg(sidx + at);
+                    pvv[e] = __ldcg(sp + at);
+                } else if (p.src_mode == 1) {
+                    jv[e] = (int32_t)pos;
+                    pvv[e] = 1.0f;
+                } else {
+                    jv[e] = p.idx_in[(int64_t)u * p.cap + pos];
+                    pvv[e] = p.p_in[(int64_t)u * p.cap + pos];
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int i = e * k3Threads + tid;
+            if (i >= n) continue;
+            const int64_t pos = c0 + i;
+            const int32_t j = jv[e];
+            const float pv = pvv[e];
+            const bool ok = j >= 0 && (int64_t)j < pl.N && pv > 0.0f && pv <= 1.0f;
+            if (!ok) flag(status, DEV_BAD_INDEX);
+            cidx[i] = ok ? j : -1;
+            clp[i] = ok ? logf(pv) : 0.0f;
+            if (p.idx_out) {
+                if (pos < p.cap) {
+                    p.idx_out[(int64_t)u * p.cap + pos] = j;
+                    p.p_out[(int64_t)u * p.cap + pos] = pv;
+                } else {
+                    flag(status, DEV_OVERFLOW);
+                }
+            }
+        }
+        __syncthreads();
+        if (!p.attend) continue;
+        const int nsteps = (n + CF::RPS - 1) / CF::RPS;
+        auto issue = [&](int step) {
+            const int row = step * CF::RPS + warp * CF::RPW + sub;
+            if (step < nsteps && row < n) {
+                const int32_t j = cidx[row];
+                if (j >= 0) {
+                    unsigned char* dst = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
+                    if constexpr (DPL == 8) {
+                        cp_async_16(dst, Kb + (int64_t)j * D + li * DPL);
+                        cp_async_16(dst + CF::ROWB, Vb + (int64_t)j * D + li * DPL);
+                    } else {
+                        cp_async_8(dst, Kb + (int64_t)j * D + li * DPL);
+                        cp_async_8(dst + CF::ROWB, Vb + (int64_t)j * D + li * DPL);
+                    }
+                }
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int s = 0; s < CF::NS - 1; ++s) issue(s);
+        for (int step = 0; step < nsteps; ++step) {
+            issue(step + CF::NS - 1);
+            cp_async_wait<CF::NS - 1>();
+            const int row = step * CF::RPS + warp * CF::RPW + sub;
+            const bool valid = row < n && cidx[row] >= 0;
+            const float lp = valid ? clp[row] : 0.0f;
+            const unsigned char* src = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
+            float kf[DPL], vf[DPL];
+            if constexpr (DPL == 8) {
+                const uint4 kw = *reinterpret_cast<const uint4*>(src);
+                const uint4 vw = *reinterpret_cast<const uint4*>(src + CF::ROWB);
+                const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w}, va[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    kf[2 * i] = bf16_lo(ka[i]);
+                    kf[2 * i + 1] = bf16_hi(ka[i]);
+                    vf[2 * i] = bf16_lo(va[i]);
+                    vf[2 * i + 1] = bf16_hi(va[i]);
+                }
+            } else {
+                const uint2 kw = *reinterpret_cast<const uint2*>(src);
+                const uint2 vw = *reinterpret_cast<const uint2*>(src + CF::ROWB);
+                kf[0] = bf16_lo(kw.x); kf[1] = bf16_hi(kw.x); kf[2] = bf16_lo(kw.y); kf[3] = bf16_hi(kw.y);
+                vf[0] = bf16_lo(vw.x); vf[1] = bf16_hi(vw.x); vf[2] = bf16_lo(vw.y); vf[3] = bf16_hi(vw.y);
+            }
+            float dot[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float sacc = 0.0f;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) sacc = fmaf(qv[g][c], kf[c], sacc);
+                dot[g] = sacc;
+            }
+#pragma unroll
+            for (int o = CF::LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+                for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], o);
+            if (valid) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float x = dot[g] * p.scale - lp;
+                    if (x > mrun[g]) {
+                        const float a = expf(mrun[g] - x);
+                        lrun[g] *= a;
+#pragma unroll
+                        for (int c = 0; c < DPL; ++c) acc[g][c] *= a;
+                        mrun[g] = x;
+                    }
+                    const float w = expf(x - mrun[g]);
+                    lrun[g] += w;
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) acc[g][c] = fmaf(w, vf[c], acc[g][c]);
+                }
+            }
+        }
+        cp_async_wait<0>();
+    }
+    SSA_MARK(8);
+
+    float* part = ws_part(p) + ((size_t)u * P + r) * (size_t)(G * D + 2 * G);
+    if (p.attend) {
+        // merge the row streams of a warp (lanes li, li + LPR, ...)
+#pragma unroll
+        for (int o = CF::LPR; o < 32; o <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, mrun[g], o);
+                const float lo_ = __shfl_xor_sync(0xffffffffu, lrun[g], o);
+                const float M = fmaxf(mrun[g], mo);
+                const float a = (mrun[g] == -INFINITY) ? 0.0f : expf(mrun[g] - M);
+                const float ao = (mo == -INFINITY) ? 0.0f : expf(mo - M);
+                lrun[g] = lrun[g] * a + lo_ * ao;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) {
+                    const float xo = __shfl_xor_sync(0xffffffffu, acc[g][c], o);
+                    acc[g][c] = acc[g][c] * a + xo * ao;
+                }
+                mrun[g] = M;
+            }
+        }
+        __syncthreads();   // the ring is reused for the warp partials
+        float* wpart = reinterpret_cast<float*>(smem);   // [k3Warps][G][D]
+        if (lane < CF::LPR) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) wpart[((size_t)warp * G + g) * D + li * DPL + c] = acc[g][c];
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                ks.wm[warp][g] = mrun[g];
+                ks.wl[warp][g] = lrun[g];
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < G * D; i += k3Threads) {
+            const int g = i / D, c = i % D;
+            float M = -INFINITY;
+            for (int w = 0; w < k3Warps; ++w) M = fmaxf(M, ks.wm[w][g]);
+            float A = 0.0f, Ls = 0.0f;
+            if (M != -INFINITY) {
+                for (int w = 0; w < k3Warps; ++w) {
+                    const float mw = ks.wm[w][g];
+                    if (mw == -INFINITY) continue;
+                    const float e = expf(mw - M);
+                    A = fmaf(wpart[((size_t)w * G + g) * D + c], e, A);
+                    Ls = fmaf(ks.wl[w][g], e, Ls);
+                }
+            }
+            part[i] = A;
+            if (c == 0) {
+                part[G * D + g] = M;
+                part[G * D + G + g] = Ls;
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) ks.is_last = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
+    __syncthreads();
+    SSA_MARK(12);
+    if (!ks.is_last) return;
+    __threadfence();
+    if (p.count_out && tid == 0) p.count_out[u] = (int32_t)min(total, (int64_t)INT32_MAX);
+    if (!p.attend) return;
+    // merge the P partials in a fixed order: (m, l) through shared memory,
+    // then every thread its accumulator elements, loads issued in batches
+    const float* parts = ws_part(p) + (size_t)u * P * (size_t)(G * D + 2 * G);
+    constexpr int PS = G * D + 2 * G;   // floats per partial
+    float* pm = reinterpret_cast<float*>(smem);        // [P][G] m, then weights exp(m - M)
+    float* pl_ = pm + (size_t)P * G;                   // [P][G] l
+    float* gM = pl_ + (size_t)P * G;                   // [G] max m
+    float* gL = gM + G;                                // [G] merged l
+    __syncthreads();
+    for (int i = tid; i < P * G; i += k3Threads) {
+        const int rr = i / G, g = i % G;
+        pm[i] = __ldcg(parts + (size_t)rr * PS + G * D + g);
+        pl_[i] = __ldcg(parts + (size_t)rr * PS + G * D + G + g);
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int rr = 0; rr < P; ++rr) M = fmaxf(M, pm[rr * G + tid]);
+        float Ls = 0.0f;
+        for (int rr = 0; rr < P; ++rr) {
+            const float mr = pm[rr * G + tid];
+            const float wgt = (M == -INFINITY || mr == -INFINITY) ? 0.0f : expf(mr - M);
+            pm[rr * G + tid] = wgt;
+            Ls = fmaf(pl_[rr * G + tid], wgt, Ls);
+        }
+        gM[tid] = M;
+        gL[tid] = Ls;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += k3Threads) {
+        const int g = i / D, c = i % D;
+        float A = 0.0f;
+        for (int r0 = 0; r0 < P; r0 += 16) {
+            float a[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a[j] = (r0 + j < P) ? __ldcg(parts + (size_t)(r0 + j) * PS + i) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (r0 + j < P) A = fmaf(a[j], pm[(r0 + j) * G + g], A);
+        }
+        const float Ls = gL[g];
+        const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + g;
+        p.out[head * D + c] = (Ls > 0.0f) ? A / Ls : 0.0f;
+        if (c == 0) p.lse[head] = (Ls > 0.0f) ? gM[g] + logf(Ls) : -INFINITY;
+    }
+    SSA_MARK(9);
+}
+
+// Append-time summary: Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]].
+__global__ void pack_summary_kernel(const uint16_t* __restrict__ K, const int32_t* __restrict__ sel_ch,
+                                    uint16_t* __restrict__ Ks, int32_t Hkv, int32_t d, int32_t d_sel,
+                                    int64_t N, int64_t kv_sb, int64_t kv_sh, int64_t ks_sb, int64_t ks_sh,
+                                    int64_t total, uint32_t* status)
+{
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(e % d_sel);
+        const int64_t i = (e / d_sel) % N;
+        const int64_t bh = e / ((int64_t)d_sel * N);
+        const int h = (int)(bh % Hkv);
+        const int64_t b = bh / Hkv;
+        int ch = sel_ch[h * d_sel + j];
+        if ((unsigned)ch >= (unsigned)d) {
+            flag(status, DEV_BAD_INDEX);
+            ch = ch < 0 ? 0 : d - 1;
+        }
+        Ks[b * ks_sb + h * ks_sh + i * d_sel + j] = K[b * kv_sb + h * kv_sh + i * d + ch];
+    }
+}
+
+}  // namespace ssa

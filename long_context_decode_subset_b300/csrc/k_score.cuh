@@ -1,0 +1,393 @@
+// k_score.cuh -- K0 (per-step initialisation) and K1 (approximate scores on
+// the tensor cores).
+//
+// Sources (page title, section):
+//  * "FASA: Frequency-Aware Sparse Attention", section 3 (Method), Stage 1
+//    "Token Importance Prediction": every token is scored online from a
+//    fixed, pre-calibrated subset of dominant RoPE chunks only -- here the
+//    key summary Ks[b][h][i][0..d_sel), stored contiguously at append time.
+//  * The GQA group's query heads are combined by max:
+//        s_i = fl32(scale * max_g sum_j q_g[S_ch[j]] * Ks[i][j]).
+//  * Philox4x32-10 (Salmon et al., SC'11) draws each token's uniform; K1
+//    keeps the top 8 bits of word 0 so that the decision kernel recomputes
+//    the full word only for the few tokens whose probability falls in the
+//    same 1/256 interval.
+//
+// K1 is persistent (one CTA per SM, the unit x 512-token stages split evenly
+// over the CTAs) and warp-specialised:
+//   warp 0   issues the TMA copies: two 256-token boxes of the summary per
+//            stage (swizzled to the 64- or 32-byte row width so that the
+//            tensor cores read them as K-major operands), into a ring;
+//   warp 3   writes each stage's 1 KB query operand (the unit's G query
+//            heads on the summary channels, same swizzle) beside it;
+//   warp 1   issues tcgen05.mma (M = 128 tokens, N = 16 query-head slots,
+//            K = d_sel; bf16 in, fp32 accumulators in tensor memory), four
+//            tiles per stage, and commits to the "stage free" and
+//            "accumulators ready" barriers;
+//   warp 2   allocates and frees the tensor memory;
+//   warps 4-19 (four warpgroups, one per 128-token tile) read the
+//            accumulators back (tcgen05.ld), take the max over the G heads,
+//            write the scores, count the top 12 order-key bits per unit, and
+//            draw the Philox bytes.
+#pragma once
+#include "common.cuh"
+
+namespace ssa {
+
+struct Params {
+    CUtensorMap ks_map;        // key summary [Bt][Hkv][N][d_sel] as a 4-D tensor (K1)
+    Plan pl;
+    int32_t Bt, Hq, Hkv, d, d_sel;
+    int32_t dense;             // every token selected with p = 1 (top_k >= N or budget = +inf)
+    int32_t attend;            // K3 computes attention (else it only writes the compact list)
+    int32_t src_mode;          // K3 rows: 0 per-tile lists, 1 all tokens, 2 the caller's compact list
+    const uint16_t* q;         // [Bt][Hq][d]
+    const uint16_t* K;         // [Bt][Hkv][N][d] with the strides below
+    const uint16_t* V;
+    const int32_t* sel_ch;     // [Hkv][d_sel]
+    int64_t kv_sb, kv_sh;
+    float scale;
+    float budget;
+    int64_t top_k;
+    uint64_t seed;
+    char* ws;                  // workspace base
+    float* s_dst;              // K1 writes the scores here ([U][N])
+    const float* s_src;        // K2a / K2c read the scores here ([U][N])
+    const int32_t* idx_in;     // K3 source 2: [U][cap] / count [U]
+    const float* p_in;
+    const int32_t* count_in;
+    int32_t* idx_out;          // compact list out (may be null): [U][cap] / count [U]
+    float* p_out;
+    int32_t* count_out;
+    int64_t cap;
+    float* out;                // [Bt][Hq][d]
+    float* lse;                // [Bt][Hq]
+};
+
+__device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
+__device__ __forceinline__ UnitCtrl* ws_ctrl(const Params& p) { return reinterpret_cast<UnitCtrl*>(p.ws + p.pl.o_ctrl); }
+__device__ __forceinline__ uint32_t* ws_hist1(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_hist1); }
+__device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_hist2); }
+__device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
+__device__ __forceinline__ uint32_t* ws_ccount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_ccount); }
+__device__ __forceinline__ uint32_t* ws_scount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_scount); }
+__device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
+__device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
+__device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
+__device__ __forceinline__ uint8_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint8_t*>(p.ws + p.pl.o_ubuf); }
+__device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
+
+// ---------------------------------------------------------------------------
+// K0: zero the unit's control block and histograms.  One CTA per unit.  It
+// lets the next kernel launch at once: K1 streams the summary meanwhile and
+// waits for K0 only before its first histogram flush.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Params p)
+{
+    grid_dep_launch();
+    const int u = blockIdx.x;
+    const int tid = threadIdx.x;
+    uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
+    if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
+    uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);
+    uint4* h2 = reinterpret_cast<uint4*>(ws_hist2(p) + (size_t)u * kBins);
+    for (int i = tid; i < kBins / 4; i += 256) {
+        h1[i] = make_uint4(0, 0, 0, 0);
+        h2[i] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K1: scores
+// ---------------------------------------------------------------------------
+
+constexpr int k1Threads = 640;   // warps 0-3: copies, MMA, tensor memory, query operand; 4-19: epilogue
+constexpr int k1EpiThreads = 512;
+
+template <int DSEL>
+struct K1Cfg {
+    static constexpr uint32_t ROW = DSEL * 2;                        // bytes per token row
+    static constexpr uint32_t BOX = 256u * ROW;                      // one TMA box
+    static constexpr uint32_t STAGE = (uint32_t)kStageTok * ROW;     // 32 KB or 16 KB
+    static constexpr int S = (int)((192u * 1024u) / STAGE);          // 6 or 12 stages
+    static constexpr int NB = 4;                                     // accumulator buffers
+    static constexpr uint32_t TCOLS = 256;                           // NB x 4 tiles x 16 columns
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 16);
+    static constexpr uint32_t OFF_BOP = (uint32_t)S * STAGE;
+    static constexpr uint32_t OFF_HIST = OFF_BOP + (uint32_t)S * kQselBytes;
+    static constexpr uint32_t OFF_BAR = OFF_HIST + kBins * 4;
+    static constexpr uint32_t SMEM = OFF_BAR + (2u * S + 2u * NB) * 8u + 16u + 1024u;   // + alignment slack
+    static_assert(STAGE % 1024 == 0, "stages keep the swizzle atoms aligned");
+};
+
+template <int DSEL>
+constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL>::SMEM; }
+
+template <int G, int DSEL, bool HIST, bool UBUF>
+__global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_constant__ Params p)
+{
+    using CF = K1Cfg<DSEL>;
+    constexpr int S = CF::S, NB = CF::NB;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* ring = smem;
+    unsigned char* bop = smem + CF::OFF_BOP;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + CF::OFF_HIST);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;
+    uint64_t* tempty = tfull + NB;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + NB);
+
+    const Plan& pl = p.pl;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t g0 = pl.stages * blockIdx.x / gridDim.x;
+    const int64_t g1 = pl.stages * (blockIdx.x + 1) / gridDim.x;
+    const int nstage = (int)(g1 - g0);
+    uint32_t* status = ws_status(p);
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 2);    // the summary copies (with their bytes) + the query operand
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], k1EpiThreads / 32);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&p.ks_map);
+    }
+    if constexpr (HIST) {
+        for (int i = tid; i < kBins; i += k1Threads) hist[i] = 0u;
+    }
+    if (warp == 2) tmem_alloc(tslot, CF::TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    SSA_MARK(0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
+            for (int c = 0; c < nstage; ++c, ++j) {
+                if (j == pl.nst) {
+                    j = 0;
+                    ++u;
+                }
+                const int st = c % S;
+                if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+                const int b = u / p.Hkv, h = u % p.Hkv;
+                mbar_arrive_expect_tx(&full[st], CF::STAGE);
+                unsigned char* dst = ring + (size_t)st * CF::STAGE;
+                tma_load_4d(dst, &p.ks_map, 0, j * kStageTok, h, b, &full[st], pol);
+                tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
+            }
+        }
+    } else if (warp == 3) {
+        // the query operand of each stage's unit: row g < G = q_g[S_ch[j]] over j,
+        // rows G..15 zero, K-major in the 64/32-byte swizzled layout the TMA
+        // writes for the summary.  Lane l builds half of row l / 2.
+        constexpr int HALF = DSEL / 2;   // channels per lane: 16 or 8 (two or one 16-byte chunks)
+        const int r = lane >> 1, hf = lane & 1;
+        uint4 vals[HALF / 8];
+        int cur_u = -1;
+        int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
+        for (int c = 0; c < nstage; ++c, ++j) {
+            if (j == pl.nst) {
+                j = 0;
+                ++u;
+            }
+            const int st = c % S;
+            if (u != cur_u) {
+                cur_u = u;
+                const int b = u / p.Hkv, h = u % p.Hkv;
+                uint16_t v[HALF];
+#pragma unroll
+                for (int k = 0; k < HALF; ++k) {
+                    v[k] = 0;
+                    if (r < G) {
+                        int ch = p.sel_ch[(int64_t)h * DSEL + hf * HALF + k];
+                        if ((unsigned)ch >= (unsigned)p.d) {
+                            flag(status, DEV_BAD_INDEX);
+                            ch = 0;
+                        }
+                        v[k] = p.q[((int64_t)b * p.Hq + (int64_t)h * G + r) * p.d + ch];
+                    }
+                }
+#pragma unroll
+                for (int q8 = 0; q8 < HALF / 8; ++q8)
+                    vals[q8] = make_uint4((uint32_t)v[q8 * 8 + 0] | ((uint32_t)v[q8 * 8 + 1] << 16),
+                                          (uint32_t)v[q8 * 8 + 2] | ((uint32_t)v[q8 * 8 + 3] << 16),
+                                          (uint32_t)v[q8 * 8 + 4] | ((uint32_t)v[q8 * 8 + 5] << 16),
+                                          (uint32_t)v[q8 * 8 + 6] | ((uint32_t)v[q8 * 8 + 7] << 16));
+            }
+            if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+            unsigned char* row = bop + (size_t)st * kQselBytes + (size_t)r * CF::ROW;
+#pragma unroll
+            for (int q8 = 0; q8 < HALF / 8; ++q8) {
+                const int chunk = hf * (HALF / 8) + q8;
+                const int phys = (DSEL == 32) ? (chunk ^ ((r >> 1) & 3)) : (chunk ^ ((r >> 2) & 1));
+                *reinterpret_cast<uint4*>(row + phys * 16) = vals[q8];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t ring_a = smem_addr(ring), bop_a = smem_addr(bop);
+            for (int c = 0; c < nstage; ++c) {
+                const int st = c % S, nb = c % NB;
+                if (!mbar_wait_bounded(&full[st], (uint32_t)(c / S) & 1u)) flag(status, DEV_TIMEOUT);
+                if (c >= NB && !mbar_wait_bounded(&tempty[nb], (uint32_t)((c / NB) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+                tc_fence_after();
+                const uint32_t a0 = ring_a + (uint32_t)st * CF::STAGE;
+                const uint32_t b0 = bop_a + (uint32_t)st * kQselBytes;
+                const uint32_t dcol = tbase + (uint32_t)nb * 64u;
+#pragma unroll
+                for (int tile = 0; tile < 4; ++tile) {
+#pragma unroll
+                    for (int ks = 0; ks < DSEL / 16; ++ks) {
+                        const uint64_t ad = smem_desc_kmajor_swz(a0 + (uint32_t)tile * 128u * CF::ROW + ks * 32u, CF::ROW);
+                        const uint64_t bd = smem_desc_kmajor_swz(b0 + ks * 32u, CF::ROW);
+                        tc_mma_bf16(dcol + (uint32_t)tile * 16u, ad, bd, CF::IDESC, ks > 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(&empty[st]);
+                tc_commit(&tfull[nb]);
+            }
+        }
+    } else if (warp >= 4) {
+        const int tile = (warp - 4) >> 2, quarter = warp & 3, etid = tid - 128;
+        const uint32_t k0 = (uint32_t)(p.seed & 0xffffffffu), k1 = (uint32_t)(p.seed >> 32);
+        uint32_t* hist1 = ws_hist1(p);
+        uint8_t* ubuf = ws_ubuf(p);
+        int cur_u = -1;
+        bool waited = false;
+        auto flush = [&](int uu) {
+            if (!waited) {
+                grid_dep_wait();   // K0 has zeroed the histograms
+                waited = true;
+            }
+            named_bar_sync(1, k1EpiThreads);
+            for (int i = etid; i < kBins; i += k1EpiThreads) {
+                const uint32_t v = hist[i];
+                if (v) {
+                    atomicAdd(hist1 + (size_t)uu * kBins + i, v);
+                    hist[i] = 0u;
+                }
+            }
+            named_bar_sync(1, k1EpiThreads);
+        };
+        const uint32_t tl = ((uint32_t)(quarter * 32) << 16) + (uint32_t)tile * 16u;   // lane quarter, tile columns
+        int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
+        for (int c = 0; c < nstage; ++c, ++j) {
+            if (j == pl.nst) {
+                j = 0;
+                ++u;
+            }
+            const int nb = c % NB;
+            if (!mbar_wait_bounded(&tfull[nb], (uint32_t)(c / NB) & 1u)) flag(status, DEV_TIMEOUT);
+            tc_fence_after();
+            float acc[G];
+            const uint32_t taddr = tbase + tl + (uint32_t)nb * 64u;
+            if constexpr (G == 1) {
+                uint32_t r[1];
+                tmem_ld_x1(taddr, r);
+                tmem_ld_wait();
+                acc[0] = __uint_as_float(r[0]);
+            } else if constexpr (G == 2) {
+                uint32_t r[2];
+                tmem_ld_x2(taddr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 2; ++g) acc[g] = __uint_as_float(r[g]);
+            } else if constexpr (G == 4) {
+                uint32_t r[4];
+                tmem_ld_x4(taddr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) acc[g] = __uint_as_float(r[g]);
+            } else {
+                uint32_t r[8];
+                tmem_ld_x8(taddr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 8; ++g) acc[g] = __uint_as_float(r[g]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[nb]);
+
+            if constexpr (HIST) {
+                if (u != cur_u) {
+                    if (cur_u >= 0) flush(cur_u);
+                    cur_u = u;
+                }
+            }
+            const int t = j * kStageTok + tile * 128 + quarter * 32 + lane;
+            if (t < pl.N) {
+                float best = acc[0];
+#pragma unroll
+                for (int gg = 1; gg < G; ++gg) best = fmaxf(best, acc[gg]);
+                const float s = best * p.scale;
+                if (!isfinite(s)) flag(status, DEV_NONFINITE);
+                p.s_dst[(int64_t)u * pl.N + t] = s;
+                if constexpr (HIST) atomicAdd(&hist[okey(s) >> 20], 1u);
+                if constexpr (UBUF) {
+                    const int b = u / p.Hkv, h = u % p.Hkv;
+                    const uint32_t x0 = philox_word0((uint32_t)t, (uint32_t)h, (uint32_t)b, 0u, k0, k1);
+                    ubuf[(int64_t)u * pl.np + t] = (uint8_t)(x0 >> 24);
+                }
+            }
+        }
+        if constexpr (HIST) {
+            if (cur_u >= 0) flush(cur_u);
+        }
+    }
+    SSA_MARK(1);
+    tc_fence_before();
+    __syncthreads();
+    grid_dep_launch();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tbase, CF::TCOLS);
+    }
+}
+
+// K1 for ssa_select (scores given): per-unit histogram of the top 12 key bits
+// and the Philox bytes.  One CTA per (unit, tile).
+__global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_constant__ Params p)
+{
+    __shared__ uint32_t hist[kBins];
+    const Plan& pl = p.pl;
+    const int u = blockIdx.x / pl.ntile, tile = blockIdx.x % pl.ntile;
+    const int tid = threadIdx.x;
+    const int64_t t0 = (int64_t)tile * pl.tt;
+    const int n = (int)min((int64_t)pl.tt, pl.N - t0);
+    const int b = u / p.Hkv, h = u % p.Hkv;
+    const uint32_t k0 = (uint32_t)(p.seed & 0xffffffffu), k1 = (uint32_t)(p.seed >> 32);
+    uint32_t* status = ws_status(p);
+    for (int i = tid; i < kBins; i += k3Threads) hist[i] = 0u;
+    __syncthreads();
+    grid_dep_wait();
+    for (int i = tid; i < n; i += k3Threads) {
+        const int64_t t = t0 + i;
+        const float s = p.s_src[(int64_t)u * pl.N + t];
+        if (!isfinite(s)) flag(status, DEV_NONFINITE);
+        atomicAdd(&hist[okey(s) >> 20], 1u);
+        const uint32_t x0 = philox_word0((uint32_t)t, (uint32_t)h, (uint32_t)b, 0u, k0, k1);
+        ws_ubuf(p)[(int64_t)u * pl.np + t] = (uint8_t)(x0 >> 24);
+    }
+    __syncthreads();
+    uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
+    for (int i = tid; i < kBins; i += k3Threads)
+        if (hist[i]) atomicAdd(hist1 + i, hist[i]);
+    grid_dep_launch();
+}
+
+}  // namespace ssa

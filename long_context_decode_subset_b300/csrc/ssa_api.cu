@@ -1,61 +1,101 @@
-// ssa_api.cu -- host side of libssa: argument checks, workspace layout,
-// launch planning and the C entry points declared in include/ssa.h.
+// ssa_api.cu -- host side of libssa: argument checks, the per-shape plan and
+// workspace layout, launches, and the C entry points declared in
+// include/ssa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
-#include <tuple>
 
 #include "ssa.h"
-#include "kernels.cuh"
+#include "k_attend.cuh"
 
 using namespace ssa;
 
 namespace {
 
 constexpr size_t kStatusBytes = 256;
-constexpr int64_t kScoreTile = 8192;   // tokens per CTA for the standalone score launch
+constexpr int kMaxSplit = 64;          // K3 CTAs per unit at most (the workspace is sized for it)
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
-struct WsLayout {
-    size_t status, scores, idx, prob, count, hq, hout, hlse, total;
-};
-
-int64_t eff_cap(const ssa_shape& s, int64_t cap) { return cap > 0 ? cap : (s.ctx_len > 0 ? s.ctx_len : 1); }
-
-WsLayout ws_layout(const ssa_shape& s, int64_t cap)
+int env_int(const char* name, int dflt)
 {
-    const int64_t units = (int64_t)s.batch * s.n_kv_heads;
-    const int64_t n = s.ctx_len > 0 ? s.ctx_len : 1;
-    const int64_t c = eff_cap(s, cap);
-    const int64_t heads = (int64_t)s.batch * s.n_q_heads;
-    WsLayout L{};
-    size_t o = 0;
-    L.status = o;
-    o += kStatusBytes;
-    L.scores = o;
-    o += align256((size_t)(units * n * 4));
-    L.idx = o;
-    o += align256((size_t)(units * c * 4));
-    L.prob = o;
-    o += align256((size_t)(units * c * 4));
-    L.count = o;
-    o += align256((size_t)(units * 4));
-    L.hq = o;
-    o += align256((size_t)(heads * s.head_dim * 2));
-    L.hout = o;
-    o += align256((size_t)(heads * s.head_dim * 4));
-    L.hlse = o;
-    o += align256((size_t)(heads * 4));
-    L.total = o;
-    return L;
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::atoi(v) : dflt;
 }
 
-bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 148;
+    }
+    return n > 0 ? n : 148;
+}
+
+// Plan and workspace layout.  The layout does not depend on the device; the
+// K1 grid and the K3 split do (the workspace is sized for the largest split).
+// SSA_FORCE_TILE / SSA_FORCE_SPLIT override the tile size and the split (the
+// tests use them to cover many tiles and splits on small inputs).
+ssa::Plan make_plan(const ssa_shape& s, bool with_device)
+{
+    ssa::Plan pl{};
+    pl.U = s.batch * s.n_kv_heads;
+    pl.G = s.n_q_heads / s.n_kv_heads;
+    pl.N = s.ctx_len;
+    const int64_t U = pl.U, N = s.ctx_len;
+    pl.nst = (int32_t)((N + kStageTok - 1) / kStageTok);
+    pl.stages = U * pl.nst;
+    const int sms = with_device ? device_sms() : 148;
+    pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
+    int64_t tt = (int64_t)kTileTok * std::max<int64_t>(1, (N + (int64_t)kTileTok * kMaxTiles - 1) /
+                                                               ((int64_t)kTileTok * kMaxTiles));
+    const int forced_tile = env_int("SSA_FORCE_TILE", 0);
+    if (forced_tile >= 512 && forced_tile % 512 == 0 && (N + forced_tile - 1) / forced_tile <= kMaxTiles)
+        tt = forced_tile;
+    pl.tt = (int32_t)tt;
+    pl.ntile = (int32_t)((N + tt - 1) / tt);
+    pl.np = (int64_t)pl.ntile * tt;
+    pl.P = 1;   // set at launch (attend_split)
+
+    const int64_t G = pl.G, D = s.head_dim;
+    const int64_t heads = (int64_t)s.batch * s.n_q_heads;
+    const int64_t nl = (int64_t)pl.ntile * kSelWarps;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align256(bytes);
+        return at;
+    };
+    pl.o_status = take(kStatusBytes);
+    pl.o_ctrl = take((size_t)U * sizeof(UnitCtrl));
+    pl.o_hist1 = take((size_t)U * kBins * 4);
+    pl.o_hist2 = take((size_t)U * kBins * 4);
+    pl.zero_bytes = o - pl.o_ctrl;
+    pl.o_zpart = take((size_t)U * pl.ntile * 8);
+    pl.o_ccount = take((size_t)U * nl * 4);
+    pl.o_scount = take((size_t)U * nl * 4);
+    pl.o_cand = take((size_t)U * pl.np * 8);
+    pl.o_sel_idx = take((size_t)U * pl.np * 4);
+    pl.o_sel_p = take((size_t)U * pl.np * 4);
+    pl.o_scores = take((size_t)U * N * 4);
+    pl.o_ubuf = take((size_t)U * pl.np);
+    pl.o_part = take((size_t)U * kMaxSplit * (size_t)(G * D + 2 * G) * 4);
+    pl.o_hq = take((size_t)heads * D * 2);
+    pl.o_hout = take((size_t)heads * D * 4);
+    pl.o_hlse = take((size_t)heads * 4);
+    pl.total = o;
+    return pl;
+}
 
 ssa_status check_shape(const ssa_shape* s)
 {
@@ -66,7 +106,8 @@ ssa_status check_shape(const ssa_shape* s)
     if (G != 1 && G != 2 && G != 4 && G != 8) return SSA_ERR_UNSUPPORTED;
     if (s->head_dim != 64 && s->head_dim != 128) return SSA_ERR_UNSUPPORTED;
     if (s->d_sel != 16 && s->d_sel != 32) return SSA_ERR_UNSUPPORTED;
-    if (s->ctx_len < 0 || s->ctx_len >= (int64_t)INT32_MAX) return SSA_ERR_INVALID_ARG;
+    if (s->ctx_len < 0 || s->ctx_len > (int64_t)INT32_MAX - 4096) return SSA_ERR_INVALID_ARG;
+    if ((int64_t)s->batch * s->n_kv_heads > (int64_t)INT32_MAX / (kMaxSplit * 2)) return SSA_ERR_UNSUPPORTED;
     const int64_t N = s->ctx_len;
     if (s->kv_stride_h < N * s->head_dim || s->ks_stride_h < N * s->d_sel) return SSA_ERR_INVALID_ARG;
     if (s->kv_stride_b < (int64_t)(s->n_kv_heads - 1) * s->kv_stride_h + N * s->head_dim) return SSA_ERR_INVALID_ARG;
@@ -76,250 +117,199 @@ ssa_status check_shape(const ssa_shape* s)
     return SSA_OK;
 }
 
-ssa_status check_ws(void* ws, size_t ws_bytes, const ssa_shape& s, int64_t cap)
+ssa_status check_ws(void* ws, size_t ws_bytes, const ssa::Plan& pl)
 {
     if (!ws || !aligned(ws, 256)) return SSA_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(s, cap).total) return SSA_ERR_WORKSPACE;
+    if (ws_bytes < pl.total) return SSA_ERR_WORKSPACE;
     return SSA_OK;
 }
 
-typedef void (*kfn_t)(Params);
+bool bad_scalars(int64_t top_k, float budget) { return top_k < 0 || !(budget >= 0.0f); }
+bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
 
-template <int G, int MODE, bool RES>
-kfn_t pick_dsel_d(int dsel, int d)
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    if (dsel == 16) return d == 64 ? &unit_kernel<G, 16, 64, MODE, RES> : &unit_kernel<G, 16, 128, MODE, RES>;
-    return d == 64 ? &unit_kernel<G, 32, 64, MODE, RES> : &unit_kernel<G, 32, 128, MODE, RES>;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
 }
 
-template <int MODE, bool RES>
-kfn_t pick_g(int G, int dsel, int d)
+// The key summary [Bt][Hkv][N][d_sel] as a 4-D tensor for TMA: boxes of
+// 256 tokens x d_sel channels, swizzled to the row width (64 or 32 bytes)
+// so that the tensor cores read them as K-major operands.
+ssa_status encode_summary_map(CUtensorMap* map, const ssa_bf16* Ks, const ssa_shape& s)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return SSA_ERR_CUDA;
+    cuuint64_t dims[4] = {(cuuint64_t)s.d_sel, (cuuint64_t)s.ctx_len, (cuuint64_t)s.n_kv_heads, (cuuint64_t)s.batch};
+    cuuint64_t strides[3] = {(cuuint64_t)s.d_sel * 2, (cuuint64_t)s.ks_stride_h * 2, (cuuint64_t)s.ks_stride_b * 2};
+    cuuint32_t box[4] = {(cuuint32_t)s.d_sel, 256u, 1u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<ssa_bf16*>(Ks), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           s.d_sel == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SSA_OK : SSA_ERR_CUDA;
+}
+
+typedef void (*kfn_t)(ssa::Params);
+
+template <int G, int DSEL>
+kfn_t pick_score_hd(bool hist)
+{
+    return hist ? &score_kernel<G, DSEL, true, true> : &score_kernel<G, DSEL, false, false>;
+}
+
+kfn_t pick_score(int G, int dsel, bool hist)
 {
     switch (G) {
-        case 1: return pick_dsel_d<1, MODE, RES>(dsel, d);
-        case 2: return pick_dsel_d<2, MODE, RES>(dsel, d);
-        case 4: return pick_dsel_d<4, MODE, RES>(dsel, d);
-        default: return pick_dsel_d<8, MODE, RES>(dsel, d);
+        case 1: return dsel == 16 ? pick_score_hd<1, 16>(hist) : pick_score_hd<1, 32>(hist);
+        case 2: return dsel == 16 ? pick_score_hd<2, 16>(hist) : pick_score_hd<2, 32>(hist);
+        case 4: return dsel == 16 ? pick_score_hd<4, 16>(hist) : pick_score_hd<4, 32>(hist);
+        default: return dsel == 16 ? pick_score_hd<8, 16>(hist) : pick_score_hd<8, 32>(hist);
     }
 }
 
-template <int G>
-kfn_t pick_score(int dsel)
+template <int G, int D>
+kfn_t att_fn(uint32_t* smem, int nlists)
 {
-    return dsel == 16 ? &unit_kernel<G, 16, 64, MODE_SCORE, false> : &unit_kernel<G, 32, 64, MODE_SCORE, false>;
+    *smem = k3_smem_bytes<G, D>(nlists);
+    return &attend_kernel<G, D>;
 }
 
-template <int G>
-kfn_t pick_attend(int d)
+kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists)
 {
-    return d == 64 ? &unit_kernel<G, 16, 64, MODE_ATTEND, false> : &unit_kernel<G, 16, 128, MODE_ATTEND, false>;
-}
-
-kfn_t pick_kernel(int mode, int G, int dsel, int d, bool res)
-{
-    switch (mode) {
-        case MODE_SCORE:
-            switch (G) {
-                case 1: return pick_score<1>(dsel);
-                case 2: return pick_score<2>(dsel);
-                case 4: return pick_score<4>(dsel);
-                default: return pick_score<8>(dsel);
-            }
-        case MODE_SELECT:
-            return res ? &unit_kernel<1, 16, 64, MODE_SELECT, true> : &unit_kernel<1, 16, 64, MODE_SELECT, false>;
-        case MODE_ATTEND:
-            switch (G) {
-                case 1: return pick_attend<1>(d);
-                case 2: return pick_attend<2>(d);
-                case 4: return pick_attend<4>(d);
-                default: return pick_attend<8>(d);
-            }
-        default:
-            return res ? pick_g<MODE_SCORE | MODE_SELECT | MODE_ATTEND, true>(G, dsel, d)
-                       : pick_g<MODE_SCORE | MODE_SELECT | MODE_ATTEND, false>(G, dsel, d);
+    switch (G) {
+        case 1: return d == 64 ? att_fn<1, 64>(smem, nlists) : att_fn<1, 128>(smem, nlists);
+        case 2: return d == 64 ? att_fn<2, 64>(smem, nlists) : att_fn<2, 128>(smem, nlists);
+        case 4: return d == 64 ? att_fn<4, 64>(smem, nlists) : att_fn<4, 128>(smem, nlists);
+        default: return d == 64 ? att_fn<8, 64>(smem, nlists) : att_fn<8, 128>(smem, nlists);
     }
 }
 
-int env_int(const char* name, int dflt)
+// Launch `fn` on `stream`.  Every kernel of a step after the first is a
+// programmatic dependent launch: it may start while its predecessor drains
+// and waits (griddepcontrol.wait) before reading its results.
+ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::Params& prm, cudaStream_t stream,
+                  bool dependent)
 {
-    const char* v = std::getenv(name);
-    return (v && *v) ? std::atoi(v) : dflt;
-}
-
-std::mutex g_mu;
-
-// Largest number of clusters of size C of this kernel that can be resident at once.
-int max_active_clusters(kfn_t fn, int C, uint32_t smem)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    static std::map<std::tuple<void*, int, uint32_t, int>, int> cache;
-    const auto key = std::make_tuple((void*)fn, C, smem, dev);
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    int n = 0;
-    bool ok = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
-              cudaSuccess;
-    if (ok && C > 8)
-        ok = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    if (ok) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(C * 64), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = (unsigned)C;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) n = 0;
-    }
-    if (!ok || n == 0) cudaGetLastError();
-    std::lock_guard<std::mutex> lk(g_mu);
-    cache[key] = n;
-    return n;
-}
-
-struct Plan {
-    int C = 1;
-    bool res = false;
-    int64_t seg = kSegAlign;
-    uint32_t smem = 0;
-    bool cluster = true;
-};
-
-int64_t round_seg(int64_t n, int C)
-{
-    const int64_t per = (n + C - 1) / C;
-    return ((per + kSegAlign - 1) / kSegAlign) * kSegAlign;
-}
-
-// One cluster per unit: the largest C in {16, 8, 4, 2, 1} whose clusters
-// all fit on the GPU at once (a single wave), without CTAs of fewer than
-// 512 tokens.  SSA_FORCE_CLUSTER / SSA_FORCE_GLOBAL_SCORES override the
-// choice (used by the tests to cover every path on small inputs).
-Plan make_plan(int mode, const ssa_shape& s)
-{
-    const int G = s.n_q_heads / s.n_kv_heads;
-    const int64_t units = (int64_t)s.batch * s.n_kv_heads;
-    const int64_t n = s.ctx_len > 0 ? s.ctx_len : 1;
-    Plan pl;
-    if (mode == MODE_SCORE) {
-        pl.seg = kScoreTile;
-        pl.C = (int)((n + kScoreTile - 1) / kScoreTile);
-        pl.cluster = false;
-        pl.smem = make_layout(mode, false, pl.seg, 1).total;
-        return pl;
-    }
-    const int forced = env_int("SSA_FORCE_CLUSTER", 0);
-    const bool force_global = env_int("SSA_FORCE_GLOBAL_SCORES", 0) != 0;
-    int maxC = 1;
-    while (maxC < 16 && (int64_t)(maxC * 2) * kSegAlign <= n) maxC *= 2;
-    Plan best;
-    bool have_best = false;
-    int64_t best_score = -1;
-    for (int C = 16; C >= 1; C /= 2) {
-        if (forced > 0 && C != forced) continue;
-        if (forced <= 0 && C > maxC) continue;
-        Plan cand;
-        cand.C = C;
-        cand.seg = (mode & MODE_SELECT) ? round_seg(n, C) : kSegAlign;
-        cand.res = (mode & MODE_SELECT) && !force_global &&
-                   make_layout(mode, true, cand.seg, C).total <= kSmemLimit;
-        cand.smem = make_layout(mode, cand.res, cand.seg, C).total;
-        if (cand.smem > kSmemLimit) continue;
-        if (forced > 0) return cand;
-        const int clusters = max_active_clusters(pick_kernel(mode, G, s.d_sel, s.head_dim, cand.res), C, cand.smem);
-        if (clusters <= 0) continue;
-        if (clusters >= units) return cand;
-        // otherwise prefer the choice that keeps the most CTAs busy in one wave
-        const int64_t busy = (int64_t)std::min<int64_t>(clusters, units) * C;
-        if (busy > best_score) {
-            best_score = busy;
-            best = cand;
-            have_best = true;
-        }
-    }
-    if (have_best) return best;
-    Plan fb;
-    fb.C = 1;
-    fb.seg = (mode & MODE_SELECT) ? round_seg(n, 1) : kSegAlign;
-    fb.res = false;
-    fb.smem = make_layout(mode, false, fb.seg, 1).total;
-    return fb;
-}
-
-ssa_status launch(int mode, const ssa_shape& s, const Plan& pl, const Params& prm, cudaStream_t stream)
-{
-    const int G = s.n_q_heads / s.n_kv_heads;
-    const int64_t units = (int64_t)s.batch * s.n_kv_heads;
-    if (units == 0) return SSA_OK;
-    if (pl.smem > kSmemLimit) return SSA_ERR_UNSUPPORTED;
-    kfn_t fn = pick_kernel(mode, G, s.d_sel, s.head_dim, pl.res);
-    if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-        cudaSuccess) {
+    if (grid <= 0) return SSA_OK;
+    if (grid > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    if (smem > 48u * 1024u &&
+        cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return SSA_ERR_CUDA;
     }
-    if (pl.cluster && pl.C > 8 &&
-        cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-        cudaGetLastError();
-        return SSA_ERR_CUDA;
-    }
-    const int64_t blocks = units * pl.C;
-    if (blocks > INT32_MAX) return SSA_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
-    if (pl.cluster) {
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = (unsigned)pl.C;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
+    if (dependent) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
     }
-    Params p = prm;
-    p.C = pl.C;
-    p.seg_len = pl.seg;
-    const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, p);
-    if (err != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, fn, prm) != cudaSuccess) {
         cudaGetLastError();
         return SSA_ERR_CUDA;
     }
     return SSA_OK;
 }
 
-Params base_params(const ssa_shape& s, void* ws)
+ssa::Params base_params(const ssa_shape& s, const ssa::Plan& pl, void* ws)
 {
-    Params p = {};
+    ssa::Params p;
+    std::memset(&p, 0, sizeof p);
+    p.pl = pl;
     p.Bt = s.batch;
     p.Hq = s.n_q_heads;
     p.Hkv = s.n_kv_heads;
     p.d = s.head_dim;
     p.d_sel = s.d_sel;
-    p.N = s.ctx_len;
     p.kv_sb = s.kv_stride_b;
     p.kv_sh = s.kv_stride_h;
-    p.ks_sb = s.ks_stride_b;
-    p.ks_sh = s.ks_stride_h;
-    p.status = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + ws_layout(s, 1).status);
+    p.ws = static_cast<char*>(ws);
     return p;
 }
 
-bool bad_scalars(int64_t top_k, float budget) { return top_k < 0 || !(budget >= 0.0f); }
-bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
+ssa_status launch_init(const ssa::Params& p, cudaStream_t stream)
+{
+    return launch(&init_kernel, p.pl.U, 256, 0, p, stream, false);
+}
+
+ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cudaStream_t stream, bool dependent)
+{
+    const uint32_t smem = s.d_sel == 32 ? k1_smem_bytes<32>() : k1_smem_bytes<16>();
+    return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1Threads, smem, p, stream, dependent);
+}
+
+ssa_status launch_select(const ssa::Params& p, cudaStream_t stream)
+{
+    const int64_t grid = (int64_t)p.pl.U * p.pl.ntile;
+    ssa_status st = launch(&bucket_kernel, grid, kSelThreads, k2a_smem_bytes(p.pl.ntile * kSelWarps), p, stream, true);
+    if (st != SSA_OK) return st;
+    return launch(&decide_kernel, grid, kSelThreads, 0, p, stream, true);
+}
+
+// CTAs of `fn` resident per SM (cached per kernel and shared-memory size).
+int blocks_per_sm(kfn_t fn, int block, uint32_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<void*, uint32_t>, int> cache;
+    const auto key = std::make_pair((void*)fn, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if ((smem > 48u * 1024u &&
+         cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)fn, block, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    n = std::max(n, 1);
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+// K3 CTAs per unit: as many as fit in one wave with every unit getting the
+// same number (at most kMaxSplit), unless SSA_FORCE_SPLIT says otherwise.
+int attend_split(const ssa::Plan& pl, const ssa_shape& s)
+{
+    const int forced = env_int("SSA_FORCE_SPLIT", 0);
+    if (forced > 0) return std::min(forced, kMaxSplit);
+    uint32_t smem = 0;
+    kfn_t fn = pick_attend(pl.G, s.head_dim, &smem, pl.ntile * kSelWarps);
+    const int64_t slots = (int64_t)blocks_per_sm(fn, k3Threads, smem) * device_sms();
+    return (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, slots / std::max<int64_t>(pl.U, 1)));
+}
+
+ssa_status launch_attend(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream)
+{
+    uint32_t smem = 0;
+    kfn_t fn = pick_attend(p.pl.G, s.head_dim, &smem, p.pl.ntile * kSelWarps);
+    if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
+    ssa::Params q = p;
+    q.pl.P = attend_split(p.pl, s);
+    return launch(fn, (int64_t)q.pl.U * q.pl.P, k3Threads, smem, q, stream, true);
+}
 
 }  // namespace
 
@@ -371,12 +361,13 @@ const char* ssa_status_string(int status)
     }
 }
 
-int ssa_version(void) { return 100; }
+int ssa_version(void) { return 200; }
 
 size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap)
 {
+    (void)list_cap;
     if (check_shape(shape) != SSA_OK) return 0;
-    return ws_layout(*shape, list_cap).total;
+    return make_plan(*shape, false).total;
 }
 
 ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* Ks, void* ws, size_t ws_bytes,
@@ -385,17 +376,18 @@ ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* 
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!K || !sel_ch || !Ks) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, 0)) != SSA_OK) return st;
+    const ssa::Plan pl = make_plan(*shape, false);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     const int64_t total = (int64_t)shape->batch * shape->n_kv_heads * shape->ctx_len * shape->d_sel;
     if (total == 0) return SSA_OK;
-    const Params bp = base_params(*shape, ws);
     const int threads = 256;
     const int64_t want = (total + threads - 1) / threads;
     const unsigned blocks = (unsigned)std::min<int64_t>(want, 148 * 32);
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + pl.o_status);
     pack_summary_kernel<<<blocks, threads, 0, stream>>>(K, sel_ch, Ks, shape->n_kv_heads, shape->head_dim,
                                                         shape->d_sel, shape->ctx_len, shape->kv_stride_b,
                                                         shape->kv_stride_h, shape->ks_stride_b,
-                                                        shape->ks_stride_h, total, bp.status);
+                                                        shape->ks_stride_h, total, status);
     if (cudaGetLastError() != cudaSuccess) return SSA_ERR_CUDA;
     return SSA_OK;
 }
@@ -408,15 +400,16 @@ ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_c
     if (!q || !Ks || !sel_ch || !s_hat) return SSA_ERR_INVALID_ARG;
     if (!aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, 0)) != SSA_OK) return st;
-    if (shape->ctx_len == 0) return SSA_OK;
-    Params p = base_params(*shape, ws);
+    const ssa::Plan pl = make_plan(*shape, true);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (shape->ctx_len == 0 || pl.U == 0) return SSA_OK;
+    ssa::Params p = base_params(*shape, pl, ws);
+    if ((st = encode_summary_map(&p.ks_map, Ks, *shape)) != SSA_OK) return st;
     p.q = q;
-    p.Ks = Ks;
     p.sel_ch = sel_ch;
     p.scale = scale;
-    p.s_out = s_hat;
-    return launch(MODE_SCORE, *shape, make_plan(MODE_SCORE, *shape), p, stream);
+    p.s_dst = s_hat;
+    return launch_score(p, *shape, false, stream, false);
 }
 
 ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t seed, int32_t* idx, float* p,
@@ -427,17 +420,28 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
     if (st != SSA_OK) return st;
     if (!s_hat || !idx || !p || !count) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget)) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, list_cap)) != SSA_OK) return st;
-    Params prm = base_params(*shape, ws);
-    prm.s_in = s_hat;
+    const ssa::Plan pl = make_plan(*shape, true);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (pl.U == 0) return SSA_OK;
+    ssa::Params prm = base_params(*shape, pl, ws);
+    prm.s_src = s_hat;
     prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
-    prm.idx = idx;
-    prm.p = p;
-    prm.count = count;
-    prm.cap = eff_cap(*shape, list_cap);
-    return launch(MODE_SELECT, *shape, make_plan(MODE_SELECT, *shape), prm, stream);
+    prm.idx_out = idx;
+    prm.p_out = p;
+    prm.count_out = count;
+    prm.cap = list_cap > 0 ? list_cap : std::max<int64_t>(shape->ctx_len, 1);
+    prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
+    prm.src_mode = prm.dense ? 1 : 0;
+    prm.attend = 0;
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    if (!prm.dense) {
+        if ((st = launch(&score_input_kernel, (int64_t)pl.U * pl.ntile, k3Threads, 0, prm, stream, true)) != SSA_OK)
+            return st;
+        if ((st = launch_select(prm, stream)) != SSA_OK) return st;
+    }
+    return launch_attend(prm, *shape, stream);
 }
 
 ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const int32_t* idx, const float* p,
@@ -449,19 +453,25 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     if (!q || !idx || !p || !count || !out || !lse || (shape->ctx_len > 0 && (!K || !V))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, list_cap)) != SSA_OK) return st;
-    Params prm = base_params(*shape, ws);
+    const ssa::Plan pl = make_plan(*shape, true);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (pl.U == 0) return SSA_OK;
+    ssa::Params prm = base_params(*shape, pl, ws);
     prm.q = q;
     prm.K = K;
     prm.V = V;
     prm.scale = scale;
-    prm.idx = const_cast<int32_t*>(idx);
-    prm.p = const_cast<float*>(p);
-    prm.count = const_cast<int32_t*>(count);
-    prm.cap = eff_cap(*shape, list_cap);
+    prm.idx_in = idx;
+    prm.p_in = p;
+    prm.count_in = count;
+    prm.cap = list_cap > 0 ? list_cap : std::max<int64_t>(shape->ctx_len, 1);
     prm.out = out;
     prm.lse = lse;
-    return launch(MODE_ATTEND, *shape, make_plan(MODE_ATTEND, *shape), prm, stream);
+    prm.src_mode = 2;
+    prm.attend = 1;
+    // K0 zeroes the merge counters (sel_ch is not given, so no query operand is built)
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    return launch_attend(prm, *shape, stream);
 }
 
 ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
@@ -475,28 +485,39 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     if (!q || !sel_ch || !out || !lse || (!empty && (!K || !V || !Ks))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget) || bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, list_cap)) != SSA_OK) return st;
-    const WsLayout wl = ws_layout(*shape, list_cap);
+    if ((idx_opt == nullptr) != (p_opt == nullptr)) return SSA_ERR_INVALID_ARG;
+    const ssa::Plan pl = make_plan(*shape, true);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (pl.U == 0) return SSA_OK;
     char* w = static_cast<char*>(ws);
-    const Plan pl = make_plan(MODE_SCORE | MODE_SELECT | MODE_ATTEND, *shape);
-    Params prm = base_params(*shape, ws);
+    ssa::Params prm = base_params(*shape, pl, ws);
+    if (!empty && (st = encode_summary_map(&prm.ks_map, Ks, *shape)) != SSA_OK) return st;
     prm.q = q;
     prm.K = K;
     prm.V = V;
-    prm.Ks = Ks;
     prm.sel_ch = sel_ch;
     prm.scale = scale;
     prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
-    prm.s_out = s_hat_opt ? s_hat_opt : (pl.res ? nullptr : reinterpret_cast<float*>(w + wl.scores));
-    prm.idx = idx_opt ? idx_opt : reinterpret_cast<int32_t*>(w + wl.idx);
-    prm.p = p_opt ? p_opt : reinterpret_cast<float*>(w + wl.prob);
-    prm.count = count_opt;
-    prm.cap = eff_cap(*shape, list_cap);
+    float* scores = s_hat_opt ? s_hat_opt : reinterpret_cast<float*>(w + pl.o_scores);
+    prm.s_dst = scores;
+    prm.s_src = scores;
+    prm.idx_out = idx_opt;
+    prm.p_out = p_opt;
+    prm.count_out = count_opt;
+    prm.cap = list_cap > 0 ? list_cap : std::max<int64_t>(shape->ctx_len, 1);
     prm.out = out;
     prm.lse = lse;
-    return launch(MODE_SCORE | MODE_SELECT | MODE_ATTEND, *shape, pl, prm, stream);
+    prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
+    prm.src_mode = prm.dense ? 1 : 0;
+    prm.attend = 1;
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    if (!empty && (!prm.dense || s_hat_opt)) {
+        if ((st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
+        if (!prm.dense && (st = launch_select(prm, stream)) != SSA_OK) return st;
+    }
+    return launch_attend(prm, *shape, stream);
 }
 
 ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
@@ -507,13 +528,13 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!q_host || !out_host || !lse_host) return SSA_ERR_INVALID_ARG;
-    if ((st = check_ws(ws, ws_bytes, *shape, 0)) != SSA_OK) return st;
-    const WsLayout wl = ws_layout(*shape, 0);
+    const ssa::Plan pl = make_plan(*shape, false);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     char* w = static_cast<char*>(ws);
     const size_t heads = (size_t)shape->batch * shape->n_q_heads;
-    ssa_bf16* q_dev = reinterpret_cast<ssa_bf16*>(w + wl.hq);
-    float* out_dev = reinterpret_cast<float*>(w + wl.hout);
-    float* lse_dev = reinterpret_cast<float*>(w + wl.hlse);
+    ssa_bf16* q_dev = reinterpret_cast<ssa_bf16*>(w + pl.o_hq);
+    float* out_dev = reinterpret_cast<float*>(w + pl.o_hout);
+    float* lse_dev = reinterpret_cast<float*>(w + pl.o_hlse);
     if (cudaMemcpyAsync(q_dev, q_host, heads * shape->head_dim * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
         cudaGetLastError();
         return SSA_ERR_CUDA;
@@ -537,7 +558,8 @@ ssa_status ssa_decode_static(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
 {
     const ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    if (ws_layout(*shape, 0).total > (size_t)SSA_STATIC_SCRATCH_BYTES) return SSA_ERR_WORKSPACE;
+    const ssa::Plan pl = make_plan(*shape, false);
+    if (pl.total > (size_t)SSA_STATIC_SCRATCH_BYTES) return SSA_ERR_WORKSPACE;
     void* ws = static_scratch_address();
     if (!ws) return SSA_ERR_CUDA;
     // the status word accumulates device flags: start this call from zero
@@ -574,15 +596,15 @@ ssa_status ssa_get_device_status(void* ws, cudaStream_t stream, uint32_t* flags_
     return SSA_OK;
 }
 
-ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* cluster_size, int32_t* scores_resident,
-                          int32_t* smem_bytes)
+ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* tiles_per_unit,
+                          int32_t* attend_ctas_per_unit)
 {
     const ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    const Plan pl = make_plan(MODE_SCORE | MODE_SELECT | MODE_ATTEND, *shape);
-    if (cluster_size) *cluster_size = pl.C;
-    if (scores_resident) *scores_resident = pl.res ? 1 : 0;
-    if (smem_bytes) *smem_bytes = (int32_t)pl.smem;
+    const ssa::Plan pl = make_plan(*shape, true);
+    if (score_ctas) *score_ctas = pl.k1_grid;
+    if (tiles_per_unit) *tiles_per_unit = pl.ntile;
+    if (attend_ctas_per_unit) *attend_ctas_per_unit = attend_split(pl, *shape);
     return SSA_OK;
 }
 

@@ -254,11 +254,11 @@ def ssa_get_device_status(ws: torch.Tensor, stream=None):
 
 
 def ssa_query_plan(shape: ssa_shape):
-    """(cluster size, scores resident in shared memory, dynamic shared memory bytes)."""
+    """(score-kernel CTAs, selection tiles per unit, attention CTAs per unit)."""
     c, r, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(load_library().ssa_query_plan(ctypes.byref(shape), ctypes.byref(c), ctypes.byref(r), ctypes.byref(s)),
            "ssa_query_plan")
-    return c.value, bool(r.value), s.value
+    return c.value, r.value, s.value
 
 
 def default_scale(head_dim: int) -> float:

@@ -53,6 +53,8 @@ def _load():
             i32, i64, u64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
             lib.oracle_orderkey.argtypes = [f32]
             lib.oracle_orderkey.restype = ctypes.c_uint32
+            lib.oracle_bucket_floor.argtypes = [f32]
+            lib.oracle_bucket_floor.restype = f32
             lib.oracle_philox4x32_10.argtypes = [P, P, P]
             lib.oracle_philox4x32_10.restype = None
             lib.oracle_uniform.argtypes = [u64, i64, i32, i32]
@@ -97,6 +99,11 @@ def num_threads() -> int:
 
 def orderkey(x: float) -> int:
     return int(_load().oracle_orderkey(float(x)))
+
+
+def bucket_floor(x: float) -> np.float32:
+    """Lower edge of the bucket of binary32 values sharing x's top 12 order-key bits."""
+    return np.float32(_load().oracle_bucket_floor(float(x)))
 
 
 def philox4x32_10(ctr, key) -> np.ndarray:

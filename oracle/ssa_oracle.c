@@ -37,7 +37,13 @@
  *    dot products taken in double from exact bf16 inputs;
  *  - the deterministic stratum T is the top-k under the total order
  *    (orderkey(s) descending, index ascending);
- *  - m = s of the k-th element of that order (the largest s when k == 0);
+ *  - the reference point m of the exponentials (p does not depend on it)
+ *    is the lower edge of the bucket of the k-th element of that order (the
+ *    largest s when k == 0), the bucket being the set of binary32 values
+ *    sharing the top 12 bits of the order key (sign, exponent and top three
+ *    mantissa bits); m is the smallest value of that bucket, so that
+ *    s_(k) - m < |s_(k)| / 8 and every remainder term is at most
+ *    exp(|s_(k)| / 8);
  *  - e_j = fl32(exp(fl32(s_j - m))) for j in R (the complement of T);
  *  - Z = sum over R of e_j, summed EXACTLY (every fp32 value is an integer
  *    multiple of 2^-149, so the sum is an exact big integer) and rounded to
@@ -84,6 +90,19 @@ uint32_t oracle_orderkey(float x)
     uint32_t u = bits_from_f32(x);
     if (u & 0x80000000u) return ~u;
     return u | 0x80000000u;
+}
+
+/* Inverse of oracle_orderkey. */
+static float value_of_orderkey(uint32_t key)
+{
+    return f32_from_bits((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+/* The smallest binary32 value whose order key shares the top 12 bits with
+ * that of x (the lower edge of x's bucket). */
+float oracle_bucket_floor(float x)
+{
+    return value_of_orderkey(oracle_orderkey(x) & 0xFFF00000u);
 }
 
 /* ------------------------------------------------------------------ */
@@ -138,9 +157,9 @@ float oracle_uniform(uint64_t seed, int64_t j, int32_t h_kv, int32_t b)
 
 /* A non-negative binary32 x equals M * 2^(sh - 149) with M < 2^24 an
  * integer, so x * 2^149 is the integer M << sh.  We keep the running sum
- * of those integers in 8 little-endian 32-bit limbs (256 bits); 2^31 terms
- * of at most 2^150 each stay below 2^181. */
-#define EXACT_LIMBS 8
+ * of those integers in 10 little-endian 32-bit limbs (320 bits); 2^31
+ * terms of at most 2^128 * 2^149 each stay below 2^309. */
+#define EXACT_LIMBS 10
 typedef struct { uint32_t limb[EXACT_LIMBS]; } exact_sum;
 
 static void exact_add(exact_sum* z, float x)
@@ -299,7 +318,7 @@ int64_t oracle_select_unit(const float* s, int64_t N, int64_t top_k, float budge
     /* in_T[i] = 1 for the top-k stratum */
     unsigned char* in_T = (unsigned char*)calloc((size_t)N, 1);
     for (int64_t r = 0; r < k; ++r) in_T[order[r].idx] = 1;
-    const float m = s[order[(k > 0 ? k : 1) - 1].idx];
+    const float m = oracle_bucket_floor(s[order[(k > 0 ? k : 1) - 1].idx]);
 
     /* normaliser over the remainder, summed exactly */
     float* e = (float*)malloc(sizeof(float) * (size_t)N);

@@ -3,7 +3,7 @@
 The GPU computes the scores in fp32, the oracle in double, so the two may
 differ by rounding; the selection can then differ only at its boundaries:
   * top-k boundary: a token whose oracle score is within twice the score
-    tolerance of the oracle's threshold m;
+    tolerance of the oracle's k-th largest score;
   * sampling boundary: |u - p| <= 1e-6 + 3e-5 p (a score perturbation of the
     tolerance moves p by that relative amount).
 Units whose lists agree exactly must agree in out / lse within 2e-3 abs +
@@ -60,12 +60,13 @@ def check_unit(oracle_mod, w, g, b, h, k, B, seed, stats):
     gd = dict(zip(g_idx.tolist(), g_p.tolist()))
     od = dict(zip(o_idx.tolist(), o_p.tolist()))
     diff = set(gd) ^ set(od)
+    kth = float(np.sort(s_ora)[::-1][min(max(k, 1), N) - 1]) if N else 0.0
     for j in diff:
         u = oracle_mod.uniform(seed, j, h, b)
         pj = float(p_all[j])
-        topk_edge = abs(float(s_ora[j]) - float(m)) <= 2 * float(tol[j]) + 1e-30
+        topk_edge = abs(float(s_ora[j]) - kth) <= 2 * float(tol[j]) + 1e-30
         samp_edge = abs(u - pj) <= 1e-6 + 3e-5 * pj
-        assert topk_edge or samp_edge, f"unit ({b},{h}) token {j}: u={u} p={pj} s={s_ora[j]} m={m}"
+        assert topk_edge or samp_edge, f"unit ({b},{h}) token {j}: u={u} p={pj} s={s_ora[j]} kth={kth}"
     stats["boundary"] = stats.get("boundary", 0) + len(diff)
     stats["units"] = stats.get("units", 0) + 1
     if diff:

@@ -17,7 +17,7 @@ DEV = "cuda"
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("plan", [(None, False), (1, False), (4, True), (16, False)])
+@pytest.mark.parametrize("plan", [(None, None), (512, 1), (512, 9), (1024, 64), (2048, 3)])
 def test_decode_parity(oracle_mod, name, plan):
     w = case(name)
     cfg = w["cfg"]

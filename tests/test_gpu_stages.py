@@ -1,5 +1,5 @@
 """GPU parity, stage by stage, against the CPU oracle (small sizes that span
-several tiles, ragged tails and every cluster size).
+several tiles, ragged tails, several selection tile sizes and attention splits).
 
 Tolerances:
   * pack: bit-exact.
@@ -29,16 +29,15 @@ DEV = "cuda"
 
 
 @contextlib.contextmanager
-def plan_env(cluster=None, global_scores=False):
-    old = {k: os.environ.get(k) for k in ("SSA_FORCE_CLUSTER", "SSA_FORCE_GLOBAL_SCORES")}
-    if cluster:
-        os.environ["SSA_FORCE_CLUSTER"] = str(cluster)
-    else:
-        os.environ.pop("SSA_FORCE_CLUSTER", None)
-    if global_scores:
-        os.environ["SSA_FORCE_GLOBAL_SCORES"] = "1"
-    else:
-        os.environ.pop("SSA_FORCE_GLOBAL_SCORES", None)
+def plan_env(tile=None, split=None):
+    """Force the selection tile size (tokens) and the attention split (CTAs per unit)."""
+    keys = ("SSA_FORCE_TILE", "SSA_FORCE_SPLIT")
+    old = {k: os.environ.get(k) for k in keys}
+    for k, v in zip(keys, (tile, split)):
+        if v:
+            os.environ[k] = str(v)
+        else:
+            os.environ.pop(k, None)
     try:
         yield
     finally:
@@ -100,10 +99,10 @@ def test_score_parity(oracle_mod, name):
     assert np.all(np.abs(s_gpu - s_ora) <= tol), np.max(np.abs(s_gpu - s_ora) / tol)
 
 
-def _select_and_compare(oracle_mod, s_np, k, B, seed, cluster=None, global_scores=False, cap=None):
+def _select_and_compare(oracle_mod, s_np, k, B, seed, tile=None, split=None, cap=None):
     s = torch.from_numpy(s_np).to(DEV)
     Bt, Hkv, N = s_np.shape
-    with plan_env(cluster, global_scores):
+    with plan_env(tile, split):
         idx, p, count = ssa.ssa_select(s, k, B, seed, list_cap=cap or 0)
         ws = None
     torch.cuda.synchronize()
@@ -120,19 +119,18 @@ def _select_and_compare(oracle_mod, s_np, k, B, seed, cluster=None, global_score
     return nb
 
 
-@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("global_scores", [False, True])
-def test_select_parity_cluster_sizes(oracle_mod, cluster, global_scores):
+@pytest.mark.parametrize("tile,split", [(None, None), (512, 1), (512, 7), (1024, 3), (2048, 64), (4096, 2)])
+def test_select_parity_tiles_and_splits(oracle_mod, tile, split):
     w = case("g4_d128")
     cfg = w["cfg"]
     q, K, V, Ks, sel = oracle_inputs(w)
     s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
-    nb = _select_and_compare(oracle_mod, s_np, cfg.top_k, cfg.budget, 7, cluster, global_scores)
+    nb = _select_and_compare(oracle_mod, s_np, cfg.top_k, cfg.budget, 7, tile, split)
     assert nb <= 2
 
 
-@pytest.mark.parametrize("cluster", [1, 4, 16])
-def test_select_edge_cases(oracle_mod, cluster):
+@pytest.mark.parametrize("tile,split", [(None, None), (512, 5), (1024, 1)])
+def test_select_edge_cases(oracle_mod, tile, split):
     rng = np.random.default_rng(11)
     Bt, Hkv = 1, 2
     for N, k, B, kind in [
@@ -160,7 +158,7 @@ def test_select_edge_cases(oracle_mod, cluster):
         else:
             s = rng.standard_normal((Bt, Hkv, N)) * 1.5
         s = s.astype(np.float32)
-        nb = _select_and_compare(oracle_mod, s, k, B, 3, cluster)
+        nb = _select_and_compare(oracle_mod, s, k, B, 3, tile, split)
         assert nb <= 2, (N, k, B, kind)
 
 
@@ -177,8 +175,8 @@ def test_select_overflow_flag(oracle_mod):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("cluster", [None, 1, 8])
-def test_attend_parity(oracle_mod, name, cluster):
+@pytest.mark.parametrize("split", [None, 1, 13])
+def test_attend_parity(oracle_mod, name, split):
     w = case(name)
     cfg = w["cfg"]
     q, K, V, Ks, sel = oracle_inputs(w)
@@ -186,7 +184,7 @@ def test_attend_parity(oracle_mod, name, cluster):
     idx = torch.from_numpy(r["idx"]).to(DEV)
     p = torch.from_numpy(r["p"]).to(DEV)
     count = torch.from_numpy(r["count"].astype(np.int32)).to(DEV)
-    with plan_env(cluster):
+    with plan_env(None, split):
         out, lse = ssa.ssa_attend(w["q"], w["K"], w["V"], idx, p, count, cfg.scale)
     out, lse = out.cpu().numpy(), lse.cpu().numpy()
     assert np.allclose(out, r["out"], atol=2e-3, rtol=2e-3), np.abs(out - r["out"]).max()

@@ -12,6 +12,21 @@ import numpy as np
 import pytest
 
 
+def _next_down(x: np.float32) -> np.float32:
+    return np.nextafter(np.float32(x), np.float32(-np.inf), dtype=np.float32)
+
+
+def _check_bucket_floor(oracle_mod, m, v):
+    """m is the smallest binary32 value in v's 12-bit order-key bucket: same top 12 key
+    bits as v, m <= v, and the next value down lies in another bucket; and v - m is at most
+    |v| / 8 (a bucket spans an eighth of an octave; 2^-129 in the subnormal range)."""
+    assert m <= v
+    assert oracle_mod.orderkey(m) >> 20 == oracle_mod.orderkey(v) >> 20
+    below = _next_down(m)
+    assert not np.isfinite(below) or oracle_mod.orderkey(below) >> 20 != oracle_mod.orderkey(v) >> 20
+    assert float(v) - float(m) <= max(abs(float(v)) / 8, 2.0 ** -129)
+
+
 def _order(s):
     # brute force: descending value with -0 below +0, ties by ascending index
     key = [(-(float(v)), -math.copysign(1.0, float(v)) if v == 0 else 0.0, i) for i, v in enumerate(s)]
@@ -34,7 +49,7 @@ def test_topk_matches_brute_force_with_ties(oracle_mod, seed):
         assert idx.tolist() == want
         assert np.all(p == 1.0)
         if 0 < N and k <= N:
-            assert m == s[_order(s)[max(k, 1) - 1]]
+            _check_bucket_floor(oracle_mod, m, s[_order(s)[max(k, 1) - 1]])
 
 
 def test_budget_infinite_selects_everything(oracle_mod):
@@ -52,9 +67,29 @@ def test_k_at_least_n_is_dense(oracle_mod):
 def test_k_zero_uses_the_maximum_as_reference(oracle_mod):
     s = np.random.default_rng(2).standard_normal(100).astype(np.float32)
     idx, p, m, Z, p_all = oracle_mod.select_unit(s, 0, 10.0, 5, 0, 0, want_p_all=True)
-    assert m == s.max()
-    assert Z >= 1.0  # the arg-max term is exp(0) = 1
+    _check_bucket_floor(oracle_mod, m, s.max())
+    assert Z >= 1.0  # the arg-max term is exp(max - m) >= 1
     assert np.all(p_all < 1.0 + 1e-7)
+
+
+@pytest.mark.parametrize("v", [0.25, 1.0, 1.7, 3.14159, -0.3, -2.5, 1e-30, -1e-30, 0.0, -0.0, 1e30, -1e30,
+                               1.4e-45, -1.4e-45, 3.4e38, -3.4e38])
+def test_bucket_floor_is_the_lower_edge_of_the_key_bucket(oracle_mod, v):
+    v = np.float32(v)
+    _check_bucket_floor(oracle_mod, oracle_mod.bucket_floor(v), v)
+    # normal positive powers of two are their own bucket floor: their low key bits are zero
+    if v >= 2.0 ** -126 and float(v) == 2.0 ** math.floor(math.log2(float(v))):
+        assert oracle_mod.bucket_floor(v) == v
+
+
+def test_p_does_not_depend_on_the_reference_point(oracle_mod):
+    # p_j = B exp(s_j - m) / sum_R exp(s_l - m): shifting every score by a power of two that
+    # moves m across buckets leaves p unchanged up to rounding
+    rng = np.random.default_rng(8)
+    s = (rng.standard_normal(3000) * 0.7).astype(np.float32)
+    _, _, m1, _, p1 = oracle_mod.select_unit(s, 30, 60.0, 2, 0, 0, want_p_all=True)
+    _, _, m2, _, p2 = oracle_mod.select_unit(s + np.float32(0.5), 30, 60.0, 2, 0, 0, want_p_all=True)
+    assert np.allclose(p1, p2, rtol=2e-5, atol=1e-12)
 
 
 def test_inclusion_probabilities_sum_to_budget(oracle_mod):
