@@ -2,18 +2,19 @@
 // workspace layout, the per-unit control block and small device helpers.
 //
 // A "unit" is one (batch b, KV head h_kv) pair; u = b * Hkv + h_kv.  One
-// decode step runs five kernels on the caller's stream (programmatic
+// decode step runs four kernels on the caller's stream (programmatic
 // dependent launch lets each start while the previous one drains):
 //   K0 init     zero the per-unit counters and histograms (K1 starts at
 //               once and waits for K0 only before its first histogram flush);
 //   K1 score    every SM streams the key summary (TMA) and scores it on the
 //               tensor cores; order-key histogram; Philox bytes;
-//   K2a bucket  find the bucket of the k-th score, gather its members as
-//               candidates, sum the normaliser over the tokens below it;
-//               the last tile of a unit resolves the exact k-th token;
-//   K2c decide  top-k stratum or Poisson draw for every token, per-tile lists;
-//   K3 attend   split-K gather of the selected K/V rows with the corrected
-//               online softmax; the last CTA of a unit merges the partials.
+//   K2 bucket   find the bucket of the k-th score; list every token above it,
+//               its members (candidates) and the remainder tokens that can
+//               still be drawn; sum the normaliser over the tokens below it;
+//               the last tile of a unit resolves the exact k-th token and Z;
+//   K3 attend   decide every listed token (top-k stratum or the draw u < p),
+//               split-K gather of the kept K/V rows with the corrected online
+//               softmax; the last CTA of a unit merges the partials.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -21,9 +22,13 @@
 #include "ptx.cuh"
 
 // Phase markers: no-ops unless a profiling build defines SSA_MARK(k) to
-// record a timestamp for phase boundary k.
+// record a timestamp for phase boundary k (and SSA_NOTE(k, v) to record a
+// value).
 #ifndef SSA_MARK
 #define SSA_MARK(k) ((void)0)
+#endif
+#ifndef SSA_NOTE
+#define SSA_NOTE(k, v) ((void)0)
 #endif
 
 namespace ssa {
@@ -40,18 +45,20 @@ constexpr int kMaxTiles = 1024;        // K2: tiles per unit at most (the tile g
 constexpr int kSelThreads = 512;       // K2a / K2c block size; each warp owns a slice (a list) of a tile
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int k3Threads = 256;         // K3 block size
+constexpr int kMaxSplit = 64;          // K3 CTAs per unit at most (the workspace is sized for it)
 constexpr int k3Warps = k3Threads / 32;
 constexpr int kQselBytes = 1024;       // B operand: 16 rows x d_sel bf16, swizzled
 
 // Per-unit control block (zeroed by K0).
 struct UnitCtrl {
-    uint32_t k2a_done;   // K2a tiles finished
+    uint32_t k2a_done;   // K2 tiles finished
     uint32_t k3_done;    // K3 CTAs finished
+    uint32_t ncand;      // members of the threshold bucket (the candidate array's length)
     uint32_t theta;      // order key of the k-th largest score
     int32_t idx_cut;     // key == theta and index <= idx_cut: top-k stratum (-1: none)
     float m;             // reference point of the exponentials
     float Z;             // normaliser over the remainder
-    uint32_t pad[10];
+    uint32_t pad[9];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 
@@ -68,9 +75,8 @@ struct Plan {
     int64_t np;          // ntile * tt: padded tokens per unit
     int32_t P;           // K3 CTAs per unit
     // workspace byte offsets
-    size_t o_status, o_ctrl, o_hist1, o_hist2, o_zpart, o_ccount, o_scount, o_cand, o_sel_idx, o_sel_p,
-        o_scores, o_ubuf, o_part, o_hq, o_hout, o_hlse, total;
-    size_t zero_bytes;   // ctrl + hist1 + hist2, contiguous from o_ctrl
+    size_t o_status, o_ctrl, o_hist1, o_zpart, o_scount, o_kept, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf,
+        o_part, o_hq, o_hout, o_hlse, total;
 };
 
 // ---------------------------------------------------------------------------

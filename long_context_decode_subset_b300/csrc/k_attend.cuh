@@ -134,6 +134,19 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
         for (int c = 0; c < DPL; ++c) acc[g][c] = 0.0f;
     }
     unsigned char* wring = smem + (size_t)warp * CF::NS * CF::STAGE_W + (size_t)sub * 2u * CF::ROWB + li * DPL * 2;
+    // the unit's threshold and normaliser (per-tile lists only)
+    uint32_t d_theta = 0;
+    int64_t d_cut = -1;
+    float d_m = 0.0f, d_Z = 0.0f;
+    if (p.src_mode == 0) {
+        const UnitCtrl* ctrl = ws_ctrl(p) + u;
+        d_theta = __ldcg(&ctrl->theta);
+        d_cut = __ldcg(&ctrl->idx_cut);
+        d_m = __ldcg(&ctrl->m);
+        d_Z = __ldcg(&ctrl->Z);
+    }
+    const bool d_sampling = p.budget > 0.0f && d_Z > 0.0f;
+    int64_t kept = 0;   // entries this CTA keeps
 
     for (int64_t c0 = lo; c0 < hi; c0 += CF::CHUNK) {
         const int n = (int)min((int64_t)CF::CHUNK, hi - c0);
@@ -167,32 +180,70 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
                 }
             }
         }
+        // final decisions (per-tile lists): the top-k stratum, then the draw u < p
+        bool kp[PER];
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
             const int i = e * k3Threads + tid;
+            kp[e] = false;
             if (i >= n) continue;
-            const int64_t pos = c0 + i;
-            const int32_t j = jv[e];
-            const float pv = pvv[e];
-            const bool ok = j >= 0 && (int64_t)j < pl.N && pv > 0.0f && pv <= 1.0f;
-            if (!ok) flag(status, DEV_BAD_INDEX);
-            cidx[i] = ok ? j : -1;
-            clp[i] = ok ? logf(pv) : 0.0f;
-            if (p.idx_out) {
-                if (pos < p.cap) {
-                    p.idx_out[(int64_t)u * p.cap + pos] = j;
-                    p.p_out[(int64_t)u * p.cap + pos] = pv;
+            int32_t j = jv[e];
+            float pv = pvv[e];
+            if (p.src_mode == 0) {
+                const bool is_cand = ((uint32_t)j & kCandFlag) != 0u;
+                j = (int32_t)((uint32_t)j & ~kCandFlag);
+                bool keep = false;
+                if (pv == INFINITY) {                     // above the threshold bucket
+                    keep = true;
+                    pv = 1.0f;
                 } else {
-                    flag(status, DEV_OVERFLOW);
+                    float ev = pv;                        // a remainder term ...
+                    if (is_cand) {                        // ... or a candidate's score
+                        const uint32_t k = okey(pv);
+                        if (k > d_theta || (k == d_theta && (int64_t)j <= d_cut)) {
+                            keep = true;
+                            pv = 1.0f;
+                        }
+                        ev = expf(__fsub_rn(pv, d_m));
+                    }
+                    if (!keep) {
+                        pv = d_sampling ? prob_from_term(ev, p.budget, d_Z) : 0.0f;
+                        keep = pv > 0.0f && token_uniform(p.seed, j, h, b) < pv;
+                    }
                 }
+                jv[e] = j;
+                pvv[e] = pv;
+                kp[e] = keep;
+            } else {
+                const bool ok = j >= 0 && (int64_t)j < pl.N && pv > 0.0f && pv <= 1.0f;
+                if (!ok) flag(status, DEV_BAD_INDEX);
+                kp[e] = ok;
             }
         }
+        // keep the chosen entries in list order: cidx / clp[0, nk)
+        int nk = 0;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan<k3Threads>(kp[e] ? 1u : 0u, ks.scan, tot);
+            if (kp[e]) {
+                const int at = nk + (int)ex;
+                cidx[at] = jv[e];
+                clp[at] = logf(pvv[e]);
+                if (p.idx_out) {   // staged for the unit's compact list
+                    uint2* stage = ws_cand(p) + (size_t)u * pl.N + (size_t)(lo + kept);
+                    stage[at] = make_uint2((uint32_t)jv[e], __float_as_uint(pvv[e]));
+                }
+            }
+            nk += (int)tot;
+        }
+        kept += nk;
         __syncthreads();
         if (!p.attend) continue;
-        const int nsteps = (n + CF::RPS - 1) / CF::RPS;
+        const int nsteps = (nk + CF::RPS - 1) / CF::RPS;
         auto issue = [&](int step) {
             const int row = step * CF::RPS + warp * CF::RPW + sub;
-            if (step < nsteps && row < n) {
+            if (step < nsteps && row < nk) {
                 const int32_t j = cidx[row];
                 if (j >= 0) {
                     unsigned char* dst = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
@@ -213,7 +264,7 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
             issue(step + CF::NS - 1);
             cp_async_wait<CF::NS - 1>();
             const int row = step * CF::RPS + warp * CF::RPW + sub;
-            const bool valid = row < n && cidx[row] >= 0;
+            const bool valid = row < nk;
             const float lp = valid ? clp[row] : 0.0f;
             const unsigned char* src = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
             float kf[DPL], vf[DPL];
@@ -326,6 +377,8 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
             }
         }
     }
+    uint32_t* kept_all = ws_kept(p) + (size_t)u * kMaxSplit;
+    if (tid == 0) kept_all[r] = (uint32_t)kept;
     __threadfence();
     __syncthreads();
     if (tid == 0) ks.is_last = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
@@ -333,7 +386,43 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
     SSA_MARK(12);
     if (!ks.is_last) return;
     __threadfence();
-    if (p.count_out && tid == 0) p.count_out[u] = (int32_t)min(total, (int64_t)INT32_MAX);
+    if (p.count_out || p.idx_out) {
+        // the unit's kept entries: prefix over the P CTAs, then (if asked) the
+        // compact list in list order, copied from the per-CTA staging
+        uint32_t* koff = reinterpret_cast<uint32_t*>(smem);   // [P + 1]
+        if (warp == 0) {
+            uint32_t run = 0;
+            for (int r0 = 0; r0 < P; r0 += 32) {
+                const uint32_t v = (r0 + lane < P) ? __ldcg(kept_all + r0 + lane) : 0u;
+                const uint32_t x = warp_incl_scan(v);
+                if (r0 + lane < P) koff[r0 + lane] = run + x - v;
+                run += __shfl_sync(0xffffffffu, x, 31);
+            }
+            if (lane == 0) koff[P] = run;
+        }
+        __syncthreads();
+        const uint32_t kept_total = koff[P];
+        if (p.count_out && tid == 0) p.count_out[u] = (int32_t)kept_total;
+        if (p.idx_out) {
+            const uint2* stage = ws_cand(p) + (size_t)u * pl.N;
+            for (uint32_t o = tid; o < kept_total; o += k3Threads) {
+                int lo_r = 0, hi_r = P;   // koff[lo_r] <= o < koff[hi_r]
+                while (hi_r - lo_r > 1) {
+                    const int mid = (lo_r + hi_r) >> 1;
+                    if (koff[mid] <= o) lo_r = mid; else hi_r = mid;
+                }
+                const int64_t src = total * lo_r / P + (int64_t)(o - koff[lo_r]);
+                const uint2 v = __ldcg(stage + src);
+                if ((int64_t)o < p.cap) {
+                    p.idx_out[(int64_t)u * p.cap + o] = (int32_t)v.x;
+                    p.p_out[(int64_t)u * p.cap + o] = __uint_as_float(v.y);
+                } else {
+                    flag(status, DEV_OVERFLOW);
+                }
+            }
+        }
+        __syncthreads();
+    }
     if (!p.attend) return;
     // merge the P partials in a fixed order: (m, l) through shared memory,
     // then every thread its accumulator elements, loads issued in batches

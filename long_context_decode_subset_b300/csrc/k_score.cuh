@@ -67,9 +67,8 @@ struct Params {
 __device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
 __device__ __forceinline__ UnitCtrl* ws_ctrl(const Params& p) { return reinterpret_cast<UnitCtrl*>(p.ws + p.pl.o_ctrl); }
 __device__ __forceinline__ uint32_t* ws_hist1(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_hist1); }
-__device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_hist2); }
 __device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
-__device__ __forceinline__ uint32_t* ws_ccount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_ccount); }
+__device__ __forceinline__ uint32_t* ws_kept(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_kept); }
 __device__ __forceinline__ uint32_t* ws_scount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_scount); }
 __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
@@ -78,7 +77,7 @@ __device__ __forceinline__ uint8_t* ws_ubuf(const Params& p) { return reinterpre
 __device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
 
 // ---------------------------------------------------------------------------
-// K0: zero the unit's control block and histograms.  One CTA per unit.  It
+// K0: zero the unit's control block and histogram.  One CTA per unit.  It
 // lets the next kernel launch at once: K1 streams the summary meanwhile and
 // waits for K0 only before its first histogram flush.
 // ---------------------------------------------------------------------------
@@ -90,11 +89,7 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
     uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
     if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
     uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);
-    uint4* h2 = reinterpret_cast<uint4*>(ws_hist2(p) + (size_t)u * kBins);
-    for (int i = tid; i < kBins / 4; i += 256) {
-        h1[i] = make_uint4(0, 0, 0, 0);
-        h2[i] = make_uint4(0, 0, 0, 0);
-    }
+    for (int i = tid; i < kBins / 4; i += 256) h1[i] = make_uint4(0, 0, 0, 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -21,7 +21,6 @@ using namespace ssa;
 namespace {
 
 constexpr size_t kStatusBytes = 256;
-constexpr int kMaxSplit = 64;          // K3 CTAs per unit at most (the workspace is sized for it)
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
@@ -79,12 +78,10 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.o_status = take(kStatusBytes);
     pl.o_ctrl = take((size_t)U * sizeof(UnitCtrl));
     pl.o_hist1 = take((size_t)U * kBins * 4);
-    pl.o_hist2 = take((size_t)U * kBins * 4);
-    pl.zero_bytes = o - pl.o_ctrl;
     pl.o_zpart = take((size_t)U * pl.ntile * 8);
-    pl.o_ccount = take((size_t)U * nl * 4);
     pl.o_scount = take((size_t)U * nl * 4);
-    pl.o_cand = take((size_t)U * pl.np * 8);
+    pl.o_kept = take((size_t)U * kMaxSplit * 4);
+    pl.o_cand = take((size_t)U * N * 8);
     pl.o_sel_idx = take((size_t)U * pl.np * 4);
     pl.o_sel_p = take((size_t)U * pl.np * 4);
     pl.o_scores = take((size_t)U * N * 4);
@@ -259,10 +256,7 @@ ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cud
 
 ssa_status launch_select(const ssa::Params& p, cudaStream_t stream)
 {
-    const int64_t grid = (int64_t)p.pl.U * p.pl.ntile;
-    ssa_status st = launch(&bucket_kernel, grid, kSelThreads, k2a_smem_bytes(p.pl.ntile * kSelWarps), p, stream, true);
-    if (st != SSA_OK) return st;
-    return launch(&decide_kernel, grid, kSelThreads, 0, p, stream, true);
+    return launch(&bucket_kernel, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, k2_smem_bytes(), p, stream, true);
 }
 
 // CTAs of `fn` resident per SM (cached per kernel and shared-memory size).
