@@ -126,8 +126,9 @@ const char* ssa_status_string(int status);
 int ssa_version(void);
 
 /* Bytes of device workspace every entry point below needs for this shape
- * (about 21 bytes per cached token plus 32 KB per unit: scores, candidate
- * and selection lists sized for the worst case, Philox bytes, histograms).
+ * (about 22 bytes per cached token plus 32 KB per unit: scores, candidate
+ * and selection lists sized for the worst case, 16-bit Philox prefixes,
+ * histograms).
  * Independent of the stream, the device and list_cap (kept for symmetry with
  * the calls that take a list capacity); 0 on invalid input. */
 size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap);

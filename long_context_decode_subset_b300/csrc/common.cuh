@@ -7,7 +7,7 @@
 //   K0 init     zero the per-unit counters and histograms (K1 starts at
 //               once and waits for K0 only before its first histogram flush);
 //   K1 score    every SM streams the key summary (TMA) and scores it on the
-//               tensor cores; order-key histogram; Philox bytes;
+//               tensor cores; order-key histogram; 16-bit Philox prefixes;
 //   K2 bucket   find the bucket of the k-th score; list every token above it,
 //               its members (candidates) and the remainder tokens that can
 //               still be drawn; sum the normaliser over the tokens below it;
@@ -26,6 +26,12 @@
 // value).
 #ifndef SSA_MARK
 #define SSA_MARK(k) ((void)0)
+#endif
+#ifndef SSA_GT
+#define SSA_GT(k) ((void)0)
+#endif
+#ifndef SSA_MARKW
+#define SSA_MARKW(k) ((void)0)
 #endif
 #ifndef SSA_NOTE
 #define SSA_NOTE(k, v) ((void)0)
@@ -58,7 +64,8 @@ struct UnitCtrl {
     int32_t idx_cut;     // key == theta and index <= idx_cut: top-k stratum (-1: none)
     float m;             // reference point of the exponentials
     float Z;             // normaliser over the remainder
-    uint32_t pad[9];
+    uint32_t k1_next;    // unit 0 only: K1's shared stage queue (stages taken)
+    uint32_t pad[8];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 
@@ -68,6 +75,7 @@ struct Plan {
     int32_t G;           // query heads per KV head
     int64_t N;           // tokens per unit
     int32_t nst;         // K1 stages per unit
+    int32_t sf;          // K1 stages per unit split statically over the CTAs (the rest are queued)
     int64_t stages;      // K1 stages in all
     int32_t k1_grid;     // K1 CTAs (persistent)
     int32_t tt;          // K2 tile tokens (multiple of kTileTok)

@@ -41,6 +41,7 @@ struct K3Cfg {
     static constexpr uint32_t OFF_CHUNK = RING > MERGE ? RING : MERGE;
     static constexpr int CHUNK = 1024;                        // list entries staged at a time
     static constexpr uint32_t OFF_PRE = OFF_CHUNK + (uint32_t)CHUNK * 8u;
+    static_assert(OFF_CHUNK >= (uint32_t)CHUNK * 8u, "the raw chunk staging fits in front of the kept lists");
 };
 
 // Dynamic shared memory of K3 for nlists per-tile lists.
@@ -78,24 +79,27 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
     const int nlists = pl.ntile * kSelWarps;   // K2c writes one list per warp slice of a tile
     const int W2 = pl.tt / kSelWarps;
     uint32_t* status = ws_status(p);
+    SSA_GT(4);
     grid_dep_wait();
     SSA_MARK(7);
+    SSA_GT(5);
 
     // the unit's list length and (per-tile lists) its prefix over the lists
     int64_t total = 0;
     if (p.src_mode == 0) {
         const uint32_t* sc = ws_scount(p) + (size_t)u * nlists;
+#pragma unroll 1
+        for (int l = tid; l < nlists; l += k3Threads) cp_async_4(pre + l, sc + l);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
         const int l0 = nlists * tid / k3Threads, l1 = nlists * (tid + 1) / k3Threads;
         uint32_t mine = 0;
-        for (int l = l0; l < l1; l += 32) {
-            uint32_t c[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) c[j] = (l + j < l1) ? __ldcg(sc + l + j) : 0u;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (l + j < l1) pre[l + j] = mine;
-                mine += c[j];
-            }
+#pragma unroll 1
+        for (int l = l0; l < l1; ++l) {
+            const uint32_t c = pre[l];
+            pre[l] = mine;
+            mine += c;
         }
         uint32_t tot;
         const uint32_t before = block_excl_scan<k3Threads>(mine, ks.scan, tot);
@@ -151,92 +155,104 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
     for (int64_t c0 = lo; c0 < hi; c0 += CF::CHUNK) {
         const int n = (int)min((int64_t)CF::CHUNK, hi - c0);
         __syncthreads();   // the previous chunk is consumed
-        constexpr int PER = CF::CHUNK / k3Threads;   // entries per thread, loaded at once
-        int32_t jv[PER];
-        float pvv[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            const int i = e * k3Threads + tid;
-            const int64_t pos = c0 + i;
-            jv[e] = -1;
-            pvv[e] = 0.0f;
-            if (i < n) {
-                if (p.src_mode == 0) {
-                    int lo_l = 0, hi_l = nlists;   // pre[lo_l] <= pos < pre[hi_l]
-                    while (hi_l - lo_l > 1) {
-                        const int mid = (lo_l + hi_l) >> 1;
-                        if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
-                    }
-                    const size_t at =
-                        (size_t)(lo_l / kSelWarps) * pl.tt + (size_t)(lo_l % kSelWarps) * W2 + (pos - pre[lo_l]);
-                    jv[e] = __ldcg(sidx + at);
-                    pvv[e] = __ldcg(sp + at);
-                } else if (p.src_mode == 1) {
-                    jv[e] = (int32_t)pos;
-                    pvv[e] = 1.0f;
-                } else {
-                    jv[e] = p.idx_in[(int64_t)u * p.cap + pos];
-                    pvv[e] = p.p_in[(int64_t)u * p.cap + pos];
+        constexpr int PER = CF::CHUNK / k3Threads;   // consecutive entries per thread
+        // the chunk's raw entries into shared memory (cp.async, one wave)
+        int32_t* ridx = reinterpret_cast<int32_t*>(smem);
+        float* rval = reinterpret_cast<float*>(smem + CF::CHUNK * 4);
+        if (p.src_mode == 0) {
+#pragma unroll 1
+            for (int i = tid; i < n; i += k3Threads) {
+                const int64_t pos = c0 + i;
+                int lo_l = 0, hi_l = nlists;   // pre[lo_l] <= pos < pre[hi_l]
+                while (hi_l - lo_l > 1) {
+                    const int mid = (lo_l + hi_l) >> 1;
+                    if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
                 }
+                const size_t at = (size_t)(lo_l / kSelWarps) * pl.tt + (size_t)(lo_l % kSelWarps) * W2 + (pos - pre[lo_l]);
+                cp_async_4(ridx + i, sidx + at);
+                cp_async_4(rval + i, sp + at);
+            }
+        } else if (p.src_mode == 2) {
+#pragma unroll 1
+            for (int i = tid; i < n; i += k3Threads) {
+                cp_async_4(ridx + i, p.idx_in + (int64_t)u * p.cap + c0 + i);
+                cp_async_4(rval + i, p.p_in + (int64_t)u * p.cap + c0 + i);
             }
         }
-        // final decisions (per-tile lists): the top-k stratum, then the draw u < p
-        bool kp[PER];
-#pragma unroll
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        SSA_MARK(28);
+        // final decisions for this thread's PER consecutive entries (per-tile
+        // lists: the top-k stratum, then the draw u < p); one bit each
+        uint32_t kbits = 0, kcount = 0;
+#pragma unroll 1
         for (int e = 0; e < PER; ++e) {
-            const int i = e * k3Threads + tid;
-            kp[e] = false;
-            if (i >= n) continue;
-            int32_t j = jv[e];
-            float pv = pvv[e];
-            if (p.src_mode == 0) {
-                const bool is_cand = ((uint32_t)j & kCandFlag) != 0u;
-                j = (int32_t)((uint32_t)j & ~kCandFlag);
-                bool keep = false;
-                if (pv == INFINITY) {                     // above the threshold bucket
-                    keep = true;
-                    pv = 1.0f;
-                } else {
-                    float ev = pv;                        // a remainder term ...
-                    if (is_cand) {                        // ... or a candidate's score
-                        const uint32_t k = okey(pv);
-                        if (k > d_theta || (k == d_theta && (int64_t)j <= d_cut)) {
-                            keep = true;
-                            pv = 1.0f;
-                        }
-                        ev = expf(__fsub_rn(pv, d_m));
-                    }
-                    if (!keep) {
-                        pv = d_sampling ? prob_from_term(ev, p.budget, d_Z) : 0.0f;
-                        keep = pv > 0.0f && token_uniform(p.seed, j, h, b) < pv;
-                    }
-                }
-                jv[e] = j;
-                pvv[e] = pv;
-                kp[e] = keep;
+            const int i = tid * PER + e;
+            if (i >= n) break;
+            int32_t j;
+            float pv;
+            bool keep;
+            if (p.src_mode == 1) {
+                j = (int32_t)(c0 + i);
+                pv = 1.0f;
+                keep = true;
             } else {
-                const bool ok = j >= 0 && (int64_t)j < pl.N && pv > 0.0f && pv <= 1.0f;
-                if (!ok) flag(status, DEV_BAD_INDEX);
-                kp[e] = ok;
+                j = ridx[i];
+                pv = rval[i];
+                if (p.src_mode == 0) {
+                    const bool is_cand = ((uint32_t)j & kCandFlag) != 0u;
+                    j = (int32_t)((uint32_t)j & ~kCandFlag);
+                    keep = false;
+                    if (pv == INFINITY) {                     // above the threshold bucket
+                        keep = true;
+                        pv = 1.0f;
+                    } else {
+                        float ev = pv;                        // a remainder term ...
+                        if (is_cand) {                        // ... or a candidate's score
+                            const uint32_t k = okey(pv);
+                            if (k > d_theta || (k == d_theta && (int64_t)j <= d_cut)) {
+                                keep = true;
+                                pv = 1.0f;
+                            }
+                            ev = expf(__fsub_rn(pv, d_m));
+                        }
+                        if (!keep) {
+                            pv = d_sampling ? prob_from_term(ev, p.budget, d_Z) : 0.0f;
+                            keep = pv > 0.0f && token_uniform(p.seed, j, h, b) < pv;
+                        }
+                    }
+                } else {
+                    keep = j >= 0 && (int64_t)j < pl.N && pv > 0.0f && pv <= 1.0f;
+                    if (!keep) flag(status, DEV_BAD_INDEX);
+                }
+                ridx[i] = j;
+                rval[i] = pv;
+            }
+            if (keep) {
+                kbits |= 1u << e;
+                ++kcount;
             }
         }
         // keep the chosen entries in list order: cidx / clp[0, nk)
-        int nk = 0;
-#pragma unroll
+        uint32_t nk_u;
+        uint32_t at = block_excl_scan<k3Threads>(kcount, ks.scan, nk_u);
+        const int nk = (int)nk_u;
+#pragma unroll 1
         for (int e = 0; e < PER; ++e) {
-            uint32_t tot;
-            const uint32_t ex = block_excl_scan<k3Threads>(kp[e] ? 1u : 0u, ks.scan, tot);
-            if (kp[e]) {
-                const int at = nk + (int)ex;
-                cidx[at] = jv[e];
-                clp[at] = logf(pvv[e]);
-                if (p.idx_out) {   // staged for the unit's compact list
-                    uint2* stage = ws_cand(p) + (size_t)u * pl.N + (size_t)(lo + kept);
-                    stage[at] = make_uint2((uint32_t)jv[e], __float_as_uint(pvv[e]));
-                }
+            if (!((kbits >> e) & 1u)) continue;
+            const int i = tid * PER + e;
+            const int32_t j = (p.src_mode == 1) ? (int32_t)(c0 + i) : ridx[i];
+            const float pv = (p.src_mode == 1) ? 1.0f : rval[i];
+            cidx[at] = j;
+            clp[at] = logf(pv);
+            if (p.idx_out) {   // staged for the unit's compact list
+                uint2* stage = ws_cand(p) + (size_t)u * pl.N + (size_t)(lo + kept);
+                stage[at] = make_uint2((uint32_t)j, __float_as_uint(pv));
             }
-            nk += (int)tot;
+            ++at;
         }
+        SSA_MARK(29);
         kept += nk;
         __syncthreads();
         if (!p.attend) continue;
@@ -384,6 +400,7 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
     if (tid == 0) ks.is_last = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
     __syncthreads();
     SSA_MARK(12);
+    SSA_GT(6);
     if (!ks.is_last) return;
     __threadfence();
     if (p.count_out || p.idx_out) {
@@ -423,53 +440,59 @@ __global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant
         }
         __syncthreads();
     }
+    SSA_MARK(14);
     if (!p.attend) return;
-    // merge the P partials in a fixed order: (m, l) through shared memory,
-    // then every thread its accumulator elements, loads issued in batches
+    // merge the P partials in a fixed order (r ascending).  Every thread owns
+    // G * D / k3Threads accumulator elements of one head g and reads that
+    // head's (m, l) of all P partials itself, so the merge is one wave of
+    // loads and no block barrier.
     const float* parts = ws_part(p) + (size_t)u * P * (size_t)(G * D + 2 * G);
     constexpr int PS = G * D + 2 * G;   // floats per partial
-    float* pm = reinterpret_cast<float*>(smem);        // [P][G] m, then weights exp(m - M)
-    float* pl_ = pm + (size_t)P * G;                   // [P][G] l
-    float* gM = pl_ + (size_t)P * G;                   // [G] max m
-    float* gL = gM + G;                                // [G] merged l
-    __syncthreads();
-    for (int i = tid; i < P * G; i += k3Threads) {
-        const int rr = i / G, g = i % G;
-        pm[i] = __ldcg(parts + (size_t)rr * PS + G * D + g);
-        pl_[i] = __ldcg(parts + (size_t)rr * PS + G * D + G + g);
-    }
-    __syncthreads();
-    if (tid < G) {
+    constexpr int EPT = (G * D + k3Threads - 1) / k3Threads;   // elements per thread (same head)
+    static_assert((G * D) % k3Threads == 0 || G * D < k3Threads, "elements split evenly");
+    const int e0 = tid * EPT;
+    if (e0 < G * D) {
+        const int g = e0 / D;
         float M = -INFINITY;
-        for (int rr = 0; rr < P; ++rr) M = fmaxf(M, pm[rr * G + tid]);
-        float Ls = 0.0f;
-        for (int rr = 0; rr < P; ++rr) {
-            const float mr = pm[rr * G + tid];
-            const float wgt = (M == -INFINITY || mr == -INFINITY) ? 0.0f : expf(mr - M);
-            pm[rr * G + tid] = wgt;
-            Ls = fmaf(pl_[rr * G + tid], wgt, Ls);
-        }
-        gM[tid] = M;
-        gL[tid] = Ls;
-    }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += k3Threads) {
-        const int g = i / D, c = i % D;
-        float A = 0.0f;
         for (int r0 = 0; r0 < P; r0 += 16) {
-            float a[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) a[j] = (r0 + j < P) ? __ldcg(parts + (size_t)(r0 + j) * PS + i) : 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                if (r0 + j < P) A = fmaf(a[j], pm[(r0 + j) * G + g], A);
+                if (r0 + j < P) M = fmaxf(M, __ldcg(parts + (size_t)(r0 + j) * PS + G * D + g));
         }
-        const float Ls = gL[g];
+        float Ls = 0.0f, A[EPT];
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
+        if (M != -INFINITY) {
+            for (int r0 = 0; r0 < P; r0 += 8) {
+                float mr[8], lr[8], ar[8][EPT];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float* pr = parts + (size_t)(r0 + j) * PS;
+                    const bool ok = r0 + j < P;
+                    mr[j] = ok ? __ldcg(pr + G * D + g) : -INFINITY;
+                    lr[j] = ok ? __ldcg(pr + G * D + G + g) : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) ar[j][e] = ok ? __ldcg(pr + e0 + e) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float wgt = (mr[j] == -INFINITY) ? 0.0f : expf(mr[j] - M);
+                    Ls = fmaf(lr[j], wgt, Ls);
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) A[e] = fmaf(ar[j][e], wgt, A[e]);
+                }
+            }
+        }
         const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + g;
-        p.out[head * D + c] = (Ls > 0.0f) ? A / Ls : 0.0f;
-        if (c == 0) p.lse[head] = (Ls > 0.0f) ? gM[g] + logf(Ls) : -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            const int c = (e0 + e) % D;
+            p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
+            if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
+        }
     }
     SSA_MARK(9);
+    SSA_GT(7);
 }
 
 // Append-time summary: Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]].

@@ -9,15 +9,18 @@
 //  * The GQA group's query heads are combined by max:
 //        s_i = fl32(scale * max_g sum_j q_g[S_ch[j]] * Ks[i][j]).
 //  * Philox4x32-10 (Salmon et al., SC'11) draws each token's uniform; K1
-//    keeps the top 8 bits of word 0 so that the decision kernel recomputes
-//    the full word only for the few tokens whose probability falls in the
-//    same 1/256 interval.
+//    keeps the top 16 bits of word 0, a lower bound of u to 2^-16, so that
+//    the bucket pass lists only the tokens that can be drawn and the
+//    attention kernel recomputes the full word for those few.
 //
-// K1 is persistent (one CTA per SM, the unit x 512-token stages split evenly
-// over the CTAs) and warp-specialised:
-//   warp 0   issues the TMA copies: two 256-token boxes of the summary per
-//            stage (swizzled to the 64- or 32-byte row width so that the
-//            tensor cores read them as K-major operands), into a ring;
+// K1 is persistent (one CTA per SM; three quarters of every unit's
+// 512-token stages split evenly over the CTAs, the rest a shared queue that
+// CTAs drain as they finish, since SMs stream at different rates) and
+// warp-specialised:
+//   warp 0   takes the stages, publishes each one's (unit, j) and issues its
+//            TMA copies: two 256-token boxes of the summary (swizzled to the
+//            64- or 32-byte row width so that the tensor cores read them as
+//            K-major operands), into a ring;
 //   warp 3   writes each stage's 1 KB query operand (the unit's G query
 //            heads on the summary channels, same swizzle) beside it;
 //   warp 1   issues tcgen05.mma (M = 128 tokens, N = 16 query-head slots,
@@ -28,7 +31,7 @@
 //   warps 4-19 (four warpgroups, one per 128-token tile) read the
 //            accumulators back (tcgen05.ld), take the max over the G heads,
 //            write the scores, count the top 12 order-key bits per unit, and
-//            draw the Philox bytes.
+//            draw the 16-bit Philox prefixes.
 #pragma once
 #include "common.cuh"
 
@@ -67,17 +70,19 @@ struct Params {
 __device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
 __device__ __forceinline__ UnitCtrl* ws_ctrl(const Params& p) { return reinterpret_cast<UnitCtrl*>(p.ws + p.pl.o_ctrl); }
 __device__ __forceinline__ uint32_t* ws_hist1(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_hist1); }
+// level-2 histogram (the next 12 key bits of the threshold bucket's members), [U][kBins]
+__device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return ws_hist1(p) + (size_t)p.pl.U * kBins; }
 __device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
 __device__ __forceinline__ uint32_t* ws_kept(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_kept); }
 __device__ __forceinline__ uint32_t* ws_scount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_scount); }
 __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
-__device__ __forceinline__ uint8_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint8_t*>(p.ws + p.pl.o_ubuf); }
+__device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
 __device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
 
 // ---------------------------------------------------------------------------
-// K0: zero the unit's control block and histogram.  One CTA per unit.  It
+// K0: zero the unit's control block and histograms.  One CTA per unit.  It
 // lets the next kernel launch at once: K1 streams the summary meanwhile and
 // waits for K0 only before its first histogram flush.
 // ---------------------------------------------------------------------------
@@ -89,15 +94,21 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
     uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
     if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
     uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);
-    for (int i = tid; i < kBins / 4; i += 256) h1[i] = make_uint4(0, 0, 0, 0);
+    uint4* h2 = reinterpret_cast<uint4*>(ws_hist2(p) + (size_t)u * kBins);
+    for (int i = tid; i < kBins / 4; i += 256) {
+        h1[i] = make_uint4(0, 0, 0, 0);
+        h2[i] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 // ---------------------------------------------------------------------------
 // K1: scores
 // ---------------------------------------------------------------------------
 
-constexpr int k1Threads = 640;   // warps 0-3: copies, MMA, tensor memory, query operand; 4-19: epilogue
+constexpr int k1Threads = 640;   // warp 0: copies; 1: MMA; 2: tensor memory; 3: query operand; 4-19: epilogue
 constexpr int k1EpiThreads = 512;
+constexpr int kGrab = 2;         // stages a CTA takes from the shared queue at a time
+constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages + accumulator buffers)
 
 template <int DSEL>
 struct K1Cfg {
@@ -110,13 +121,76 @@ struct K1Cfg {
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 16);
     static constexpr uint32_t OFF_BOP = (uint32_t)S * STAGE;
     static constexpr uint32_t OFF_HIST = OFF_BOP + (uint32_t)S * kQselBytes;
-    static constexpr uint32_t OFF_BAR = OFF_HIST + kBins * 4;
-    static constexpr uint32_t SMEM = OFF_BAR + (2u * S + 2u * NB) * 8u + 16u + 1024u;   // + alignment slack
+    static constexpr uint32_t OFF_QROWS = OFF_HIST + kBins * 4;                 // G query rows (<= 2 KB)
+    static constexpr uint32_t OFF_INFO = OFF_QROWS + 2048u;                     // kInfo stage descriptors
+    static constexpr uint32_t OFF_BAR = OFF_INFO + kInfo * 8u;
+    static constexpr uint32_t SMEM = OFF_BAR + (3u * S + 2u * NB) * 8u + 16u + 1024u;   // + alignment slack
     static_assert(STAGE % 1024 == 0, "stages keep the swizzle atoms aligned");
+    static_assert(kInfo > S + NB, "a descriptor outlives its stage's epilogue");
 };
 
 template <int DSEL>
 constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL>::SMEM; }
+
+// K1's work: every unit's stages j < sf are split evenly and contiguously over
+// the CTAs in (unit, j) order; the stages j >= sf of all units form a queue, in
+// (unit, j) order, that the CTAs drain kGrab at a time once their own share is
+// done (a counter in unit 0's control block, zeroed by K0), so that CTAs that
+// stream faster take more of it.
+struct K1Sched {
+    int64_t s_cur, s_end;      // this CTA's static stages [s_cur, s_end)
+    int64_t d_cur, d_end;      // the current queue chunk
+    int64_t pending;           // the next chunk's start (a grab in flight), or -1
+    int32_t sf, nd;            // static / queued stages per unit
+    int64_t dtotal;            // queued stages in all
+    uint32_t* counter;
+    bool waited;
+
+    __device__ void init(const Plan& pl, uint32_t* ctr)
+    {
+        sf = pl.sf;
+        nd = pl.nst - pl.sf;
+        dtotal = (int64_t)pl.U * nd;
+        const int64_t st = (int64_t)pl.U * sf;
+        s_cur = st * blockIdx.x / gridDim.x;
+        s_end = st * (blockIdx.x + 1) / gridDim.x;
+        d_cur = d_end = 0;
+        pending = -1;
+        counter = ctr;
+        waited = false;
+    }
+    __device__ int64_t grab()
+    {
+        if (!waited) {
+            grid_dep_wait();   // K0 has zeroed the counter
+            waited = true;
+        }
+        return (int64_t)atomicAdd(counter, (uint32_t)kGrab);
+    }
+    // the next stage (unit, j); false at the end of the work
+    __device__ bool next(int& u, int& j)
+    {
+        if (s_cur < s_end) {
+            const int64_t g = s_cur++;
+            u = (int)(g / sf);
+            j = (int)(g % sf);
+            if (s_cur + 1 >= s_end && pending < 0 && dtotal > 0) pending = grab();   // one stage ahead
+            return true;
+        }
+        if (d_cur == d_end) {
+            if (dtotal == 0) return false;
+            if (pending < 0) pending = grab();
+            if (pending >= dtotal) return false;
+            d_cur = pending;
+            d_end = min(pending + kGrab, dtotal);
+            pending = grab();   // the next chunk's grab goes out now
+        }
+        const int64_t d = d_cur++;
+        u = (int)(d / nd);
+        j = sf + (int)(d % nd);
+        return true;
+    }
+};
 
 template <int G, int DSEL, bool HIST, bool UBUF>
 __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_constant__ Params p)
@@ -129,23 +203,24 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     unsigned char* ring = smem;
     unsigned char* bop = smem + CF::OFF_BOP;
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + CF::OFF_HIST);
+    uint16_t* qrows = reinterpret_cast<uint16_t*>(smem + CF::OFF_QROWS);
+    int2* info = reinterpret_cast<int2*>(smem + CF::OFF_INFO);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + NB;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + NB);
+    uint64_t* ready = tempty + NB;   // a stage's (unit, j) is published
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(ready + S);
 
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t g0 = pl.stages * blockIdx.x / gridDim.x;
-    const int64_t g1 = pl.stages * (blockIdx.x + 1) / gridDim.x;
-    const int nstage = (int)(g1 - g0);
     uint32_t* status = ws_status(p);
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 2);    // the summary copies (with their bytes) + the query operand
             mbar_init(&empty[i], 1);
+            mbar_init(&ready[i], 1);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&tfull[i], 1);
@@ -158,6 +233,32 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
         for (int i = tid; i < kBins; i += k1Threads) hist[i] = 0u;
     }
     if (warp == 2) tmem_alloc(tslot, CF::TCOLS);
+    // the query operand's inputs: the G query rows and the channel list of a
+    // unit (the first unit's fetched before the summary copies start, so that
+    // they do not queue behind them)
+    constexpr int QPL = G >= 2 ? G / 2 : 1;   // 16-byte pieces of the G rows per lane (d <= 128)
+    const int nch = G * p.d / 8;
+    uint4 nq[QPL];
+    int nsel = 0;
+    auto fetch_q = [&](int uu) {
+        const int bb = uu / p.Hkv, hh = uu % p.Hkv;
+        const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + ((int64_t)bb * p.Hq + (int64_t)hh * G) * p.d);
+#pragma unroll
+        for (int i = 0; i < QPL; ++i) {
+            const int ci = lane + 32 * i;
+            nq[i] = (ci < nch) ? __ldg(qsrc + ci) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        nsel = (lane < DSEL) ? __ldg(p.sel_ch + (int64_t)hh * DSEL + lane) : 0;
+    };
+    int first_u = -1;
+    if (warp == 3) {
+        const int64_t st = (int64_t)pl.U * pl.sf;
+        const int64_t g0 = st * blockIdx.x / gridDim.x;
+        if (g0 < st * (blockIdx.x + 1) / gridDim.x) {
+            first_u = (int)(g0 / pl.sf);
+            fetch_q(first_u);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -165,16 +266,24 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     SSA_MARK(0);
 
     if (warp == 0) {
+        // lane 0 takes the stages, publishes each one's (unit, j) and issues
+        // its TMA copies (two 256-token boxes)
         if (lane == 0) {
+            K1Sched sch;
+            sch.init(pl, &ws_ctrl(p)[0].k1_next);
             const uint64_t pol = l2_policy_evict_first();
-            int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
-            for (int c = 0; c < nstage; ++c, ++j) {
-                if (j == pl.nst) {
-                    j = 0;
-                    ++u;
-                }
+#pragma unroll 1
+            for (int c = 0;; ++c) {
                 const int st = c % S;
                 if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+                int u = -1, j = 0;
+                if (!sch.next(u, j)) u = -1;
+                info[c % kInfo] = make_int2(u, j);
+                mbar_arrive(&ready[st]);
+                if (u < 0) {
+                    mbar_arrive(&full[st]);   // the end marker carries no copies
+                    break;
+                }
                 const int b = u / p.Hkv, h = u % p.Hkv;
                 mbar_arrive_expect_tx(&full[st], CF::STAGE);
                 unsigned char* dst = ring + (size_t)st * CF::STAGE;
@@ -182,36 +291,45 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
                 tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
             }
         }
+        SSA_MARKW(22);
     } else if (warp == 3) {
-        // the query operand of each stage's unit: row g < G = q_g[S_ch[j]] over j,
-        // rows G..15 zero, K-major in the 64/32-byte swizzled layout the TMA
-        // writes for the summary.  Lane l builds half of row l / 2.
+        // the stage's query operand: row g < G = q_g[S_ch[j]] over j, rows
+        // G..15 zero, K-major in the 64/32-byte swizzled layout the TMA writes
+        // for the summary (lane l builds half of row l / 2)
         constexpr int HALF = DSEL / 2;   // channels per lane: 16 or 8 (two or one 16-byte chunks)
         const int r = lane >> 1, hf = lane & 1;
         uint4 vals[HALF / 8];
         int cur_u = -1;
-        int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
-        for (int c = 0; c < nstage; ++c, ++j) {
-            if (j == pl.nst) {
-                j = 0;
-                ++u;
-            }
+#pragma unroll 1
+        for (int c = 0;; ++c) {
             const int st = c % S;
+            if (lane == 0 && !mbar_wait_bounded(&ready[st], (uint32_t)(c / S) & 1u)) flag(status, DEV_TIMEOUT);
+            __syncwarp();
+            const int u = info[c % kInfo].x;
+            if (u < 0) {
+                if (lane == 0) mbar_arrive(&full[st]);
+                break;
+            }
             if (u != cur_u) {
+                if (u != first_u || cur_u >= 0) fetch_q(u);
                 cur_u = u;
-                const int b = u / p.Hkv, h = u % p.Hkv;
+                // stage the unit's rows, then gather the channels
+#pragma unroll
+                for (int i = 0; i < QPL; ++i) {
+                    const int ci = lane + 32 * i;
+                    if (ci < nch) reinterpret_cast<uint4*>(qrows)[ci] = nq[i];
+                }
+                int sel = nsel;
+                if ((unsigned)sel >= (unsigned)p.d) {
+                    if (lane < DSEL) flag(status, DEV_BAD_INDEX);
+                    sel = 0;
+                }
+                __syncwarp();
                 uint16_t v[HALF];
 #pragma unroll
                 for (int k = 0; k < HALF; ++k) {
-                    v[k] = 0;
-                    if (r < G) {
-                        int ch = p.sel_ch[(int64_t)h * DSEL + hf * HALF + k];
-                        if ((unsigned)ch >= (unsigned)p.d) {
-                            flag(status, DEV_BAD_INDEX);
-                            ch = 0;
-                        }
-                        v[k] = p.q[((int64_t)b * p.Hq + (int64_t)h * G + r) * p.d + ch];
-                    }
+                    const int ch = __shfl_sync(0xffffffffu, sel, hf * HALF + k);
+                    v[k] = (r < G) ? qrows[r * p.d + ch] : (uint16_t)0;
                 }
 #pragma unroll
                 for (int q8 = 0; q8 < HALF / 8; ++q8)
@@ -219,8 +337,8 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
                                           (uint32_t)v[q8 * 8 + 2] | ((uint32_t)v[q8 * 8 + 3] << 16),
                                           (uint32_t)v[q8 * 8 + 4] | ((uint32_t)v[q8 * 8 + 5] << 16),
                                           (uint32_t)v[q8 * 8 + 6] | ((uint32_t)v[q8 * 8 + 7] << 16));
+                __syncwarp();
             }
-            if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
             unsigned char* row = bop + (size_t)st * kQselBytes + (size_t)r * CF::ROW;
 #pragma unroll
             for (int q8 = 0; q8 < HALF / 8; ++q8) {
@@ -235,10 +353,15 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t ring_a = smem_addr(ring), bop_a = smem_addr(bop);
-            for (int c = 0; c < nstage; ++c) {
+#pragma unroll 1
+            for (int c = 0;; ++c) {
                 const int st = c % S, nb = c % NB;
                 if (!mbar_wait_bounded(&full[st], (uint32_t)(c / S) & 1u)) flag(status, DEV_TIMEOUT);
                 if (c >= NB && !mbar_wait_bounded(&tempty[nb], (uint32_t)((c / NB) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+                if (info[c % kInfo].x < 0) {   // end of the work: pass the marker on
+                    mbar_arrive(&tfull[nb]);
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t a0 = ring_a + (uint32_t)st * CF::STAGE;
                 const uint32_t b0 = bop_a + (uint32_t)st * kQselBytes;
@@ -260,7 +383,7 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
         const int tile = (warp - 4) >> 2, quarter = warp & 3, etid = tid - 128;
         const uint32_t k0 = (uint32_t)(p.seed & 0xffffffffu), k1 = (uint32_t)(p.seed >> 32);
         uint32_t* hist1 = ws_hist1(p);
-        uint8_t* ubuf = ws_ubuf(p);
+        uint16_t* ubuf = ws_ubuf(p);
         int cur_u = -1;
         bool waited = false;
         auto flush = [&](int uu) {
@@ -269,6 +392,7 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
                 waited = true;
             }
             named_bar_sync(1, k1EpiThreads);
+#pragma unroll 1
             for (int i = etid; i < kBins; i += k1EpiThreads) {
                 const uint32_t v = hist[i];
                 if (v) {
@@ -279,40 +403,40 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
             named_bar_sync(1, k1EpiThreads);
         };
         const uint32_t tl = ((uint32_t)(quarter * 32) << 16) + (uint32_t)tile * 16u;   // lane quarter, tile columns
-        int u = (int)(g0 / pl.nst), j = (int)(g0 % pl.nst);
-        for (int c = 0; c < nstage; ++c, ++j) {
-            if (j == pl.nst) {
-                j = 0;
-                ++u;
-            }
+#pragma unroll 1
+        for (int c = 0;; ++c) {
             const int nb = c % NB;
             if (!mbar_wait_bounded(&tfull[nb], (uint32_t)(c / NB) & 1u)) flag(status, DEV_TIMEOUT);
+            const int2 in = info[c % kInfo];
+            if (in.x < 0) break;
+            const int u = in.x, j = in.y;
+            if (c == 0 && warp == 4) SSA_MARKW(21);
             tc_fence_after();
             float acc[G];
             const uint32_t taddr = tbase + tl + (uint32_t)nb * 64u;
             if constexpr (G == 1) {
-                uint32_t r[1];
-                tmem_ld_x1(taddr, r);
+                uint32_t rr[1];
+                tmem_ld_x1(taddr, rr);
                 tmem_ld_wait();
-                acc[0] = __uint_as_float(r[0]);
+                acc[0] = __uint_as_float(rr[0]);
             } else if constexpr (G == 2) {
-                uint32_t r[2];
-                tmem_ld_x2(taddr, r);
+                uint32_t rr[2];
+                tmem_ld_x2(taddr, rr);
                 tmem_ld_wait();
 #pragma unroll
-                for (int g = 0; g < 2; ++g) acc[g] = __uint_as_float(r[g]);
+                for (int g = 0; g < 2; ++g) acc[g] = __uint_as_float(rr[g]);
             } else if constexpr (G == 4) {
-                uint32_t r[4];
-                tmem_ld_x4(taddr, r);
+                uint32_t rr[4];
+                tmem_ld_x4(taddr, rr);
                 tmem_ld_wait();
 #pragma unroll
-                for (int g = 0; g < 4; ++g) acc[g] = __uint_as_float(r[g]);
+                for (int g = 0; g < 4; ++g) acc[g] = __uint_as_float(rr[g]);
             } else {
-                uint32_t r[8];
-                tmem_ld_x8(taddr, r);
+                uint32_t rr[8];
+                tmem_ld_x8(taddr, rr);
                 tmem_ld_wait();
 #pragma unroll
-                for (int g = 0; g < 8; ++g) acc[g] = __uint_as_float(r[g]);
+                for (int g = 0; g < 8; ++g) acc[g] = __uint_as_float(rr[g]);
             }
             tc_fence_before();
             __syncwarp();
@@ -336,15 +460,18 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
                 if constexpr (UBUF) {
                     const int b = u / p.Hkv, h = u % p.Hkv;
                     const uint32_t x0 = philox_word0((uint32_t)t, (uint32_t)h, (uint32_t)b, 0u, k0, k1);
-                    ubuf[(int64_t)u * pl.np + t] = (uint8_t)(x0 >> 24);
+                    ubuf[(int64_t)u * pl.np + t] = (uint16_t)(x0 >> 16);
                 }
             }
         }
+        if (warp == 4) SSA_MARKW(23);
         if constexpr (HIST) {
             if (cur_u >= 0) flush(cur_u);
         }
+        if (warp == 4) SSA_MARKW(24);
     }
     SSA_MARK(1);
+    SSA_GT(0);
     tc_fence_before();
     __syncthreads();
     grid_dep_launch();
@@ -355,7 +482,7 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
 }
 
 // K1 for ssa_select (scores given): per-unit histogram of the top 12 key bits
-// and the Philox bytes.  One CTA per (unit, tile).
+// and the 16-bit Philox prefixes.  One CTA per (unit, tile).
 __global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_constant__ Params p)
 {
     __shared__ uint32_t hist[kBins];
@@ -376,7 +503,7 @@ __global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_con
         if (!isfinite(s)) flag(status, DEV_NONFINITE);
         atomicAdd(&hist[okey(s) >> 20], 1u);
         const uint32_t x0 = philox_word0((uint32_t)t, (uint32_t)h, (uint32_t)b, 0u, k0, k1);
-        ws_ubuf(p)[(int64_t)u * pl.np + t] = (uint8_t)(x0 >> 24);
+        ws_ubuf(p)[(int64_t)u * pl.np + t] = (uint16_t)(x0 >> 16);
     }
     __syncthreads();
     uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;

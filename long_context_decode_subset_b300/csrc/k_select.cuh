@@ -21,7 +21,8 @@
 //     Z (compensated sum, fixed order), and it joins the slice's list only
 //     if it could be drawn at all: p <= B e / Z_lb for a lower bound Z_lb
 //     of Z read off the histogram (every term of bucket c is at least
-//     exp(floor_c - m)), so u >= B e / Z_lb rules it out for good.
+//     exp(floor_c - m)), and u is at least its 16-bit prefix (drawn by the
+//     score kernel), so prefix >= B e / Z_lb rules it out for good.
 // The last tile of a unit to finish (a counter in the unit's control block)
 // resolves the exact k-th token among the candidates -- in shared memory:
 // a 12-bit histogram, then the few members sharing 24 key bits ranked
@@ -36,8 +37,6 @@
 
 namespace ssa {
 
-constexpr int kBatch = 16;            // strips loaded per thread before use
-constexpr int kCandSmem = 8192;       // candidates the resolve stages in shared memory
 constexpr uint32_t kCandFlag = 0x80000000u;   // list entry: a candidate (its value is the score)
 
 struct SelShared {
@@ -46,16 +45,29 @@ struct SelShared {
     float zw[kSelWarps][2];
     float zlb[kSelWarps];
     uint32_t is_last;
-    uint32_t ncand_cta, cand_base;
+    uint32_t ncand_cta;
     // resolve
-    uint32_t hist[kBins];
+    uint32_t hist[2048];   // the tie path's histograms
     uint32_t nbound;
     uint2 bound[256];
     unsigned long long zi[kSelWarps][2];
+    uint32_t coff[kMaxTiles + 1];   // per-tile candidate offsets
 };
 
-// Dynamic shared memory of K2: the resolve's candidate staging.
-inline uint32_t k2_smem_bytes() { return (uint32_t)kCandSmem * 8u; }
+// What each (unit, tile) CTA leaves for the resolve: its share of Z
+// (compensated pair) and its candidate count (its candidates sit in the
+// tile's own segment of the unit's candidate array).
+struct TilePart {
+    float zh, zl;
+    uint32_t ncand, pad;
+};
+
+constexpr int kSlice = 512;           // tokens a warp stages at a time
+constexpr int kResStage = kSelWarps * kSlice * 6 / 8;   // candidates the resolve stages at a time (same memory)
+
+// Dynamic shared memory of K2: the warps' staged chunks (scores and Philox
+// prefixes).
+inline uint32_t k2_smem_bytes() { return (uint32_t)kSelWarps * kSlice * 6u; }
 
 __device__ __forceinline__ void zacc(float& zh, float& zl, float v)
 {
@@ -92,50 +104,200 @@ __device__ __forceinline__ bool iacc(unsigned long long& lo, unsigned long long&
     return true;
 }
 
-__device__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above1, uint32_t target, float m,
-                             SelShared& sh, uint2* cs)
+// The 128-bit count (hi, lo) of 2^-23 units as an unevaluated pair of floats
+// (c_hi + c_lo equals it to a relative 2^-47): its leading 63 bits `top`
+// (value = top * 2^(sh - 23) up to the dropped low bits), top rounded to a
+// float, and the rest of top, both scaled by the power of two.
+__device__ __forceinline__ void u128_to_float2(unsigned long long hi, unsigned long long lo, float& c_hi, float& c_lo)
+{
+    int sh;
+    unsigned long long top;
+    if (hi == 0ull) {
+        sh = (lo >> 63) ? 1 : 0;
+        top = lo >> sh;
+    } else {
+        const int L = 127 - __clzll((long long)hi);   // leading bit, 64..127
+        sh = L - 62;                                  // 2..65: the leading bit lands on bit 62
+        top = (sh >= 64) ? (hi >> (sh - 64)) : ((hi << (64 - sh)) | (lo >> sh));
+    }
+    const float th = __ull2float_rn(top);                                    // <= 2^63, exact as an integer
+    const long long rest = (long long)(top - (unsigned long long)th);        // |rest| < 2^39
+    const float scale = __int_as_float((sh - 23 + 127) << 23);               // 2^(sh - 23), normal
+    c_hi = __fmul_rn(th, scale);
+    c_lo = __fmul_rn(__ll2float_rn(rest), scale);
+}
+
+// Many members share the top 24 key bits (ties, near-constant scores): the
+// last 8 key bits by histogram, then the tie by index (radix levels on the
+// index bits [20, 31), [9, 20), [0, 9) over the members equal to theta; bins
+// are counted in reverse so that the largest-first search finds the smallest
+// index); then the members outside the stratum add their terms.  Every level
+// walks the unit's candidates again (rare: a slow path).
+template <class Fetch>
+__device__ __noinline__ void resolve_ties(const Params& p, int u, uint32_t pre24, uint32_t t3, uint32_t E, float m,
+                                          SelShared& sh, Fetch& fetch, unsigned long long& ilo,
+                                          unsigned long long& ihi, bool& bad, uint32_t& theta, int64_t& idx_cut)
+{
+    const int tid = threadIdx.x;
+    uint32_t* status = ws_status(p);
+    __syncthreads();
+#pragma unroll 1
+    for (int i = tid; i < 256; i += kSelThreads) sh.hist[i] = 0u;
+    __syncthreads();
+#pragma unroll 1
+    for (uint32_t i = tid; i < E; i += kSelThreads) {
+        const uint2 e = fetch(i);
+        if ((e.x >> 8) == pre24) atomicAdd(&sh.hist[e.x & 0xffu], 1u);
+    }
+    __syncthreads();
+    const Found f3 = find_rank_desc<kSelThreads, 256, false>(sh.hist, t3, sh.scan, sh.bcast, status);
+    theta = (pre24 << 8) | f3.bin;
+    uint32_t rt = t3 - f3.above;   // the rt-th smallest index among the ties at theta
+    uint32_t prefix = 0;
+    const int shifts[3] = {20, 9, 0};
+    const uint32_t masks[3] = {0u, 0xfff00000u, 0xfffffe00u};
+#pragma unroll 1
+    for (int level = 0; level < 3; ++level) {
+        const int shift = shifts[level];
+        __syncthreads();
+#pragma unroll 1
+        for (int i = tid; i < 2048; i += kSelThreads) sh.hist[i] = 0u;
+        __syncthreads();
+#pragma unroll 1
+        for (uint32_t i = tid; i < E; i += kSelThreads) {
+            const uint2 e = fetch(i);
+            if (e.x == theta && (e.y & masks[level]) == prefix)
+                atomicAdd(&sh.hist[2047u - ((e.y >> shift) & 0x7ffu)], 1u);
+        }
+        __syncthreads();
+        const Found fi = find_rank_desc<kSelThreads, 2048, false>(sh.hist, rt, sh.scan, sh.bcast, status);
+        prefix |= (2047u - fi.bin) << shift;
+        rt -= fi.above;
+    }
+    idx_cut = (p.top_k == 0) ? -1 : (int64_t)prefix;
+    if (p.budget > 0.0f) {
+#pragma unroll 1
+        for (uint32_t i = tid; i < E; i += kSelThreads) {
+            const uint2 e = fetch(i);
+            const bool inT = e.x > theta || (e.x == theta && (int64_t)e.y <= idx_cut);
+            if ((e.x >> 8) == pre24 && !inT) bad |= !iacc(ilo, ihi, expf(__fsub_rn(okey_value(e.x), m)));
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above1, uint32_t target, float m,
+                                         SelShared& sh, uint2* cs)
 {
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
     const bool want_z = p.budget > 0.0f;
     UnitCtrl* ctrl = ws_ctrl(p) + u;
-    const uint32_t E = __ldcg(&ctrl->ncand);
-    const uint2* cand = ws_cand(p) + (size_t)u * pl.N;
-    const bool staged = E <= (uint32_t)kCandSmem;
-    auto entry = [&](uint32_t i) -> uint2 { return staged ? cs[i] : __ldcg(cand + i); };
-    if (staged) {
-        for (uint32_t i0 = 0; i0 < E; i0 += kSelThreads * 4) {
-            uint2 v[4];
+    const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.ntile;
+    // one wave of loads: the tiles' candidate counts and shares of Z (two
+    // tiles per thread: at most kMaxTiles tiles) and the candidates' level-2
+    // histogram (the next 12 key bits, counted by the tiles; 8 bins per
+    // thread, top bin first)
+    uint32_t cnt2[2];
+    float tzh[2], tzl[2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t i = i0 + j * kSelThreads + tid;
-                v[j] = (i < E) ? __ldcg(cand + i) : make_uint2(0u, 0u);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t i = i0 + j * kSelThreads + tid;
-                if (i < E) cs[i] = v[j];
-            }
-        }
+    for (int j = 0; j < 2; ++j) {
+        const int t = 2 * tid + j;
+        const bool ok = t < pl.ntile;
+        cnt2[j] = ok ? __ldcg(&tp[t].ncand) : 0u;
+        tzh[j] = ok ? __ldcg(&tp[t].zh) : 0.0f;
+        tzl[j] = ok ? __ldcg(&tp[t].zl) : 0.0f;
     }
-    for (int i = tid; i < kBins; i += kSelThreads) sh.hist[i] = 0u;
+    const uint32_t* hist2 = ws_hist2(p) + (size_t)u * kBins;
+    constexpr int CH = kBins / kSelThreads;
+    uint32_t c[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) c[j] = __ldcg(hist2 + (kBins - 1 - (tid * CH + j)));
     if (tid == 0) sh.nbound = 0;
-    __syncthreads();
-    // level 2: the next 12 key bits of the bucket's members
-    for (uint32_t i = tid; i < E; i += kSelThreads) atomicAdd(&sh.hist[(entry(i).x >> 8) & 0xfffu], 1u);
-    __syncthreads();
-    const Found f2 = find_rank_desc<kSelThreads, kBins, false>(sh.hist, target - above1, sh.scan, sh.bcast, status);
-    const uint32_t pre24 = (f1 << 12) | f2.bin;
-    const uint32_t t3 = target - above1 - f2.above;   // rank among the pre24 members (1-based)
-    for (uint32_t i = tid; i < E; i += kSelThreads) {
-        const uint2 e = entry(i);
-        if ((e.x >> 8) == pre24) {
-            const uint32_t slot = atomicAdd(&sh.nbound, 1u);
-            if (slot < 256u) sh.bound[slot] = e;
+    uint32_t E;
+    const uint32_t before = block_excl_scan<kSelThreads>(cnt2[0] + cnt2[1], sh.scan, E);
+    if (2 * tid < pl.ntile) sh.coff[2 * tid] = before;
+    if (2 * tid + 1 < pl.ntile) sh.coff[2 * tid + 1] = before + cnt2[0];
+    if (tid == 0) sh.coff[pl.ntile] = E;
+    // f2: the level-2 bin holding the k-th score
+    const uint32_t t2 = target - above1;
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) local += c[j];
+    if (tid == 0) {
+        sh.bcast[0] = 0;
+        sh.bcast[1] = 0xffffffffu;
+    }
+    uint32_t tot2;
+    const uint32_t excl = block_excl_scan<kSelThreads>(local, sh.scan, tot2);
+    if (local > 0 && excl < t2 && t2 <= excl + local) {
+        uint32_t cum = excl;
+        bool done = false;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (!done && cum + c[j] >= t2) {
+                sh.bcast[0] = (uint32_t)(kBins - 1 - (tid * CH + j));
+                sh.bcast[1] = cum;
+                done = true;
+            }
+            cum += c[j];
         }
     }
     __syncthreads();
+    Found f2{sh.bcast[0], sh.bcast[1]};
+    if (f2.above == 0xffffffffu || tot2 != E) {   // counts disagree: cannot happen
+        if (tid == 0) flag(status, DEV_BAD_INDEX);
+        f2.bin = 0;
+        f2.above = 0;
+    }
+    const uint32_t pre24 = (f1 << 12) | f2.bin;
+    const uint32_t t3 = t2 - f2.above;   // rank among the pre24 members (1-based)
+    SSA_MARK(5);
+
+    // one pass over the candidates: above pre24 -> in T; below -> in R, its
+    // term summed exactly; equal -> the member list in shared memory.  The
+    // candidates are staged in shared memory kResStage at a time, each warp
+    // copying whole tile segments (cp.async).
+    const uint2* cand = ws_cand(p) + (size_t)u * pl.N;
+    auto fetch = [&](uint32_t i) -> uint2 {   // the i-th candidate in tile order (slow path)
+        int lo_t = 0, hi_t = pl.ntile;          // coff[lo_t] <= i < coff[hi_t]
+        while (hi_t - lo_t > 1) {
+            const int mid = (lo_t + hi_t) >> 1;
+            if (sh.coff[mid] <= i) lo_t = mid; else hi_t = mid;
+        }
+        return __ldcg(cand + (size_t)lo_t * pl.tt + (i - sh.coff[lo_t]));
+    };
+    unsigned long long ilo = 0ull, ihi = 0ull;
+    bool bad = false;
+#pragma unroll 1
+    for (uint32_t r0 = 0; r0 < E; r0 += kResStage) {
+        const uint32_t r1 = min(E, r0 + (uint32_t)kResStage);
+        __syncthreads();   // the previous round is consumed
+#pragma unroll 1
+        for (int t = warp; t < pl.ntile; t += kSelWarps) {
+            const uint32_t a = max(sh.coff[t], r0), e = min(sh.coff[t + 1], r1);
+            const uint2* src = cand + (size_t)t * pl.tt + (a - sh.coff[t]);
+#pragma unroll 1
+            for (uint32_t i = lane; a + i < e; i += 32) cp_async_8(cs + (a - r0) + i, src + i);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll 1
+        for (uint32_t i = tid; i < r1 - r0; i += kSelThreads) {
+            const uint2 v = cs[i];
+            const uint32_t p24 = v.x >> 8;
+            if (p24 < pre24) {
+                if (want_z) bad |= !iacc(ilo, ihi, expf(__fsub_rn(okey_value(v.x), m)));
+            } else if (p24 == pre24) {
+                const uint32_t slot = atomicAdd(&sh.nbound, 1u);
+                if (slot < 256u) sh.bound[slot] = v;
+            }
+        }
+    }
+    __syncthreads();
+    SSA_MARK(6);
     const uint32_t nb = sh.nbound;
     uint32_t theta = 0;
     int64_t idx_cut = -1;
@@ -149,6 +311,7 @@ __device__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above
         if ((uint32_t)tid < nb) {
             const uint2 me = sh.bound[tid];
             uint32_t ahead = 0;
+#pragma unroll 1
             for (uint32_t i = 0; i < nb; ++i) {
                 const uint2 o = sh.bound[i];
                 ahead += (o.x > me.x || (o.x == me.x && o.y < me.y)) ? 1u : 0u;
@@ -166,70 +329,25 @@ __device__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above
         }
         theta = sh.bcast[4];
         idx_cut = (int64_t)sh.bcast[5];
+        if (p.top_k == 0) idx_cut = -1;   // k = 0: empty stratum, the k-th score only fixes m
+        // the members outside the stratum add their terms
+        if (want_z && (uint32_t)tid < nb) {
+            const uint2 me = sh.bound[tid];
+            const bool inT = me.x > theta || (me.x == theta && (int64_t)me.y <= idx_cut);
+            if (!inT) bad |= !iacc(ilo, ihi, expf(__fsub_rn(okey_value(me.x), m)));
+        }
         __syncthreads();
     } else {
-        // many members share the top 24 bits (ties, near-constant scores): the
-        // last 8 key bits by histogram, then the tie by index (radix levels on
-        // the index bits [20, 31), [9, 20), [0, 9) over the members equal to
-        // theta; bins are counted in reverse so that the largest-first search
-        // finds the smallest index)
-        __syncthreads();
-        for (int i = tid; i < 256; i += kSelThreads) sh.hist[i] = 0u;
-        __syncthreads();
-        for (uint32_t i = tid; i < E; i += kSelThreads) {
-            const uint2 e = entry(i);
-            if ((e.x >> 8) == pre24) atomicAdd(&sh.hist[e.x & 0xffu], 1u);
-        }
-        __syncthreads();
-        const Found f3 = find_rank_desc<kSelThreads, 256, false>(sh.hist, t3, sh.scan, sh.bcast, status);
-        theta = (pre24 << 8) | f3.bin;
-        uint32_t rt = t3 - f3.above;   // the rt-th smallest index among the ties at theta
-        uint32_t prefix = 0;
-        const int shifts[3] = {20, 9, 0};
-        const uint32_t masks[3] = {0u, 0xfff00000u, 0xfffffe00u};
-#pragma unroll
-        for (int level = 0; level < 3; ++level) {
-            const int shift = shifts[level];
-            __syncthreads();
-            for (int i = tid; i < 2048; i += kSelThreads) sh.hist[i] = 0u;
-            __syncthreads();
-            for (uint32_t i = tid; i < E; i += kSelThreads) {
-                const uint2 e = entry(i);
-                if (e.x == theta && (e.y & masks[level]) == prefix)
-                    atomicAdd(&sh.hist[2047u - ((e.y >> shift) & 0x7ffu)], 1u);
-            }
-            __syncthreads();
-            const Found fi = find_rank_desc<kSelThreads, 2048, false>(sh.hist, rt, sh.scan, sh.bcast, status);
-            prefix |= (2047u - fi.bin) << shift;
-            rt -= fi.above;
-        }
-        idx_cut = (int64_t)prefix;
+        resolve_ties(p, u, pre24, t3, E, m, sh, fetch, ilo, ihi, bad, theta, idx_cut);
     }
-    if (p.top_k == 0) idx_cut = -1;   // k = 0: empty stratum, the k-th score only fixes m
+    if (bad) flag(status, DEV_NONFINITE);
+    SSA_MARK(13);
 
-    // normaliser: tile shares (tile order, compensated) + remainder candidates (exact)
+    // normaliser: tile shares (compensated, fixed tree) + the exact sum of the
+    // remainder candidates' terms
     float zh = 0.0f, zl = 0.0f;
-    {
-        const float2* zp = ws_zpart(p) + (size_t)u * pl.ntile;
-        for (int t0 = 0; t0 < pl.ntile; t0 += kSelThreads * 4) {
-            float2 v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int t = t0 + j * kSelThreads + tid;
-                v[j] = (t < pl.ntile) ? __ldcg(zp + t) : make_float2(0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) comp_add(zh, zl, v[j].x, v[j].y);
-        }
-    }
-    unsigned long long ilo = 0ull, ihi = 0ull;
-    if (want_z) {
-        for (uint32_t i = tid; i < E; i += kSelThreads) {
-            const uint2 e = entry(i);
-            const bool inT = e.x > theta || (e.x == theta && (int64_t)e.y <= idx_cut);
-            if (!inT && !iacc(ilo, ihi, expf(__fsub_rn(okey_value(e.x), m)))) flag(status, DEV_NONFINITE);
-        }
-    }
+    comp_add(zh, zl, tzh[0], tzl[0]);
+    comp_add(zh, zl, tzh[1], tzl[1]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, ilo, o);
@@ -251,17 +369,17 @@ __device__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above
     if (tid == 0) {
         float hh = 0.0f, ll = 0.0f;
         unsigned long long slo = 0ull, shi = 0ull;
+#pragma unroll 1
         for (int w = 0; w < kSelWarps; ++w) {
             comp_add(hh, ll, sh.zw[w][0], sh.zw[w][1]);
             const unsigned long long nlo = slo + sh.zi[w][0];
             shi += sh.zi[w][1] + (nlo < slo ? 1ull : 0ull);
             slo = nlo;
         }
-        // the integer sum (units of 2^-23) as a double, then as two floats
-        const double d = __ull2double_rn(shi) * 2199023255552.0 + __ull2double_rn(slo) * 1.1920928955078125e-07;
-        const float c_hi = __double2float_rn(d);
-        const float c_lo = __double2float_rn(d - (double)c_hi);
+        float c_hi, c_lo;
+        u128_to_float2(shi, slo, c_hi, c_lo);
         comp_add(hh, ll, c_hi, c_lo);
+        ctrl->ncand = E;
         ctrl->theta = theta;
         ctrl->idx_cut = (int32_t)idx_cut;
         ctrl->m = m;
@@ -272,39 +390,96 @@ __device__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above
 // ---------------------------------------------------------------------------
 // K2: per (unit, tile)
 // ---------------------------------------------------------------------------
+
 __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_constant__ Params p)
 {
-    extern __shared__ uint2 cstage[];
+    extern __shared__ __align__(16) unsigned char k2dyn[];
     __shared__ SelShared sh;
     const Plan& pl = p.pl;
     const int u = blockIdx.x / pl.ntile, tile = blockIdx.x % pl.ntile;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W2 = pl.tt / kSelWarps;
-    const int b = u / p.Hkv, h = u % p.Hkv;
     uint32_t* status = ws_status(p);
+    SSA_MARK(20);
+    SSA_GT(1);
     grid_dep_wait();
     SSA_MARK(2);
+    SSA_GT(2);
 
-    const uint32_t target = (uint32_t)(p.top_k > 0 ? p.top_k : 1);
-    const uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
-    const Found f1 = find_rank_desc<kSelThreads, kBins, true>(hist1, target, sh.scan, sh.bcast, status);
-    const float m = okey_value(f1.bin << 20);
+    const int64_t base = (int64_t)tile * pl.tt + (int64_t)warp * W2;   // this warp's first token
+    const float* S = p.s_src + (int64_t)u * pl.N;
+    const uint16_t* ub = ws_ubuf(p) + (size_t)u * pl.np + base;
     const float B = p.budget;
     const bool sampling = B > 0.0f;
+    // Each warp stages its slice kSlice tokens at a time (scores and Philox
+    // prefixes, cp.async); the first chunk's copies go out before the
+    // histogram search.  The loop over the chunk is kept rolled: the code runs
+    // once per launch, so its size, not its instruction count, sets its time.
+    float* ssc = reinterpret_cast<float*>(k2dyn) + warp * kSlice;
+    uint16_t* su = reinterpret_cast<uint16_t*>(k2dyn + kSelWarps * kSlice * 4) + warp * kSlice;
+    auto stage = [&](int c0) {
+        const int n = min(kSlice, W2 - c0);
+#pragma unroll 1
+        for (int i = lane; i < n; i += 32) cp_async_4(ssc + i, S + min(base + c0 + i, pl.N - 1));
+        if (sampling) {
+#pragma unroll 1
+            for (int i = lane * 8; i < n; i += 256) cp_async_16(su + i, ub + c0 + i);
+        }
+        cp_async_commit();
+    };
+    stage(0);
 
-    // Z_lb: every term of bucket c < f1 is at least expf(fl32(floor_c - m)); 0.999 covers rounding
+    // bucket f1 of the k-th score (the largest when k = 0): each thread reads
+    // 8 bins of the unit's histogram, top bin first
+    const uint32_t target = (uint32_t)(p.top_k > 0 ? p.top_k : 1);
+    const uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
+    constexpr int CH = kBins / kSelThreads;
+    uint32_t c[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) c[j] = __ldcg(hist1 + (kBins - 1 - (tid * CH + j)));
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) local += c[j];
+    if (tid == 0) {
+        sh.bcast[0] = 0;
+        sh.bcast[1] = 0xffffffffu;
+        sh.ncand_cta = 0;
+    }
+    uint32_t total;
+    const uint32_t excl = block_excl_scan<kSelThreads>(local, sh.scan, total);
+    if (local > 0 && excl < target && target <= excl + local) {
+        uint32_t cum = excl;
+        bool done = false;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (!done && cum + c[j] >= target) {
+                sh.bcast[0] = (uint32_t)(kBins - 1 - (tid * CH + j));
+                sh.bcast[1] = cum;
+                done = true;
+            }
+            cum += c[j];
+        }
+    }
+    __syncthreads();
+    Found f1{sh.bcast[0], sh.bcast[1]};
+    if (f1.above == 0xffffffffu) {   // fewer than k tokens counted: inconsistent inputs
+        if (tid == 0) flag(status, DEV_BAD_INDEX);
+        f1.bin = 0;
+        f1.above = 0;
+    }
+    const float m = okey_value(f1.bin << 20);
+    SSA_MARK(16);
+
+    // Z_lb from the same bins: every term of bucket c < f1 is at least
+    // expf(fl32(floor_c - m)); 0.999 covers the rounding
     float zlb = 0.0f;
     if (sampling) {
-        constexpr int CH = kBins / kSelThreads;
         float part = 0.0f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const uint32_t c = (uint32_t)(tid * CH + j);
-            if (c < f1.bin) {
-                const uint32_t n = __ldcg(hist1 + c);
-                const float fl = okey_value(c << 20);
-                if (n && isfinite(fl)) part = fmaf((float)n, expf(__fsub_rn(fl, m)), part);
-            }
+            const uint32_t cb = (uint32_t)(kBins - 1 - (tid * CH + j));
+            const float fl = okey_value(cb << 20);
+            if (cb < f1.bin && c[j] && isfinite(fl)) part = fmaf((float)c[j], expf(__fsub_rn(fl, m)), part);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -313,54 +488,42 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         for (int w = 0; w < kSelWarps; ++w) zlb += sh.zlb[w];
         zlb *= 0.999f;
     }
-    // u >= B e / Z_lb implies u >= p for any Z >= Z_lb: the token cannot be drawn
+    // u >= prefix * 2^-16 >= B e / Z_lb >= p (any Z >= Z_lb): the token cannot be drawn
     const float bound_scale = (zlb > 0.0f) ? __fdiv_ru(B, zlb) : INFINITY;
+    SSA_MARK(17);
 
-    const int64_t base = (int64_t)tile * pl.tt + (int64_t)warp * W2;   // this warp's first token
-    const float* S = p.s_src + (int64_t)u * pl.N;
-    const uint8_t* ub = ws_ubuf(p) + (size_t)u * pl.np;
     int32_t* sidx = ws_sel_idx(p) + (size_t)u * pl.np + base;
     float* sval = ws_sel_p(p) + (size_t)u * pl.np + base;
-    uint2* cand = ws_cand(p) + (size_t)u * pl.N;
-    UnitCtrl* ctrl = ws_ctrl(p) + u;
-    if (tid == 0) sh.ncand_cta = 0;
-    __syncthreads();
+    // the tile's candidates go to its own segment of the unit's candidate
+    // array (their order is free: the resolve ranks and sums exactly)
+    uint2* cseg = ws_cand(p) + (size_t)u * pl.N + (size_t)tile * pl.tt;
+    uint32_t* hist2 = ws_hist2(p) + (size_t)u * kBins;   // level-2 histogram of the unit's candidates
     uint32_t cnt = 0;
     float zh = 0.0f, zl = 0.0f;
-    for (int st0 = 0; st0 < W2; st0 += 32 * kBatch) {
-        float sv[kBatch];
-        uint32_t u8v[kBatch / 4];   // four Philox bytes per word
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int64_t t = base + st0 + j * 32 + lane;
-            sv[j] = (st0 + j * 32 < W2 && t < pl.N) ? __ldcg(S + t) : 0.0f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < W2; c0 += kSlice) {
+        if (c0 > 0) {
+            __syncwarp();
+            stage(c0);
         }
-#pragma unroll
-        for (int j = 0; j < kBatch / 4; ++j) u8v[j] = 0u;
-        if (sampling) {
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int64_t t = base + st0 + j * 32 + lane;
-                if (st0 + j * 32 < W2 && t < pl.N) u8v[j >> 2] |= (uint32_t)__ldcg(ub + t) << (8 * (j & 3));
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            if (st0 + j * 32 >= W2) break;   // uniform across the warp
-            const int64_t t = base + st0 + j * 32 + lane;
+        cp_async_wait<0>();
+        __syncwarp();
+        const int n = min(kSlice, W2 - c0);   // a multiple of 32: the trip count is warp-uniform
+#pragma unroll 1
+        for (int i = lane; i < n; i += 32) {
+            const int64_t t = base + c0 + i;
             const bool valid = t < pl.N;
-            const uint32_t k = okey(sv[j]);
+            const float s = ssc[i];
+            const uint32_t k = okey(s);
             const uint32_t b1 = k >> 20;
             const bool above = valid && b1 > f1.bin;
             const bool is_cand = valid && b1 == f1.bin;
             bool keep = above || is_cand;
-            float val = above ? INFINITY : sv[j];
+            float val = above ? INFINITY : s;
             if (valid && b1 < f1.bin && sampling) {
-                const float e = expf(__fsub_rn(sv[j], m));
+                const float e = expf(__fsub_rn(s, m));
                 zacc(zh, zl, e);
-                const float pmax = __fmul_ru(e, bound_scale);
-                const uint32_t v8 = (u8v[j >> 2] >> (8 * (j & 3))) & 0xffu;
-                if (pmax > (float)v8 * 0.00390625f) keep = token_uniform(p.seed, t, h, b) < pmax;
+                keep = __fmul_ru(e, bound_scale) > __uint2float_rn((uint32_t)su[i]) * 1.52587890625e-05f;
                 val = e;
             }
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
@@ -370,48 +533,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
                 sval[o] = val;
             }
             cnt += __popc(km);
-            const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
-            if (cm) {   // candidates gather in shared memory first (one global reservation per CTA)
-                uint32_t slot0 = 0;
-                if (lane == __ffs(cm) - 1) slot0 = atomicAdd(&sh.ncand_cta, (uint32_t)__popc(cm));
-                slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(cm) - 1);
-                const uint32_t slot = slot0 + __popc(cm & lanemask_lt());
-                if (is_cand && slot < (uint32_t)kCandSmem) cstage[slot] = make_uint2(k, (uint32_t)t);
+            if (is_cand) {
+                cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(k, (uint32_t)t);
+                atomicAdd(hist2 + ((k >> 8) & 0xfffu), 1u);
             }
         }
     }
+    SSA_MARK(18);
     if (lane == 0) ws_scount(p)[((size_t)u * pl.ntile + tile) * kSelWarps + warp] = cnt;
-    __syncthreads();
-    {
-        // reserve the tile's share of the unit's candidate array and copy it out
-        // (the array's order is free: the resolve ranks exactly and sums exactly)
-        const uint32_t nc = sh.ncand_cta;
-        if (tid == 0) sh.cand_base = nc ? atomicAdd(&ctrl->ncand, nc) : 0u;
-        __syncthreads();
-        const uint32_t cb = sh.cand_base;
-        if (nc <= (uint32_t)kCandSmem) {
-            for (uint32_t i = tid; i < nc; i += kSelThreads) cand[cb + i] = cstage[i];
-        } else {   // too many for the staging: walk the tile again and write them all
-            if (tid == 0) sh.ncand_cta = 0;
-            __syncthreads();
-            for (int st0 = 0; st0 < W2; st0 += 32) {
-                const int64_t t = base + st0 + lane;
-                const bool valid = t < pl.N;
-                const uint32_t k = valid ? okey(__ldcg(S + t)) : 0u;
-                const bool is_cand = valid && (k >> 20) == f1.bin;
-                const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
-                if (cm) {
-                    uint32_t slot0 = 0;
-                    if (lane == __ffs(cm) - 1) slot0 = atomicAdd(&sh.ncand_cta, (uint32_t)__popc(cm));
-                    slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(cm) - 1);
-                    const uint32_t slot = slot0 + __popc(cm & lanemask_lt());
-                    if (is_cand) cand[cb + slot] = make_uint2(k, (uint32_t)t);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    SSA_MARK(10);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float h2 = __shfl_xor_sync(0xffffffffu, zh, o);
@@ -422,22 +551,31 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         sh.zw[warp][0] = zh;
         sh.zw[warp][1] = zl;
     }
+    __threadfence();
     __syncthreads();
+    SSA_MARK(19);
     if (tid == 0) {
         float hh = 0.0f, ll = 0.0f;
         for (int w = 0; w < kSelWarps; ++w) comp_add(hh, ll, sh.zw[w][0], sh.zw[w][1]);
-        ws_zpart(p)[(size_t)u * pl.ntile + tile] = make_float2(hh, ll);
+        TilePart tpo;
+        tpo.zh = hh;
+        tpo.zl = ll;
+        tpo.ncand = sh.ncand_cta;
+        tpo.pad = 0;
+        reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.ntile + tile] = tpo;
         __threadfence();
-        const uint32_t prev = atomicAdd(&ctrl->k2a_done, 1u);
+        const uint32_t prev = atomicAdd(&ws_ctrl(p)[u].k2a_done, 1u);
         sh.is_last = (prev == (uint32_t)(pl.ntile - 1)) ? 1u : 0u;
     }
     __syncthreads();
+    SSA_MARK(10);
     if (sh.is_last) {
         __threadfence();
         SSA_MARK(3);
-        resolve_unit(p, u, f1.bin, f1.above, target, m, sh, cstage);
+        resolve_unit(p, u, f1.bin, f1.above, target, m, sh, reinterpret_cast<uint2*>(k2dyn));
         SSA_MARK(4);
     }
+    SSA_GT(3);
     grid_dep_launch();
 }
 

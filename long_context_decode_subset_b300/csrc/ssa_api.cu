@@ -54,6 +54,7 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     const int64_t U = pl.U, N = s.ctx_len;
     pl.nst = (int32_t)((N + kStageTok - 1) / kStageTok);
     pl.stages = U * pl.nst;
+    pl.sf = (int32_t)((int64_t)pl.nst * 3 / 4);   // the rest of each unit goes to K1's shared queue
     const int sms = with_device ? device_sms() : 148;
     pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
     int64_t tt = (int64_t)kTileTok * std::max<int64_t>(1, (N + (int64_t)kTileTok * kMaxTiles - 1) /
@@ -77,15 +78,15 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     };
     pl.o_status = take(kStatusBytes);
     pl.o_ctrl = take((size_t)U * sizeof(UnitCtrl));
-    pl.o_hist1 = take((size_t)U * kBins * 4);
-    pl.o_zpart = take((size_t)U * pl.ntile * 8);
+    pl.o_hist1 = take((size_t)U * kBins * 4 * 2);   // level-1 then level-2 histograms
+    pl.o_zpart = take((size_t)U * pl.ntile * 16);
     pl.o_scount = take((size_t)U * nl * 4);
     pl.o_kept = take((size_t)U * kMaxSplit * 4);
     pl.o_cand = take((size_t)U * N * 8);
     pl.o_sel_idx = take((size_t)U * pl.np * 4);
     pl.o_sel_p = take((size_t)U * pl.np * 4);
     pl.o_scores = take((size_t)U * N * 4);
-    pl.o_ubuf = take((size_t)U * pl.np);
+    pl.o_ubuf = take((size_t)U * pl.np * 2);
     pl.o_part = take((size_t)U * kMaxSplit * (size_t)(G * D + 2 * G) * 4);
     pl.o_hq = take((size_t)heads * D * 2);
     pl.o_hout = take((size_t)heads * D * 4);
@@ -195,6 +196,32 @@ kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists)
     }
 }
 
+// Raise `fn`'s dynamic shared-memory limit to `smem` (static plus dynamic
+// above 48 KB needs it); remembered per kernel, per device.
+bool allow_dynamic_smem(kfn_t fn, uint32_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<void*, int>, uint32_t> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const auto key = std::make_pair((void*)fn, dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = done.find(key);
+        if (it != done.end() && it->second >= smem) return true;
+    }
+    if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    done[key] = std::max(done[key], smem);
+    return true;
+}
+
 // Launch `fn` on `stream`.  Every kernel of a step after the first is a
 // programmatic dependent launch: it may start while its predecessor drains
 // and waits (griddepcontrol.wait) before reading its results.
@@ -203,11 +230,7 @@ ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::P
 {
     if (grid <= 0) return SSA_OK;
     if (grid > INT32_MAX) return SSA_ERR_UNSUPPORTED;
-    if (smem > 48u * 1024u &&
-        cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-        cudaGetLastError();
-        return SSA_ERR_CUDA;
-    }
+    if (smem > 0 && !allow_dynamic_smem(fn, smem)) return SSA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3((unsigned)block, 1, 1);
@@ -271,8 +294,7 @@ int blocks_per_sm(kfn_t fn, int block, uint32_t smem)
         if (it != cache.end()) return it->second;
     }
     int n = 0;
-    if ((smem > 48u * 1024u &&
-         cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) ||
+    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)fn, block, smem) != cudaSuccess) {
         cudaGetLastError();
         n = 1;
@@ -403,7 +425,8 @@ ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_c
     p.sel_ch = sel_ch;
     p.scale = scale;
     p.s_dst = s_hat;
-    return launch_score(p, *shape, false, stream, false);
+    if ((st = launch_init(p, stream)) != SSA_OK) return st;   // zeroes K1's stage queue
+    return launch_score(p, *shape, false, stream, true);
 }
 
 ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t seed, int32_t* idx, float* p,

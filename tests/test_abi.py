@@ -56,8 +56,8 @@ def test_workspace_bytes():
     s = _shape()
     n = ssa.ssa_workspace_bytes(s)
     units, N = 16, 4096
-    # scores, candidate and selection lists, Philox bytes: at least 21 bytes per token
-    assert n >= units * N * 21
+    # scores, candidate and selection lists, 16-bit Philox prefixes: at least 22 bytes per token
+    assert n >= units * N * 22
     # the internal lists are sized for the worst case, so the list capacity does not matter
     assert ssa.ssa_workspace_bytes(s, 100) == n
     assert ssa.ssa_workspace_bytes(_shape(ctx_len=8192)) > n
