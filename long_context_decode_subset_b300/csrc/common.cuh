@@ -17,6 +17,7 @@
 //               softmax; the last CTA of a unit merges the partials.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -65,7 +66,8 @@ struct UnitCtrl {
     float m;             // reference point of the exponentials
     float Z;             // normaliser over the remainder
     uint32_t k1_next;    // unit 0 only: K1's shared stage queue (stages taken)
-    uint32_t pad[8];
+    uint32_t k3_cdone;   // K3 clusters finished
+    uint32_t pad[7];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 

@@ -260,21 +260,75 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr));
+}
+
 // Shared-memory matrix descriptor (tcgen05): K-major operand whose rows are
-// `row_bytes` (32 or 64) wide and stored with the matching 32/64-byte swizzle
-// (the layout a TMA copy with that swizzle writes); 8-row groups are
-// 8 * row_bytes apart.
+// `row_bytes` (32, 64 or 128) wide and stored with the matching
+// 32/64/128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7), for
+// 128 bytes); 8-row groups are 8 * row_bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_kmajor_swz(uint32_t saddr, uint32_t row_bytes)
 {
-    const uint64_t swz = (row_bytes == 64) ? 4ull : 6ull;   // 64-byte or 32-byte swizzle
+    const uint64_t swz = (row_bytes == 128) ? 2ull : (row_bytes == 64) ? 4ull : 6ull;
     const uint64_t sbo = 8ull * row_bytes;
     return (uint64_t)((saddr >> 4) & 0x3fffu) | (1ull << 16) | ((sbo >> 4) << 32) | (1ull << 46) | (swz << 61);
+}
+
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzled layout: atoms of 64 MN-elements (128 bytes) x 8 K-rows, atoms
+// `lbo` bytes apart along MN and `sbo` bytes apart along K.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Instruction descriptor for kind::f16: bf16 A and B (both K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with A MN-major (transposed), B K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(uint32_t M, uint32_t N)
+{
+    return idesc_bf16_f32(M, N) | (1u << 15);
+}
+
+// cp.async of 16 bytes that writes zeros instead when `valid` is false.
+__device__ __forceinline__ void cp_async_16_zfill(void* dst_smem, const void* src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// Thread-block clusters: this CTA's rank, a full cluster barrier, and loads
+// from another CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(const void* local_smem, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 }  // namespace ssa

@@ -179,20 +179,27 @@ kfn_t pick_score(int G, int dsel, bool hist)
     }
 }
 
-template <int G, int D>
-kfn_t att_fn(uint32_t* smem, int nlists)
+template <int G>
+kfn_t att_fn(int d, uint32_t* smem, int nlists, bool* tc)
 {
-    *smem = k3_smem_bytes<G, D>(nlists);
-    return &attend_kernel<G, D>;
+    *tc = (d == 128);
+    if (d == 128) {
+        *smem = ktc_smem_bytes<G>(nlists);
+        return &attend_tc_kernel<G>;
+    }
+    *smem = k3_smem_bytes<G, 64>(nlists);
+    return &attend_kernel<G, 64>;
 }
 
-kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists)
+// K3 for this shape: the tensor-core kernel (clusters of kClusterCtas) at
+// head_dim 128, the CUDA-core kernel at 64.
+kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists, bool* tc)
 {
     switch (G) {
-        case 1: return d == 64 ? att_fn<1, 64>(smem, nlists) : att_fn<1, 128>(smem, nlists);
-        case 2: return d == 64 ? att_fn<2, 64>(smem, nlists) : att_fn<2, 128>(smem, nlists);
-        case 4: return d == 64 ? att_fn<4, 64>(smem, nlists) : att_fn<4, 128>(smem, nlists);
-        default: return d == 64 ? att_fn<8, 64>(smem, nlists) : att_fn<8, 128>(smem, nlists);
+        case 1: return att_fn<1>(d, smem, nlists, tc);
+        case 2: return att_fn<2>(d, smem, nlists, tc);
+        case 4: return att_fn<4>(d, smem, nlists, tc);
+        default: return att_fn<8>(d, smem, nlists, tc);
     }
 }
 
@@ -226,7 +233,7 @@ bool allow_dynamic_smem(kfn_t fn, uint32_t smem)
 // programmatic dependent launch: it may start while its predecessor drains
 // and waits (griddepcontrol.wait) before reading its results.
 ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::Params& prm, cudaStream_t stream,
-                  bool dependent)
+                  bool dependent, int cluster = 1)
 {
     if (grid <= 0) return SSA_OK;
     if (grid > INT32_MAX) return SSA_ERR_UNSUPPORTED;
@@ -236,13 +243,22 @@ ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::P
     cfg.blockDim = dim3((unsigned)block, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
+    unsigned na = 0;
     if (dependent) {
-        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
+        at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
+    if (cluster > 1) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = (unsigned)cluster;
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na ? at : nullptr;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, fn, prm) != cudaSuccess) {
         cudaGetLastError();
         return SSA_ERR_CUDA;
@@ -305,14 +321,60 @@ int blocks_per_sm(kfn_t fn, int block, uint32_t smem)
     return n;
 }
 
+// Clusters of kClusterCtas CTAs of `fn` (`threads` threads, `smem` bytes)
+// resident on the device at once (cached per kernel and size).
+int64_t active_clusters(kfn_t fn, int threads, uint32_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<void*, uint32_t>, int64_t> cache;
+    const auto key = std::make_pair((void*)fn, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)kClusterCtas, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)kClusterCtas;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) || cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    const int64_t v = std::max(n, 1);
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = v;
+    return v;
+}
+
 // K3 CTAs per unit: as many as fit in one wave with every unit getting the
-// same number (at most kMaxSplit), unless SSA_FORCE_SPLIT says otherwise.
+// same number (at most kMaxSplit; a multiple of the cluster size for the
+// tensor-core kernel), unless SSA_FORCE_SPLIT says otherwise.
 int attend_split(const ssa::Plan& pl, const ssa_shape& s)
 {
-    const int forced = env_int("SSA_FORCE_SPLIT", 0);
-    if (forced > 0) return std::min(forced, kMaxSplit);
     uint32_t smem = 0;
-    kfn_t fn = pick_attend(pl.G, s.head_dim, &smem, pl.ntile * kSelWarps);
+    bool tc = false;
+    kfn_t fn = pick_attend(pl.G, s.head_dim, &smem, pl.ntile * kSelWarps, &tc);
+    const int forced = env_int("SSA_FORCE_SPLIT", 0);
+    if (tc) {
+        int ncl;
+        if (forced > 0) {
+            ncl = (forced + kClusterCtas - 1) / kClusterCtas;
+        } else {
+            ncl = (int)(active_clusters(fn, kTcThreads, smem) / std::max<int64_t>(pl.U, 1));
+        }
+        ncl = std::max(1, std::min(ncl, kMaxSplit / kClusterCtas));
+        return ncl * kClusterCtas;
+    }
+    if (forced > 0) return std::min(forced, kMaxSplit);
     const int64_t slots = (int64_t)blocks_per_sm(fn, k3Threads, smem) * device_sms();
     return (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, slots / std::max<int64_t>(pl.U, 1)));
 }
@@ -320,11 +382,13 @@ int attend_split(const ssa::Plan& pl, const ssa_shape& s)
 ssa_status launch_attend(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream)
 {
     uint32_t smem = 0;
-    kfn_t fn = pick_attend(p.pl.G, s.head_dim, &smem, p.pl.ntile * kSelWarps);
+    bool tc = false;
+    kfn_t fn = pick_attend(p.pl.G, s.head_dim, &smem, p.pl.ntile * kSelWarps, &tc);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
     ssa::Params q = p;
     q.pl.P = attend_split(p.pl, s);
-    return launch(fn, (int64_t)q.pl.U * q.pl.P, k3Threads, smem, q, stream, true);
+    return launch(fn, (int64_t)q.pl.U * q.pl.P, tc ? kTcThreads : k3Threads, smem, q, stream, true,
+                  tc ? kClusterCtas : 1);
 }
 
 }  // namespace
