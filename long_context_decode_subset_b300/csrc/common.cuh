@@ -47,7 +47,8 @@ constexpr uint32_t DEV_BAD_INDEX = 0x8u;
 
 constexpr int kBins = 4096;            // 12-bit order-key buckets
 constexpr int kStageTok = 512;         // K1: tokens per pipeline stage (4 MMA tiles of 128)
-constexpr int kTileTok = 8192;         // K2: minimum tokens per tile
+constexpr int kTileAlign = 512;       // K2: tiles are multiples of 512 tokens (32 per warp slice)
+constexpr int kSelSlots = 256;         // K2: CTAs the tiles aim at in all
 constexpr int kMaxTiles = 1024;        // K2: tiles per unit at most (the tile grows with N)
 constexpr int kSelThreads = 512;       // K2a / K2c block size; each warp owns a slice (a list) of a tile
 constexpr int kSelWarps = kSelThreads / 32;
@@ -80,7 +81,7 @@ struct Plan {
     int32_t sf;          // K1 stages per unit split statically over the CTAs (the rest are queued)
     int64_t stages;      // K1 stages in all
     int32_t k1_grid;     // K1 CTAs (persistent)
-    int32_t tt;          // K2 tile tokens (multiple of kTileTok)
+    int32_t tt;          // K2 tile tokens (multiple of kTileAlign)
     int32_t ntile;       // K2 tiles per unit
     int64_t np;          // ntile * tt: padded tokens per unit
     int32_t P;           // K3 CTAs per unit

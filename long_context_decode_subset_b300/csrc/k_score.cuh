@@ -216,6 +216,30 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
 
+    // the producer (thread 0): takes stage c, publishes its (unit, j) and
+    // issues its TMA copies (two 256-token boxes); false at the end marker
+    K1Sched sch;
+    int c_issued = 0;
+    bool ended = false;
+    auto produce = [&](int c) -> bool {
+        const int st = c % S;
+        if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+        int u = -1, j = 0;
+        if (!sch.next(u, j)) u = -1;
+        info[c % kInfo] = make_int2(u, j);
+        mbar_arrive(&ready[st]);
+        if (u < 0) {
+            mbar_arrive(&full[st]);   // the end marker carries no copies
+            return false;
+        }
+        const int b = u / p.Hkv, h = u % p.Hkv;
+        mbar_arrive_expect_tx(&full[st], CF::STAGE);
+        unsigned char* dst = ring + (size_t)st * CF::STAGE;
+        const uint64_t pol = l2_policy_evict_first();
+        tma_load_4d(dst, &p.ks_map, 0, j * kStageTok, h, b, &full[st], pol);
+        tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
+        return true;
+    };
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 2);    // the summary copies (with their bytes) + the query operand
@@ -228,6 +252,9 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
         }
         fence_mbar_init();
         tma_prefetch_desc(&p.ks_map);
+        // the first ring's worth of copies go out before the block-wide set-up ends
+        sch.init(pl, &ws_ctrl(p)[0].k1_next);
+        for (; c_issued < S && !ended; ++c_issued) ended = !produce(c_issued);
     }
     if constexpr (HIST) {
         for (int i = tid; i < kBins; i += k1Threads) hist[i] = 0u;
@@ -266,30 +293,10 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     SSA_MARK(0);
 
     if (warp == 0) {
-        // lane 0 takes the stages, publishes each one's (unit, j) and issues
-        // its TMA copies (two 256-token boxes)
+        // the producer carries on from where the set-up left it
         if (lane == 0) {
-            K1Sched sch;
-            sch.init(pl, &ws_ctrl(p)[0].k1_next);
-            const uint64_t pol = l2_policy_evict_first();
 #pragma unroll 1
-            for (int c = 0;; ++c) {
-                const int st = c % S;
-                if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
-                int u = -1, j = 0;
-                if (!sch.next(u, j)) u = -1;
-                info[c % kInfo] = make_int2(u, j);
-                mbar_arrive(&ready[st]);
-                if (u < 0) {
-                    mbar_arrive(&full[st]);   // the end marker carries no copies
-                    break;
-                }
-                const int b = u / p.Hkv, h = u % p.Hkv;
-                mbar_arrive_expect_tx(&full[st], CF::STAGE);
-                unsigned char* dst = ring + (size_t)st * CF::STAGE;
-                tma_load_4d(dst, &p.ks_map, 0, j * kStageTok, h, b, &full[st], pol);
-                tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
-            }
+            for (int c = c_issued; !ended; ++c) ended = !produce(c);
         }
         SSA_MARKW(22);
     } else if (warp == 3) {

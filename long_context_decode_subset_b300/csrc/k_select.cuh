@@ -366,16 +366,21 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
         sh.zi[warp][1] = ihi;
     }
     __syncthreads();
-    if (tid == 0) {
-        float hh = 0.0f, ll = 0.0f;
-        unsigned long long slo = 0ull, shi = 0ull;
-#pragma unroll 1
-        for (int w = 0; w < kSelWarps; ++w) {
-            comp_add(hh, ll, sh.zw[w][0], sh.zw[w][1]);
-            const unsigned long long nlo = slo + sh.zi[w][0];
-            shi += sh.zi[w][1] + (nlo < slo ? 1ull : 0ull);
+    if (warp == 0) {   // the warps' sums, a fixed tree over 16 lanes
+        float hh = lane < kSelWarps ? sh.zw[lane][0] : 0.0f, ll = lane < kSelWarps ? sh.zw[lane][1] : 0.0f;
+        unsigned long long slo = lane < kSelWarps ? sh.zi[lane][0] : 0ull, shi = lane < kSelWarps ? sh.zi[lane][1] : 0ull;
+#pragma unroll
+        for (int o = kSelWarps / 2; o > 0; o >>= 1) {
+            const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, slo, o);
+            const unsigned long long h2 = __shfl_xor_sync(0xffffffffu, shi, o);
+            const unsigned long long nlo = slo + l2;
+            shi += h2 + (nlo < slo ? 1ull : 0ull);
             slo = nlo;
+            const float fh = __shfl_xor_sync(0xffffffffu, hh, o);
+            const float fl = __shfl_xor_sync(0xffffffffu, ll, o);
+            comp_add(hh, ll, fh, fl);
         }
+        if (lane != 0) return;
         float c_hi, c_lo;
         u128_to_float2(shi, slo, c_hi, c_lo);
         comp_add(hh, ll, c_hi, c_lo);
@@ -554,18 +559,25 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
     __threadfence();
     __syncthreads();
     SSA_MARK(19);
-    if (tid == 0) {
-        float hh = 0.0f, ll = 0.0f;
-        for (int w = 0; w < kSelWarps; ++w) comp_add(hh, ll, sh.zw[w][0], sh.zw[w][1]);
-        TilePart tpo;
-        tpo.zh = hh;
-        tpo.zl = ll;
-        tpo.ncand = sh.ncand_cta;
-        tpo.pad = 0;
-        reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.ntile + tile] = tpo;
-        __threadfence();
-        const uint32_t prev = atomicAdd(&ws_ctrl(p)[u].k2a_done, 1u);
-        sh.is_last = (prev == (uint32_t)(pl.ntile - 1)) ? 1u : 0u;
+    if (warp == 0) {   // the warps' shares, a fixed tree over 16 lanes
+        float hh = lane < kSelWarps ? sh.zw[lane][0] : 0.0f, ll = lane < kSelWarps ? sh.zw[lane][1] : 0.0f;
+#pragma unroll
+        for (int o = kSelWarps / 2; o > 0; o >>= 1) {
+            const float fh = __shfl_xor_sync(0xffffffffu, hh, o);
+            const float fl = __shfl_xor_sync(0xffffffffu, ll, o);
+            comp_add(hh, ll, fh, fl);
+        }
+        if (lane == 0) {
+            TilePart tpo;
+            tpo.zh = hh;
+            tpo.zl = ll;
+            tpo.ncand = sh.ncand_cta;
+            tpo.pad = 0;
+            reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.ntile + tile] = tpo;
+            __threadfence();
+            const uint32_t prev = atomicAdd(&ws_ctrl(p)[u].k2a_done, 1u);
+            sh.is_last = (prev == (uint32_t)(pl.ntile - 1)) ? 1u : 0u;
+        }
     }
     __syncthreads();
     SSA_MARK(10);

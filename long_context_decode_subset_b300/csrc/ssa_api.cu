@@ -57,8 +57,12 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.sf = (int32_t)((int64_t)pl.nst * 3 / 4);   // the rest of each unit goes to K1's shared queue
     const int sms = with_device ? device_sms() : 148;
     pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
-    int64_t tt = (int64_t)kTileTok * std::max<int64_t>(1, (N + (int64_t)kTileTok * kMaxTiles - 1) /
-                                                               ((int64_t)kTileTok * kMaxTiles));
+    // K2 tiles: about kSelSlots CTAs in all (two per SM on most of a 148-SM part; the
+    // workspace layout must not depend on the device), 512-token multiples
+    const int64_t want = std::max<int64_t>(1, kSelSlots / std::max<int64_t>(U, 1));
+    int64_t tt = std::max<int64_t>(1, (N + want - 1) / want);
+    tt = std::max<int64_t>(kTileAlign, (tt + kTileAlign - 1) / kTileAlign * kTileAlign);
+    if ((N + tt - 1) / tt > kMaxTiles) tt = ((N + kMaxTiles - 1) / kMaxTiles + kTileAlign - 1) / kTileAlign * kTileAlign;
     const int forced_tile = env_int("SSA_FORCE_TILE", 0);
     if (forced_tile >= 512 && forced_tile % 512 == 0 && (N + forced_tile - 1) / forced_tile <= kMaxTiles)
         tt = forced_tile;
