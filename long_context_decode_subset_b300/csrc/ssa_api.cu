@@ -57,8 +57,9 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.sf = (int32_t)((int64_t)pl.nst * 3 / 4);   // the rest of each unit goes to K1's shared queue
     const int sms = with_device ? device_sms() : 148;
     pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
-    // K2 tiles: about kSelSlots CTAs in all (two per SM on most of a 148-SM part; the
-    // workspace layout must not depend on the device), 512-token multiples
+    // K2 tiles: about kSelSlots CTAs in all (two per SM on 128 SMs; filling
+    // all 148 measured slower, its last CTAs finishing later; the workspace
+    // layout must not depend on the device), 512-token multiples
     const int64_t want = std::max<int64_t>(1, kSelSlots / std::max<int64_t>(U, 1));
     int64_t tt = std::max<int64_t>(1, (N + want - 1) / want);
     tt = std::max<int64_t>(kTileAlign, (tt + kTileAlign - 1) / kTileAlign * kTileAlign);
