@@ -24,8 +24,8 @@
 //    128 at a time -- S = K Q^T and O^T = V^T P with tcgen05.mma, fp32
 //    accumulators in tensor memory, P split into two bf16 terms (hi + lo) so
 //    that the products keep fp32-level accuracy -- and the P CTAs of a unit,
-//    in clusters of 4, merge their (m, l, acc) through distributed shared
-//    memory (then the clusters' partials through global memory);
+//    in clusters of 4 or 8, merge their (m, l, acc) through distributed
+//    shared memory (then the clusters' partials through global memory);
 //  * attend_kernel (head_dim 64): CUDA cores, every warp streaming its rows
 //    with cp.async; the last CTA of a unit merges the P partials.
 #pragma once
@@ -33,7 +33,6 @@
 
 namespace ssa {
 
-constexpr int kClusterCtas = 4;   // attend_tc_kernel: CTAs of a unit merged on chip
 
 // ---------------------------------------------------------------------------
 // shared pieces: the unit's list, the final decisions, the compact list
@@ -329,7 +328,7 @@ __device__ void merge_partials(const Params& p, int b, int h, const float* parts
 }
 
 // ---------------------------------------------------------------------------
-// attend_tc_kernel: head_dim 128, tensor cores, clusters of kClusterCtas CTAs
+// attend_tc_kernel: head_dim 128, tensor cores, clusters of CL CTAs
 // ---------------------------------------------------------------------------
 
 constexpr int kTcList = 1024;   // list entries staged at a time
@@ -374,7 +373,7 @@ constexpr uint32_t ktc_smem_bytes(int nlists)
 // chunk rows for S, = head dims for O), warp 4 issues the MMAs (and owns the
 // tensor memory), warps 5 .. 11 gather the K and V rows.  Chunk g uses buffers
 // g & 1; barrier phases count chunks over the whole CTA.
-template <int G>
+template <int G, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_constant__ Params p)
 {
     using CF = KTCfg<G>;
@@ -657,7 +656,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
         tc_fence_after();
         tmem_dealloc(tbase, CF::TCOLS);
     }
-    finish_lists<kTcThreads>(p, u, P, r, kept, total, reinterpret_cast<uint32_t*>(smem + CF::OFF_K), &misc[1]);
+    if (p.count_out || p.idx_out)   // the merge below needs no "last CTA"
+        finish_lists<kTcThreads>(p, u, P, r, kept, total, reinterpret_cast<uint32_t*>(smem + CF::OFF_K), &misc[1]);
     SSA_MARK(12);
     SSA_GT(6);
     // merge the cluster's partials on chip (rank order); with one cluster
@@ -665,16 +665,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
     // partial and the last cluster to finish merges them in cluster order
     cluster_sync();
     if (p.attend && cluster_rank() == 0) {
-        const int ncl = P / kClusterCtas, cl = r / kClusterCtas;
+        const int ncl = P / CL, cl = r / CL;
         constexpr int PS = G * D + 2 * G;
         float* cpart = ws_part(p) + ((size_t)u * kMaxSplit + cl) * PS;
         constexpr int EPT = (G * D + 255) / 256;
         const int e0 = tid * EPT;
         if (tid < 256 && e0 < G * D) {
             const int gg = e0 / D;
-            float mr[kClusterCtas], M = -INFINITY;
+            float mr[CL], M = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < kClusterCtas; ++k) {
+            for (int k = 0; k < CL; ++k) {
                 mr[k] = ld_dsmem_f32(part + G * D + gg, (uint32_t)k);
                 M = fmaxf(M, mr[k]);
             }
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
             for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
             if (M != -INFINITY) {
 #pragma unroll
-                for (int k = 0; k < kClusterCtas; ++k) {
+                for (int k = 0; k < CL; ++k) {
                     const float wgt = (mr[k] == -INFINITY) ? 0.0f : expf(mr[k] - M);
                     Ls = fmaf(ld_dsmem_f32(part + G * D + G + gg, (uint32_t)k), wgt, Ls);
 #pragma unroll

@@ -290,6 +290,9 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
+    // the next kernel may be scheduled now: its CTAs take SMs as this grid's
+    // CTAs leave and wait for this grid to complete
+    grid_dep_launch();
     SSA_MARK(0);
 
     if (warp == 0) {
@@ -481,7 +484,6 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     SSA_GT(0);
     tc_fence_before();
     __syncthreads();
-    grid_dep_launch();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tbase, CF::TCOLS);

@@ -408,6 +408,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
     SSA_MARK(20);
     SSA_GT(1);
     grid_dep_wait();
+    // the attention kernel may be scheduled now: its CTAs take SMs as this
+    // grid's CTAs leave, set up, and wait for this grid to complete
+    grid_dep_launch();
     SSA_MARK(2);
     SSA_GT(2);
 
@@ -588,7 +591,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         SSA_MARK(4);
     }
     SSA_GT(3);
-    grid_dep_launch();
 }
 
 }  // namespace ssa
