@@ -24,8 +24,8 @@
 //    128 at a time -- S = K Q^T and O^T = V^T P with tcgen05.mma, fp32
 //    accumulators in tensor memory, P split into two bf16 terms (hi + lo) so
 //    that the products keep fp32-level accuracy -- and the P CTAs of a unit,
-//    in clusters of 4 or 8, merge their (m, l, acc) through distributed
-//    shared memory (then the clusters' partials through global memory);
+//    in clusters of 4, merge their (m, l, acc) through distributed shared
+//    memory (then the clusters' partials through global memory);
 //  * attend_kernel (head_dim 64): CUDA cores, every warp streaming its rows
 //    with cp.async; the last CTA of a unit merges the P partials.
 #pragma once
@@ -223,10 +223,12 @@ __device__ bool finish_lists(const Params& p, int u, int P, int r, int64_t kept,
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* kept_all = ws_kept(p) + (size_t)u * kMaxSplit;
-    if (tid == 0) kept_all[r] = (uint32_t)kept;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) *flag_smem = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
+    __syncthreads();   // the CTA's writes, then one fence and the count (cumulative)
+    if (tid == 0) {
+        kept_all[r] = (uint32_t)kept;
+        __threadfence();
+        *flag_smem = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
+    }
     __syncthreads();
     const bool last = *flag_smem != 0u;
     if (!last) return false;
@@ -328,17 +330,17 @@ __device__ void merge_partials(const Params& p, int b, int h, const float* parts
 }
 
 // ---------------------------------------------------------------------------
-// attend_tc_kernel: head_dim 128, tensor cores, clusters of CL CTAs
+// attend_tc_kernel: head_dim 128, tensor cores, clusters of kClusterCtas CTAs
 // ---------------------------------------------------------------------------
 
-constexpr int kTcList = 1024;   // list entries staged at a time
+constexpr int kClusterCtas = 4;   // attend_tc_kernel: the CTAs of a unit merged on chip
 constexpr int kTcGatherWarps = 7;                       // warps 5 .. 11
 constexpr int kTcThreads = (5 + kTcGatherWarps) * 32;   // 384
 
 // A chunk is one 128-row MMA operand of K (and one of V) rows in the
 // 128-byte swizzled layout: row i's 16-byte piece c at piece c ^ (i & 7) of
 // the row's 64-dim plane.
-template <int G>
+template <int G, int LIST>   // LIST: list entries staged at a time (1024 or 4096)
 struct KTCfg {
     static constexpr int D = 128;
     static constexpr int CH = 128;                                 // listed rows per chunk
@@ -350,8 +352,8 @@ struct KTCfg {
     static constexpr uint32_t OFF_Q = OFF_V + 2u * KV;             // query operand: 16 x 128, 4 KB
     static constexpr uint32_t OFF_P = OFF_Q + 2u * QPLANE;         // 2 x P operand: 16 columns x 128 rows
     static constexpr uint32_t OFF_LIST = OFF_P + 2u * 2u * QPLANE; // cidx, clp
-    static constexpr uint32_t OFF_RAW = OFF_LIST + (uint32_t)kTcList * 8u;    // raw list staging
-    static constexpr uint32_t OFF_PART = OFF_RAW + (uint32_t)kTcList * 8u;    // (acc, m, l): G * D + 2G floats
+    static constexpr uint32_t OFF_RAW = OFF_LIST + (uint32_t)LIST * 8u;       // raw list staging
+    static constexpr uint32_t OFF_PART = OFF_RAW + (uint32_t)LIST * 8u;       // (acc, m, l): G * D + 2G floats
     static constexpr uint32_t OFF_RED = OFF_PART + (uint32_t)(G * D + 2 * G) * 4u;   // [2][2][4][G] floats
     static constexpr uint32_t OFF_BAR = (OFF_RED + 2u * 2u * 4u * G * 4u + 7u) & ~7u;
     static constexpr uint32_t NBAR = 10;                           // kv_full, kv_free, s_full, p_ready, o_full (x2)
@@ -363,27 +365,28 @@ struct KTCfg {
     static_assert(2 * G <= 16, "P's hi and lo columns fit in N = 16");
 };
 
-template <int G>
+template <int G, int LIST>
 constexpr uint32_t ktc_smem_bytes(int nlists)
 {
-    return KTCfg<G>::OFF_PRE + (uint32_t)(nlists + 1) * 4u + 1024u;   // + alignment slack
+    return KTCfg<G, LIST>::OFF_PRE + (uint32_t)(nlists + 1) * 4u + 1024u;   // + alignment slack
 }
 
 // Thread roles (kTcThreads): warps 0-3 epilogue (tensor-memory lanes =
 // chunk rows for S, = head dims for O), warp 4 issues the MMAs (and owns the
 // tensor memory), warps 5 .. 11 gather the K and V rows.  Chunk g uses buffers
 // g & 1; barrier phases count chunks over the whole CTA.
-template <int G, int CL>
+template <int G, int LIST>
 __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_constant__ Params p)
 {
-    using CF = KTCfg<G>;
+    using CF = KTCfg<G, LIST>;
+    constexpr int CL = kClusterCtas;
     constexpr int D = CF::D;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     __shared__ uint32_t scan[kTcThreads / 32];
     int32_t* cidx = reinterpret_cast<int32_t*>(smem + CF::OFF_LIST);
-    float* clp = reinterpret_cast<float*>(smem + CF::OFF_LIST + kTcList * 4);
+    float* clp = reinterpret_cast<float*>(smem + CF::OFF_LIST + LIST * 4);
     float* part = reinterpret_cast<float*>(smem + CF::OFF_PART);
     float* red = reinterpret_cast<float*>(smem + CF::OFF_RED);   // [parity][max | sum][warp][G]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
@@ -454,11 +457,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
     const uint32_t k_a = smem_addr(smem + CF::OFF_K), v_a = smem_addr(smem + CF::OFF_V);
     const uint32_t q_a = smem_addr(smem + CF::OFF_Q), p_a = smem_addr(smem + CF::OFF_P);
 #pragma unroll 1
-    for (int64_t c0 = lo; c0 < hi; c0 += kTcList) {
-        const int n = (int)min((int64_t)kTcList, hi - c0);
+    for (int64_t c0 = lo; c0 < hi; c0 += LIST) {
+        const int n = (int)min((int64_t)LIST, hi - c0);
         int32_t* ridx = reinterpret_cast<int32_t*>(smem + CF::OFF_RAW);
-        float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + kTcList * 4);
-        const int nk = stage_decide<kTcList, kTcThreads>(p, u, b, h, c0, n, lo + kept, pre, nlists, us, ridx, rval, cidx,
+        float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4);
+        const int nk = stage_decide<LIST, kTcThreads>(p, u, b, h, c0, n, lo + kept, pre, nlists, us, ridx, rval, cidx,
                                                          clp, scan);
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
@@ -708,10 +711,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
             }
         }
         if (ncl > 1) {
-            __threadfence();
-            __syncthreads();
-            if (tid == 0)
+            __syncthreads();   // the cluster partial's writes, then one fence and the count
+            if (tid == 0) {
+                __threadfence();
                 misc[2] = (atomicAdd(&ws_ctrl(p)[u].k3_cdone, 1u) == (uint32_t)(ncl - 1)) ? 1u : 0u;
+            }
             __syncthreads();
             if (misc[2]) {
                 __threadfence();

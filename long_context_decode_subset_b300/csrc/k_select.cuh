@@ -559,8 +559,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         sh.zw[warp][0] = zh;
         sh.zw[warp][1] = zl;
     }
-    __threadfence();
-    __syncthreads();
+    __syncthreads();   // the CTA's list and candidate writes; one fence below covers them (cumulative)
     SSA_MARK(19);
     if (warp == 0) {   // the warps' shares, a fixed tree over 16 lanes
         float hh = lane < kSelWarps ? sh.zw[lane][0] : 0.0f, ll = lane < kSelWarps ? sh.zw[lane][1] : 0.0f;

@@ -185,26 +185,30 @@ kfn_t pick_score(int G, int dsel, bool hist)
 }
 
 template <int G>
-kfn_t att_fn(int d, int cl, uint32_t* smem, int nlists, bool* tc)
+kfn_t att_fn(int d, uint32_t* smem, int nlists, bool* tc)
 {
     *tc = (d == 128);
-    if (d == 128) {
-        *smem = ktc_smem_bytes<G>(nlists);
-        return cl == 8 ? &attend_tc_kernel<G, 8> : &attend_tc_kernel<G, 4>;
+    if (d == 128) {   // the larger list staging when it fits
+        if (ktc_smem_bytes<G, 4096>(nlists) <= 227u * 1024u) {
+            *smem = ktc_smem_bytes<G, 4096>(nlists);
+            return &attend_tc_kernel<G, 4096>;
+        }
+        *smem = ktc_smem_bytes<G, 1024>(nlists);
+        return &attend_tc_kernel<G, 1024>;
     }
     *smem = k3_smem_bytes<G, 64>(nlists);
     return &attend_kernel<G, 64>;
 }
 
-// K3 for this shape: the tensor-core kernel (clusters of `cl` = 4 or 8 CTAs)
-// at head_dim 128, the CUDA-core kernel at 64.
-kfn_t pick_attend(int G, int d, int cl, uint32_t* smem, int nlists, bool* tc)
+// K3 for this shape: the tensor-core kernel (clusters of kClusterCtas) at
+// head_dim 128, the CUDA-core kernel at 64.
+kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists, bool* tc)
 {
     switch (G) {
-        case 1: return att_fn<1>(d, cl, smem, nlists, tc);
-        case 2: return att_fn<2>(d, cl, smem, nlists, tc);
-        case 4: return att_fn<4>(d, cl, smem, nlists, tc);
-        default: return att_fn<8>(d, cl, smem, nlists, tc);
+        case 1: return att_fn<1>(d, smem, nlists, tc);
+        case 2: return att_fn<2>(d, smem, nlists, tc);
+        case 4: return att_fn<4>(d, smem, nlists, tc);
+        default: return att_fn<8>(d, smem, nlists, tc);
     }
 }
 
@@ -360,58 +364,38 @@ int64_t active_clusters(kfn_t fn, int cl, int threads, uint32_t smem)
     return v;
 }
 
-// K3's split: P CTAs per unit (at most kMaxSplit) and, for the tensor-core
-// kernel, the cluster size `cl`: as many clusters per unit as fit in one
-// wave, of 8 CTAs if that gives as many CTAs as clusters of 4 (fewer
-// partials to merge), else of 4.  SSA_FORCE_SPLIT sets P (clusters of 4, P
-// rounded up to a multiple).
-void attend_split(const ssa::Plan& pl, const ssa_shape& s, int* P, int* cl)
+// K3's split: P CTAs per unit (at most kMaxSplit): as many as fit in one
+// wave with every unit getting the same number (for the tensor-core kernel
+// a whole number of clusters), unless SSA_FORCE_SPLIT says otherwise
+// (rounded up to whole clusters).
+int attend_split(const ssa::Plan& pl, const ssa_shape& s)
 {
     uint32_t smem = 0;
     bool tc = false;
     const int forced = env_int("SSA_FORCE_SPLIT", 0);
     const int64_t U = std::max<int64_t>(pl.U, 1);
-    kfn_t fn = pick_attend(pl.G, s.head_dim, 4, &smem, pl.ntile * kSelWarps, &tc);
-    *cl = 1;
+    kfn_t fn = pick_attend(pl.G, s.head_dim, &smem, pl.ntile * kSelWarps, &tc);
     if (tc) {
-        int c = 4, ncl;
-        if (forced > 0) {
-            ncl = (forced + 3) / 4;
-        } else {
-            kfn_t fn8 = pick_attend(pl.G, s.head_dim, 8, &smem, pl.ntile * kSelWarps, &tc);
-            const int64_t n8 = std::min<int64_t>(active_clusters(fn8, 8, kTcThreads, smem) / U, kMaxSplit / 8);
-            const int64_t n4 = std::min<int64_t>(active_clusters(fn, 4, kTcThreads, smem) / U, kMaxSplit / 4);
-            if (n8 >= 1 && 8 * n8 >= 4 * n4) {   // as many CTAs, fewer partials to merge
-                c = 8;
-                ncl = (int)n8;
-            } else {
-                ncl = (int)n4;
-            }
-        }
-        ncl = std::max(1, std::min(ncl, kMaxSplit / c));
-        *P = ncl * c;
-        *cl = c;
-        return;
+        int64_t ncl = forced > 0 ? (forced + kClusterCtas - 1) / kClusterCtas
+                                 : active_clusters(fn, kClusterCtas, kTcThreads, smem) / U;
+        ncl = std::max<int64_t>(1, std::min<int64_t>(ncl, kMaxSplit / kClusterCtas));
+        return (int)ncl * kClusterCtas;
     }
-    if (forced > 0) {
-        *P = std::min(forced, kMaxSplit);
-        return;
-    }
+    if (forced > 0) return std::min(forced, kMaxSplit);
     const int64_t slots = (int64_t)blocks_per_sm(fn, k3Threads, smem) * device_sms();
-    *P = (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, slots / U));
+    return (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, slots / U));
 }
 
 ssa_status launch_attend(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream)
 {
-    int P = 1, cl = 1;
-    attend_split(p.pl, s, &P, &cl);
     uint32_t smem = 0;
     bool tc = false;
-    kfn_t fn = pick_attend(p.pl.G, s.head_dim, cl == 8 ? 8 : 4, &smem, p.pl.ntile * kSelWarps, &tc);
+    kfn_t fn = pick_attend(p.pl.G, s.head_dim, &smem, p.pl.ntile * kSelWarps, &tc);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
     ssa::Params q = p;
-    q.pl.P = P;
-    return launch(fn, (int64_t)q.pl.U * q.pl.P, tc ? kTcThreads : k3Threads, smem, q, stream, true, tc ? cl : 1);
+    q.pl.P = attend_split(p.pl, s);
+    return launch(fn, (int64_t)q.pl.U * q.pl.P, tc ? kTcThreads : k3Threads, smem, q, stream, true,
+                  tc ? kClusterCtas : 1);
 }
 
 }  // namespace
@@ -708,11 +692,7 @@ ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* 
     const ssa::Plan pl = make_plan(*shape, true);
     if (score_ctas) *score_ctas = pl.k1_grid;
     if (tiles_per_unit) *tiles_per_unit = pl.ntile;
-    if (attend_ctas_per_unit) {
-        int P = 1, cl = 1;
-        attend_split(pl, *shape, &P, &cl);
-        *attend_ctas_per_unit = P;
-    }
+    if (attend_ctas_per_unit) *attend_ctas_per_unit = attend_split(pl, *shape);
     return SSA_OK;
 }
 
