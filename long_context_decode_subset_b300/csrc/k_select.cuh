@@ -507,7 +507,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
     uint2* cseg = ws_cand(p) + (size_t)u * pl.N + (size_t)tile * pl.tt;
     uint32_t* hist2 = ws_hist2(p) + (size_t)u * kBins;   // level-2 histogram of the unit's candidates
     uint32_t cnt = 0;
-    float zh = 0.0f, zl = 0.0f;
+    float zq[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // two (hi, lo) Z accumulators
+    const uint32_t lt = lanemask_lt();
+    // the prefix test in units of 2^-16: prefix < B e / Z_lb * 2^16 (a power-of-two scale, exact)
+    const float bound16 = __fmul_rn(bound_scale, 65536.0f);
 #pragma unroll 1
     for (int c0 = 0; c0 < W2; c0 += kSlice) {
         if (c0 > 0) {
@@ -517,37 +520,50 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         cp_async_wait<0>();
         __syncwarp();
         const int n = min(kSlice, W2 - c0);   // a multiple of 32: the trip count is warp-uniform
+        // tokens [0, nvalid) of the chunk are in the cache (the last tile's tail is not)
+        const int nvalid = (int)min((int64_t)n, pl.N - (base + c0));
+        const uint32_t t0 = (uint32_t)(base + c0);   // token indices fit 31 bits
+        // two tokens (i, i + 32) per step, each with its own Z accumulator
+        // (independent dependency chains); lists stay in index order
 #pragma unroll 1
-        for (int i = lane; i < n; i += 32) {
-            const int64_t t = base + c0 + i;
-            const bool valid = t < pl.N;
-            const float s = ssc[i];
-            const uint32_t k = okey(s);
-            const uint32_t b1 = k >> 20;
-            const bool above = valid && b1 > f1.bin;
-            const bool is_cand = valid && b1 == f1.bin;
-            bool keep = above || is_cand;
-            float val = above ? INFINITY : s;
-            if (valid && b1 < f1.bin && sampling) {
-                const float e = expf(__fsub_rn(s, m));
-                zacc(zh, zl, e);
-                keep = __fmul_ru(e, bound_scale) > __uint2float_rn((uint32_t)su[i]) * 1.52587890625e-05f;
-                val = e;
-            }
-            const uint32_t km = __ballot_sync(0xffffffffu, keep);
-            if (keep) {
-                const uint32_t o = cnt + __popc(km & lanemask_lt());
-                sidx[o] = (int32_t)((uint32_t)t | (is_cand ? kCandFlag : 0u));
-                sval[o] = val;
-            }
-            cnt += __popc(km);
-            if (is_cand) {
-                cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(k, (uint32_t)t);
-                atomicAdd(hist2 + ((k >> 8) & 0xfffu), 1u);
+        for (int i0 = lane; i0 < n; i0 += 64) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = i0 + 32 * q;
+                if (i - lane < n) {   // warp-uniform (n is a multiple of 32)
+                const uint32_t t = t0 + (uint32_t)i;
+                const bool valid = i < nvalid;
+                const float s = ssc[i];
+                const uint32_t k = okey(s);
+                const uint32_t b1 = k >> 20;
+                const bool above = valid && b1 > f1.bin;
+                const bool is_cand = valid && b1 == f1.bin;
+                bool keep = above || is_cand;
+                float val = above ? INFINITY : s;
+                if (sampling && valid && b1 < f1.bin) {
+                    const float e = expf(__fsub_rn(s, m));
+                    zacc(zq[q][0], zq[q][1], e);
+                    keep = __fmul_ru(e, bound16) > __uint2float_rn((uint32_t)su[i]);
+                    val = e;
+                }
+                const uint32_t km = __ballot_sync(0xffffffffu, keep);
+                if (keep) {
+                    const uint32_t o = cnt + __popc(km & lt);
+                    sidx[o] = (int32_t)(t | (is_cand ? kCandFlag : 0u));
+                    sval[o] = val;
+                }
+                cnt += __popc(km);
+                if (is_cand) {
+                    cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(k, t);
+                    atomicAdd(hist2 + ((k >> 8) & 0xfffu), 1u);
+                }
+                }
             }
         }
     }
     SSA_MARK(18);
+    float zh = zq[0][0], zl = zq[0][1];
+    comp_add(zh, zl, zq[1][0], zq[1][1]);
     if (lane == 0) ws_scount(p)[((size_t)u * pl.ntile + tile) * kSelWarps + warp] = cnt;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
