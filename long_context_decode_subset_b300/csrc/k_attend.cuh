@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], kTcGatherWarps);   // one arrive per gather warp
+            mbar_init(&kv_full[i], 32 * kTcGatherWarps);   // every gather thread's copies
             mbar_init(&kv_free[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_ready[i], 4);   // one arrive per epilogue warp
@@ -469,13 +469,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
             // gather: 16-byte pieces of the chunk's K and V rows into the
             // 128-byte swizzled planes (rows past the list read as zeros)
             const int gt = tid - 160;   // 0 .. 32 * kTcGatherWarps - 1
-            // chunk c - 1 is published (its copies landed) once chunk c's are
-            // in flight, so that two chunks stream at a time
-            auto publish = [&](int gg) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kv_full[gg & 1]);
-            };
+            // each thread's copies of chunk c arrive on kv_full when they land
+            // (cp.async.mbarrier.arrive), so publishing never waits on a later
+            // chunk's buffer
 #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int g = gbase + c, bf = g & 1;
@@ -495,21 +491,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
                     cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, valid);
                     cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, valid);
                 }
-                cp_async_commit();
-                if (c >= 1) {
-                    cp_async_wait<1>();
-                    publish(g - 1);
-                }
+                cp_async_mbar_arrive(&kv_full[bf]);
             }
-            if (nc > 0) {
-                cp_async_wait<0>();
-                publish(gbase + nc - 1);
-            }
+            cp_async_wait<0>();
         } else if (warp == 4) {
             if (lane == 0) {
                 auto mma_s = [&](int g) {   // S[g & 1] = K_g Q^T
                     const int bf = g & 1;
                     if (!mbar_wait_bounded(&kv_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
+                    fence_proxy_async_smem();   // the copies (generic proxy) before the MMA's reads
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
