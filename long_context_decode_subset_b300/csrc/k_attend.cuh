@@ -545,6 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
                     uint32_t rr[8];
                     tmem_ld_x8(lane_base + bf * 16u, rr);
                     tmem_ld_wait();
+                    tmem_regs_ready(rr);
 #pragma unroll
                     for (int gg = 0; gg < G; ++gg) s[gg] = __uint_as_float(rr[gg]);
                 }
@@ -605,12 +606,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
                     uint32_t rr[16];
                     tmem_ld_x16(lane_base + 32u + bf * 16u, rr);
                     tmem_ld_wait();
+                    tmem_regs_ready(rr);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) o[k] = __uint_as_float(rr[k]);
                 } else {
                     uint32_t rr[8];
                     tmem_ld_x8(lane_base + 32u + bf * 16u, rr);
                     tmem_ld_wait();
+                    tmem_regs_ready(rr);
 #pragma unroll
                     for (int k = 0; k < 2 * G; ++k) o[k] = __uint_as_float(rr[k]);
                 }

@@ -105,12 +105,22 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
 // K1: scores
 // ---------------------------------------------------------------------------
 
-constexpr int k1Threads = 640;   // warp 0: copies; 1: MMA; 2: tensor memory; 3: query operand; 4-19: epilogue
+// warp 0: copies; 1: MMA; 2: tensor memory; 3: query operand; 4-19: epilogue;
+// with the histogram, 20-23: add the histogram buffers the epilogue hands over
+// to global memory
 constexpr int k1EpiThreads = 512;
+constexpr int kHistWarps = 4;
+__host__ __device__ constexpr int k1_threads(bool hist) { return hist ? 640 + 32 * kHistWarps : 640; }
 constexpr int kGrab = 2;         // stages a CTA takes from the shared queue at a time
+constexpr int kPreIssue = 1;     // stages issued before the set-up barrier
 constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages + accumulator buffers)
 
-template <int DSEL>
+// HIST: the histogram is kept in two shared buffers of 16-bit counts, two
+// bins to a word (the one being filled and the one warp 2 is adding to the
+// unit's global histogram); a buffer is handed over at every change of unit
+// and after kHistRun stages of one unit, so that no count passes 65535.
+constexpr int kHistRun = 127;    // 127 stages x 512 tokens = 65024 counts at most
+template <int DSEL, bool HIST>
 struct K1Cfg {
     static constexpr uint32_t ROW = DSEL * 2;                        // bytes per token row
     static constexpr uint32_t BOX = 256u * ROW;                      // one TMA box
@@ -119,18 +129,20 @@ struct K1Cfg {
     static constexpr int NB = 4;                                     // accumulator buffers
     static constexpr uint32_t TCOLS = 256;                           // NB x 4 tiles x 16 columns
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 16);
+    static constexpr uint32_t HWORDS = kBins / 2;                    // words per histogram buffer
     static constexpr uint32_t OFF_BOP = (uint32_t)S * STAGE;
     static constexpr uint32_t OFF_HIST = OFF_BOP + (uint32_t)S * kQselBytes;
-    static constexpr uint32_t OFF_QROWS = OFF_HIST + kBins * 4;                 // G query rows (<= 2 KB)
+    static constexpr uint32_t OFF_QROWS = OFF_HIST + (HIST ? 2u * HWORDS * 4u : 0u);   // G query rows (<= 2 KB)
     static constexpr uint32_t OFF_INFO = OFF_QROWS + 2048u;                     // kInfo stage descriptors
-    static constexpr uint32_t OFF_BAR = OFF_INFO + kInfo * 8u;
-    static constexpr uint32_t SMEM = OFF_BAR + (3u * S + 2u * NB) * 8u + 16u + 1024u;   // + alignment slack
+    static constexpr uint32_t OFF_HCTL = OFF_INFO + kInfo * 8u;                 // histogram hand-over words
+    static constexpr uint32_t OFF_BAR = OFF_HCTL + 16u;
+    static constexpr uint32_t SMEM = OFF_BAR + (3u * S + 2u * NB + 4u) * 8u + 16u + 1024u;   // + alignment slack
     static_assert(STAGE % 1024 == 0, "stages keep the swizzle atoms aligned");
     static_assert(kInfo > S + NB, "a descriptor outlives its stage's epilogue");
 };
 
-template <int DSEL>
-constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL>::SMEM; }
+template <int DSEL, bool HIST>
+constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL, HIST>::SMEM; }
 
 // K1's work: every unit's stages j < sf are split evenly and contiguously over
 // the CTAs in (unit, j) order; the stages j >= sf of all units form a queue, in
@@ -193,9 +205,9 @@ struct K1Sched {
 };
 
 template <int G, int DSEL, bool HIST, bool UBUF>
-__global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid_constant__ Params p)
 {
-    using CF = K1Cfg<DSEL>;
+    using CF = K1Cfg<DSEL, HIST>;
     constexpr int S = CF::S, NB = CF::NB;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -210,7 +222,10 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + NB;
     uint64_t* ready = tempty + NB;   // a stage's (unit, j) is published
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(ready + S);
+    uint64_t* hdone = ready + S;     // [2] the epilogue has left histogram buffer b
+    uint64_t* hfree = hdone + 2;     // [2] warp 2 has added buffer b to global memory and zeroed it
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(hfree + 2);
+    int* hctl = reinterpret_cast<int*>(smem + CF::OFF_HCTL);   // unit of buffer 0, of buffer 1, hand-overs + 1
 
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -250,14 +265,21 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], k1EpiThreads / 32);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&hdone[i], k1EpiThreads / 32);
+            mbar_init(&hfree[i], kHistWarps);
+        }
+        hctl[2] = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.ks_map);
-        // the first ring's worth of copies go out before the block-wide set-up ends
+        // the first stage's copies go out before the block-wide set-up ends;
+        // the rest of the ring follows it (each issue takes a few hundred
+        // cycles, and the query operand waits for the set-up barrier)
         sch.init(pl, &ws_ctrl(p)[0].k1_next);
-        for (; c_issued < S && !ended; ++c_issued) ended = !produce(c_issued);
+        for (; c_issued < kPreIssue && !ended; ++c_issued) ended = !produce(c_issued);
     }
     if constexpr (HIST) {
-        for (int i = tid; i < kBins; i += k1Threads) hist[i] = 0u;
+        for (int i = tid; i < 2 * (int)CF::HWORDS; i += k1_threads(HIST)) hist[i] = 0u;
     }
     if (warp == 2) tmem_alloc(tslot, CF::TCOLS);
     // the query operand's inputs: the G query rows and the channel list of a
@@ -389,29 +411,50 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
                 tc_commit(&tfull[nb]);
             }
         }
+    } else if (warp >= 20) {
+        if constexpr (HIST) {
+            // warps 20-23 add each histogram buffer the epilogue hands over to
+            // its unit's global histogram and zero it (a quarter each), so that
+            // the epilogue never stops for a change of unit
+            constexpr int QW = (int)CF::HWORDS / kHistWarps;
+            const int w0 = (warp - 20) * QW;
+            volatile int* hc = hctl;
+            uint32_t* hist1 = ws_hist1(p);
+            grid_dep_wait();   // K0 has zeroed the global histograms
+#pragma unroll 1
+            for (int f = 0;; ++f) {
+                const int b = f & 1;
+                if (!mbar_wait_bounded_sleep(&hdone[b], (uint32_t)(f >> 1) & 1u, 256u)) {
+                    flag(status, DEV_TIMEOUT);
+                    break;
+                }
+                const int total = hc[2];   // hand-overs + 1 once the epilogue has finished, else 0
+                if (total != 0 && f >= total - 1) break;
+                uint32_t* hb = hist + (size_t)b * CF::HWORDS;
+                uint32_t* g = hist1 + (size_t)hc[b] * kBins;
+#pragma unroll 4
+                for (int i = w0 + lane; i < w0 + QW; i += 32) {
+                    const uint32_t v = hb[i];
+                    if (v) {
+                        if (v & 0xffffu) atomicAdd(g + 2 * i, v & 0xffffu);
+                        if (v >> 16) atomicAdd(g + 2 * i + 1, v >> 16);
+                        hb[i] = 0u;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hfree[b]);
+            }
+        }
     } else if (warp >= 4) {
         const int tile = (warp - 4) >> 2, quarter = warp & 3, etid = tid - 128;
         const uint32_t k0 = (uint32_t)(p.seed & 0xffffffffu), k1 = (uint32_t)(p.seed >> 32);
-        uint32_t* hist1 = ws_hist1(p);
-        uint16_t* ubuf = ws_ubuf(p);
+        volatile int* hc = hctl;
         int cur_u = -1;
-        bool waited = false;
-        auto flush = [&](int uu) {
-            if (!waited) {
-                grid_dep_wait();   // K0 has zeroed the histograms
-                waited = true;
-            }
-            named_bar_sync(1, k1EpiThreads);
-#pragma unroll 1
-            for (int i = etid; i < kBins; i += k1EpiThreads) {
-                const uint32_t v = hist[i];
-                if (v) {
-                    atomicAdd(hist1 + (size_t)uu * kBins + i, v);
-                    hist[i] = 0u;
-                }
-            }
-            named_bar_sync(1, k1EpiThreads);
-        };
+        int hb = 0, nuse = 0, run = 0;     // histogram buffer in use, uses so far, stages in this use
+        uint32_t* hcur = hist;
+        uint32_t ub = 0u, uh = 0u;          // the unit's batch and KV head
+        float* srow = nullptr;
+        uint16_t* urow = nullptr;
         const uint32_t tl = ((uint32_t)(quarter * 32) << 16) + (uint32_t)tile * 16u;   // lane quarter, tile columns
 #pragma unroll 1
         for (int c = 0;; ++c) {
@@ -421,62 +464,77 @@ __global__ void __launch_bounds__(k1Threads, 1) score_kernel(const __grid_consta
             if (in.x < 0) break;
             const int u = in.x, j = in.y;
             if (c == 0 && warp == 4) SSA_MARKW(21);
-            tc_fence_after();
-            float acc[G];
-            const uint32_t taddr = tbase + tl + (uint32_t)nb * 64u;
-            if constexpr (G == 1) {
-                uint32_t rr[1];
-                tmem_ld_x1(taddr, rr);
-                tmem_ld_wait();
-                acc[0] = __uint_as_float(rr[0]);
-            } else if constexpr (G == 2) {
-                uint32_t rr[2];
-                tmem_ld_x2(taddr, rr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int g = 0; g < 2; ++g) acc[g] = __uint_as_float(rr[g]);
-            } else if constexpr (G == 4) {
-                uint32_t rr[4];
-                tmem_ld_x4(taddr, rr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int g = 0; g < 4; ++g) acc[g] = __uint_as_float(rr[g]);
-            } else {
-                uint32_t rr[8];
-                tmem_ld_x8(taddr, rr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int g = 0; g < 8; ++g) acc[g] = __uint_as_float(rr[g]);
+            if (u != cur_u || (HIST && run == kHistRun)) {
+                if constexpr (HIST) {
+                    if (cur_u >= 0) {
+                        // hand the filled buffer to warp 2 and take the other one
+                        if (warp == 4 && lane == 0) hc[hb] = cur_u;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&hdone[hb]);
+                        hb ^= 1;
+                        ++nuse;
+                        if (nuse >= 2 && !mbar_wait_bounded(&hfree[hb], (uint32_t)((nuse - 2) >> 1) & 1u))
+                            flag(status, DEV_TIMEOUT);
+                        hcur = hist + (size_t)hb * CF::HWORDS;
+                    }
+                    run = 0;
+                }
+                cur_u = u;
+                ub = (uint32_t)(u / p.Hkv);
+                uh = (uint32_t)(u % p.Hkv);
+                srow = p.s_dst + (int64_t)u * pl.N;
+                if constexpr (UBUF) urow = ws_ubuf(p) + (int64_t)u * pl.np;
             }
+            if constexpr (HIST) ++run;
+            tc_fence_after();
+            const int t = j * kStageTok + tile * 128 + quarter * 32 + lane;
+            const uint32_t taddr = tbase + tl + (uint32_t)nb * 64u;
+            uint32_t rr[G];
+            if constexpr (G == 1) tmem_ld_x1(taddr, rr);
+            else if constexpr (G == 2) tmem_ld_x2(taddr, rr);
+            else if constexpr (G == 4) tmem_ld_x4(taddr, rr);
+            else tmem_ld_x8(taddr, rr);
+            // the token's Philox word does not depend on the accumulator: it is
+            // computed while the load is in flight
+            uint32_t x0 = 0u;
+            if constexpr (UBUF) x0 = philox_word0((uint32_t)t, uh, ub, 0u, k0, k1);
+            tmem_ld_wait_after(x0);
+            tmem_regs_ready(rr);
+            float best = __uint_as_float(rr[0]);
+#pragma unroll
+            for (int g = 1; g < G; ++g) best = fmaxf(best, __uint_as_float(rr[g]));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[nb]);
-
-            if constexpr (HIST) {
-                if (u != cur_u) {
-                    if (cur_u >= 0) flush(cur_u);
-                    cur_u = u;
-                }
-            }
-            const int t = j * kStageTok + tile * 128 + quarter * 32 + lane;
             if (t < pl.N) {
-                float best = acc[0];
-#pragma unroll
-                for (int gg = 1; gg < G; ++gg) best = fmaxf(best, acc[gg]);
                 const float s = best * p.scale;
                 if (!isfinite(s)) flag(status, DEV_NONFINITE);
-                p.s_dst[(int64_t)u * pl.N + t] = s;
-                if constexpr (HIST) atomicAdd(&hist[okey(s) >> 20], 1u);
-                if constexpr (UBUF) {
-                    const int b = u / p.Hkv, h = u % p.Hkv;
-                    const uint32_t x0 = philox_word0((uint32_t)t, (uint32_t)h, (uint32_t)b, 0u, k0, k1);
-                    ubuf[(int64_t)u * pl.np + t] = (uint16_t)(x0 >> 16);
+                srow[t] = s;
+                if constexpr (HIST) {
+                    const uint32_t key = okey(s) >> 20;
+                    atomicAdd(&hcur[key >> 1], 1u << ((key & 1u) * 16u));
                 }
+                if constexpr (UBUF) urow[t] = (uint16_t)(x0 >> 16);
             }
         }
         if (warp == 4) SSA_MARKW(23);
         if constexpr (HIST) {
-            if (cur_u >= 0) flush(cur_u);
+            // warp 2 stops at the hand-over it waits for; the buffer in use is
+            // added to global memory here, by all the epilogue warps
+            if (warp == 4 && lane == 0) hc[2] = nuse + 1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hdone[hb]);
+            if (cur_u >= 0) {
+                grid_dep_wait();   // K0 has zeroed the global histograms
+                named_bar_sync(1, k1EpiThreads);
+                uint32_t* g = ws_hist1(p) + (size_t)cur_u * kBins;
+#pragma unroll 1
+                for (int i = etid; i < (int)CF::HWORDS; i += k1EpiThreads) {
+                    const uint32_t v = hcur[i];
+                    if (v & 0xffffu) atomicAdd(g + 2 * i, v & 0xffffu);
+                    if (v >> 16) atomicAdd(g + 2 * i + 1, v >> 16);
+                }
+            }
         }
         if (warp == 4) SSA_MARKW(24);
     }

@@ -72,6 +72,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// The same bounded wait for a thread whose wait is not on the critical path:
+// it sleeps between polls so that it takes no issue slots from the warps it
+// shares a scheduler with.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity, uint32_t sleep_ns,
+                                                        uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(sleep_ns);
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
 // L2 policy: evict-first, for data streamed once (the key summary).
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
@@ -265,6 +280,20 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8])
                  : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, placed after the computation of `x` (work done while the
+// load is in flight: the input keeps the compiler from sinking it below).
+__device__ __forceinline__ void tmem_ld_wait_after(uint32_t x)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::"r"(x) : "memory");
+}
+// After the wait: the registers a tcgen05.ld wrote are read from here on
+// (an empty statement that redefines them, so no read moves above the wait).
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
 {

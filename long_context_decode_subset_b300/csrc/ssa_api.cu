@@ -298,8 +298,9 @@ ssa_status launch_init(const ssa::Params& p, cudaStream_t stream)
 
 ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cudaStream_t stream, bool dependent)
 {
-    const uint32_t smem = s.d_sel == 32 ? k1_smem_bytes<32>() : k1_smem_bytes<16>();
-    return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1Threads, smem, p, stream, dependent);
+    const uint32_t smem = s.d_sel == 32 ? (hist ? k1_smem_bytes<32, true>() : k1_smem_bytes<32, false>())
+                                        : (hist ? k1_smem_bytes<16, true>() : k1_smem_bytes<16, false>());
+    return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1_threads(hist), smem, p, stream, dependent);
 }
 
 ssa_status launch_select(const ssa::Params& p, cudaStream_t stream)
