@@ -140,6 +140,20 @@ ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* 
                             void* ws, size_t ws_bytes, const ssa_shape* shape,
                             cudaStream_t stream);
 
+/* Append step, the step just before the decode path ("FASA: Frequency-Aware
+ * Sparse Attention", section 3, Stage 1: the dominant channels of a token's
+ * key are stored contiguously when the token is appended):
+ *   K[b][h][pos][:] = k_new[b][h][:],   V[b][h][pos][:] = v_new[b][h][:],
+ *   Ks[b][h][pos][j] = k_new[b][h][sel_ch[h][j]]   for j < d_sel.
+ * k_new, v_new: [batch][n_kv_heads][head_dim], contiguous, 16-byte aligned;
+ * K, V, Ks: the cache in the layouts above, ctx_len being its capacity in
+ * tokens; 0 <= pos < ctx_len (else SSA_ERR_INVALID_ARG).  Only row pos is
+ * written.  An out-of-range channel sets SSA_DEV_BAD_INDEX (the channel is
+ * clamped).  ws holds only the device status word here. */
+ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_t* sel_ch, int64_t pos,
+                      ssa_bf16* K, ssa_bf16* V, ssa_bf16* Ks, void* ws, size_t ws_bytes,
+                      const ssa_shape* shape, cudaStream_t stream);
+
 /* Step (a): s_hat[b][h][i] for every token (FASA section 3, Stage 1). */
 ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_ch, float scale,
                      float* s_hat, void* ws, size_t ws_bytes, const ssa_shape* shape,
@@ -174,6 +188,17 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
                       cudaStream_t stream);
+
+/* Append and decode in one chain: the new token (k_new, v_new, as in
+ * ssa_append) is written at position ctx_len - 1 of K, V and Ks by the
+ * chain's first kernel, and the step then attends over all ctx_len tokens,
+ * the new one included.  ctx_len >= 1.  Same results as ssa_append followed
+ * by ssa_decode, without the extra launch. */
+ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new,
+                             ssa_bf16* K, ssa_bf16* V, ssa_bf16* Ks, const int32_t* sel_ch,
+                             int64_t top_k, float budget, uint64_t seed, float scale,
+                             float* out, float* lse, void* ws, size_t ws_bytes,
+                             const ssa_shape* shape, cudaStream_t stream);
 
 /* ssa_decode with the step's query read from, and its result written to,
  * HOST memory (pinned for asynchrony): copies q_host to a device staging

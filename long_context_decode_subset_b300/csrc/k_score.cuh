@@ -65,6 +65,15 @@ struct Params {
     int64_t cap;
     float* out;                // [Bt][Hq][d]
     float* lse;                // [Bt][Hq]
+    // append step (K0 or append_kernel), active when k_new is set: the new
+    // token's rows [Bt][Hkv][d] go to position app_pos of K, V and Ks
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* app_K;
+    uint16_t* app_V;
+    uint16_t* app_Ks;
+    int64_t app_pos;
+    int64_t ks_sb, ks_sh;
 };
 
 __device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
@@ -86,11 +95,46 @@ __device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_
 // lets the next kernel launch at once: K1 streams the summary meanwhile and
 // waits for K0 only before its first histogram flush.
 // ---------------------------------------------------------------------------
+// The append step for unit u = (b, h_kv), the step just before the decode path
+// ("FASA: Frequency-Aware Sparse Attention", section 3, Stage 1: a token's
+// dominant channels are stored contiguously when it is appended):
+//   K[b][h][pos] = k_new[b][h],  V[b][h][pos] = v_new[b][h],
+//   Ks[b][h][pos][j] = k_new[b][h][S_ch[h][j]].
+// An out-of-range channel is flagged and clamped.
+__device__ __forceinline__ void append_unit(const Params& p, int u, int tid, int nthreads)
+{
+    const int b = u / p.Hkv, h = u % p.Hkv;
+    const int d = p.d;
+    const int64_t src = ((int64_t)b * p.Hkv + h) * d;
+    const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh + p.app_pos * d;
+    const int nq = d / 8;   // 16-byte pieces of a row
+    for (int i = tid; i < 2 * nq; i += nthreads) {
+        if (i < nq)
+            reinterpret_cast<uint4*>(p.app_K + dst)[i] = reinterpret_cast<const uint4*>(p.k_new + src)[i];
+        else
+            reinterpret_cast<uint4*>(p.app_V + dst)[i - nq] = reinterpret_cast<const uint4*>(p.v_new + src)[i - nq];
+    }
+    for (int j = tid; j < p.d_sel; j += nthreads) {
+        int ch = p.sel_ch[h * p.d_sel + j];
+        if ((unsigned)ch >= (unsigned)d) {
+            flag(ws_status(p), DEV_BAD_INDEX);
+            ch = ch < 0 ? 0 : d - 1;
+        }
+        p.app_Ks[(int64_t)b * p.ks_sb + (int64_t)h * p.ks_sh + p.app_pos * p.d_sel + j] = p.k_new[src + ch];
+    }
+}
+
+__global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ Params p)
+{
+    append_unit(p, blockIdx.x, threadIdx.x, 128);
+}
+
 __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Params p)
 {
     grid_dep_launch();
     const int u = blockIdx.x;
     const int tid = threadIdx.x;
+    if (p.k_new != nullptr) append_unit(p, u, tid, 256);   // read by K1 only after its wait for this grid
     uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
     if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
     uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);

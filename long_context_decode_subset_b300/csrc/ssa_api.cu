@@ -563,10 +563,36 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     return launch_attend(prm, *shape, stream);
 }
 
-ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
-                      const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale, float* out,
-                      float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
-                      int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// The new token of a fused append (ssa_decode_append), or none.
+struct AppendArgs {
+    const ssa_bf16* k_new;
+    const ssa_bf16* v_new;
+    ssa_bf16* K;
+    ssa_bf16* V;
+    ssa_bf16* Ks;
+};
+
+void set_append(ssa::Params& p, const AppendArgs& a, int64_t pos, const ssa_shape& s)
+{
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.app_K = a.K;
+    p.app_V = a.V;
+    p.app_Ks = a.Ks;
+    p.app_pos = pos;
+    p.ks_sb = s.ks_stride_b;
+    p.ks_sh = s.ks_stride_h;
+}
+
+ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                       const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed,
+                       float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
+                       int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                       cudaStream_t stream)
 {
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
@@ -601,12 +627,65 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
     prm.src_mode = prm.dense ? 1 : 0;
     prm.attend = 1;
+    if (app) {
+        // K0 writes the new token at ctx_len - 1.  The score kernel reads that
+        // summary row only from its shared queue (the last stage is never in
+        // a CTA's static share: sf < number of stages), i.e. after its wait
+        // for K0; the attention reads rows after its own wait.
+        if (pl.sf >= pl.nst) return SSA_ERR_UNSUPPORTED;
+        set_append(prm, *app, shape->ctx_len - 1, *shape);
+    }
     if ((st = launch_init(prm, stream)) != SSA_OK) return st;
     if (!empty && (!prm.dense || s_hat_opt)) {
         if ((st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
         if (!prm.dense && (st = launch_select(prm, stream)) != SSA_OK) return st;
     }
     return launch_attend(prm, *shape, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
+                      const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale, float* out,
+                      float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
+                      int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
+{
+    return decode_impl(nullptr, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt, idx_opt, p_opt,
+                       count_opt, list_cap, ws, ws_bytes, shape, stream);
+}
+
+ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K,
+                             ssa_bf16* V, ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
+                             uint64_t seed, float scale, float* out, float* lse, void* ws, size_t ws_bytes,
+                             const ssa_shape* shape, cudaStream_t stream)
+{
+    const ssa_status st = check_shape(shape);
+    if (st != SSA_OK) return st;
+    if (shape->ctx_len < 1 || !k_new || !v_new || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SSA_ERR_INVALID_ARG;
+    const AppendArgs app{k_new, v_new, K, V, Ks};
+    return decode_impl(&app, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, nullptr, nullptr, nullptr,
+                       nullptr, 0, ws, ws_bytes, shape, stream);
+}
+
+ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_t* sel_ch, int64_t pos,
+                      ssa_bf16* K, ssa_bf16* V, ssa_bf16* Ks, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                      cudaStream_t stream)
+{
+    ssa_status st = check_shape(shape);
+    if (st != SSA_OK) return st;
+    if (!k_new || !v_new || !sel_ch || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
+    if (pos < 0 || pos >= shape->ctx_len) return SSA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(K, 16) || !aligned(V, 16)) return SSA_ERR_INVALID_ARG;
+    const ssa::Plan pl = make_plan(*shape, false);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (pl.U == 0) return SSA_OK;
+    ssa::Params prm = base_params(*shape, pl, ws);
+    prm.sel_ch = sel_ch;
+    set_append(prm, AppendArgs{k_new, v_new, K, V, Ks}, pos, *shape);
+    return launch(&append_kernel, pl.U, 128, 0, prm, stream, false);
 }
 
 ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,

@@ -28,7 +28,7 @@ DEV_NONFINITE, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8
 EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
-    "ssa_query_plan", "ssa_decode_static",
+    "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append",
 ]
 
 
@@ -67,6 +67,8 @@ def load_library():
         "ssa_version": ([], ctypes.c_int),
         "ssa_workspace_bytes": ([SP, i64], sz),
         "ssa_pack_summary": ([P, P, P, P, sz, SP, P], ctypes.c_int),
+        "ssa_append": ([P, P, P, i64, P, P, P, P, sz, SP, P], ctypes.c_int),
+        "ssa_decode_append": ([P, P, P, P, P, P, P, i64, f32, u64, f32, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_score": ([P, P, P, f32, P, P, sz, SP, P], ctypes.c_int),
         "ssa_select": ([P, i64, f32, u64, P, P, P, i64, P, sz, SP, P], ctypes.c_int),
         "ssa_attend": ([P, P, P, P, P, P, i64, f32, P, P, P, sz, SP, P], ctypes.c_int),
@@ -233,6 +235,43 @@ def ssa_decode(q, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale:
                                      float(budget), int(seed) & (2**64 - 1), float(scale), _ptr(out),
                                      _ptr(lse), _ptr(s_hat), _ptr(idx), _ptr(p), _ptr(count), int(cap),
                                      _ptr(ws), ws.numel(), ctypes.byref(shape), _stream(stream)), "ssa_decode")
+    return out, lse
+
+
+def ssa_append(k_new, v_new, sel_ch, pos: int, K, V, Ks, ws=None, stream=None):
+    """Write the new token's rows (k_new, v_new [Bt][Hkv][d]) at position pos of K, V and its summary row of Ks."""
+    Bt, Hkv, N, d = K.shape
+    if tuple(k_new.shape) != (Bt, Hkv, d) or tuple(v_new.shape) != (Bt, Hkv, d):
+        raise ValueError("k_new / v_new must be [Bt][Hkv][head_dim]")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("k_new / v_new must be contiguous")
+    shape = make_shape(Bt, Hkv, Hkv, d, Ks.shape[-1], N, (K.stride(0), K.stride(1)), (Ks.stride(0), Ks.stride(1)))
+    if ws is None:
+        ws = workspace(shape, 0, K.device)
+    _check(load_library().ssa_append(_ptr(k_new), _ptr(v_new), _ptr(sel_ch), int(pos), _ptr(K), _ptr(V), _ptr(Ks),
+                                     _ptr(ws), ws.numel(), ctypes.byref(shape), _stream(stream)), "ssa_append")
+
+
+def ssa_decode_append(q, k_new, v_new, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale: float,
+                      out=None, lse=None, ws=None, stream=None):
+    """Append the new token at position ctx_len - 1 of K, V, Ks, then decode over all ctx_len tokens."""
+    shape = shape_of(q, K, Ks)
+    Bt, Hq, d = q.shape
+    _, Hkv, _, _ = K.shape
+    if tuple(k_new.shape) != (Bt, Hkv, d) or tuple(v_new.shape) != (Bt, Hkv, d):
+        raise ValueError("k_new / v_new must be [Bt][Hkv][head_dim]")
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("k_new / v_new must be contiguous")
+    if out is None:
+        out = torch.empty((Bt, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Bt, Hq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, 0, q.device)
+    _check(load_library().ssa_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V), _ptr(Ks),
+                                            _ptr(sel_ch), int(top_k), float(budget), int(seed) & (2**64 - 1),
+                                            float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                            ctypes.byref(shape), _stream(stream)), "ssa_decode_append")
     return out, lse
 
 

@@ -135,6 +135,31 @@ def pack_summary(K: np.ndarray, sel_ch: np.ndarray, d_sel: int) -> np.ndarray:
     return Ks
 
 
+def append(K: np.ndarray, V: np.ndarray, Ks: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
+           sel_ch: np.ndarray, pos: int):
+    """The append step, the plain definition ("FASA: Frequency-Aware Sparse
+    Attention", section 3, Stage 1: a token's dominant channels are stored
+    contiguously when it is appended).  Returns new arrays with row pos of
+    every (b, h_kv) replaced:  K[b][h][pos] = k_new[b][h],
+    V[b][h][pos] = v_new[b][h],  Ks[b][h][pos][j] = k_new[b][h][sel_ch[h][j]]."""
+    K = np.array(K, np.uint16, copy=True)
+    V = np.array(V, np.uint16, copy=True)
+    Ks = np.array(Ks, np.uint16, copy=True)
+    k_new = np.asarray(k_new, np.uint16)
+    v_new = np.asarray(v_new, np.uint16)
+    sel = np.asarray(sel_ch, np.int64)
+    Bt, Hkv, N, d = K.shape
+    if not 0 <= pos < N:
+        raise ValueError(f"pos {pos} outside the cache of {N} tokens")
+    for b in range(Bt):
+        for h in range(Hkv):
+            K[b, h, pos, :] = k_new[b, h, :]
+            V[b, h, pos, :] = v_new[b, h, :]
+            for j in range(Ks.shape[-1]):
+                Ks[b, h, pos, j] = k_new[b, h, sel[h, j]]
+    return K, V, Ks
+
+
 def score(q: np.ndarray, Ks: np.ndarray, sel_ch: np.ndarray, scale: float) -> np.ndarray:
     """q: uint16 [Bt][Hq][d]; Ks: uint16 [Bt][Hkv][N][d_sel] -> s_hat fp32 [Bt][Hkv][N]."""
     q = _c(q, np.uint16)

@@ -123,3 +123,24 @@ def test_binding_requires_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         binding.load_library()
+
+
+def test_append_entry_points_validate():
+    lib = ssa.load_library()
+    s = _shape()
+    f = P(1 << 20)
+    n = s.ctx_len
+    assert lib.ssa_append(None, f, f, 0, f, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_append(f, f, f, -1, f, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_append(f, f, f, n, f, f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_append(f, f, f, 0, P((1 << 20) + 2), f, f, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_append(f, f, f, 0, f, f, f, f, 16, ctypes.byref(s), None) == 3
+    assert lib.ssa_append(f, f, f, 0, f, f, f, f, 1 << 40, ctypes.byref(_shape(head_dim=80)), None) == 2
+    assert lib.ssa_decode_append(f, None, f, f, f, f, f, 5, 1.0, 0, 0.1, f, f, f, 1 << 40, ctypes.byref(s),
+                                 None) == 1
+    assert lib.ssa_decode_append(f, f, f, f, f, f, f, 5, 1.0, 0, 0.1, f, f, f, 1 << 40,
+                                 ctypes.byref(_shape(ctx_len=0)), None) == 1
+    assert lib.ssa_decode_append(f, P((1 << 20) + 8), f, f, f, f, f, 5, 1.0, 0, 0.1, f, f, f, 1 << 40,
+                                 ctypes.byref(s), None) == 1
+    assert lib.ssa_decode_append(f, f, f, f, f, f, f, -5, 1.0, 0, 0.1, f, f, f, 1 << 40, ctypes.byref(s),
+                                 None) == 1
