@@ -278,6 +278,30 @@ def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
         res["e2e_us"] = [a.elapsed_time(b) * 1e3 for a, b in ev2]
         res["h2d"] = q_host.numel() * 2
         res["d2h"] = out_h.numel() * 4 + lse_h.numel() * 4
+
+        # the serving form of the step: the new token's K/V rows and summary row appended by the chain's
+        # first kernel (ssa_decode_append).  The appended row is the cache's last one, so the cache keeps
+        # its values from step to step.
+        N = cfg.ctx_len
+        k_new = K[:, :, N - 1].contiguous()
+        v_new = V[:, :, N - 1].contiguous()
+        ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(warmup):
+            ssa.ssa_decode_append(q, k_new, v_new, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out=out,
+                                  lse=lse, ws=ws, stream=stream)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(50_000_000)
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev3[i][0].record(stream)
+            ssa.ssa_decode_append(q, k_new, v_new, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out=out,
+                                  lse=lse, ws=ws, stream=stream)
+            ev3[i][1].record(stream)
+        torch.cuda.synchronize()
+        st, flags = ssa.ssa_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags:#x}")
+        res["append_us"] = [a.elapsed_time(b) * 1e3 for a, b in ev3]
     del flush
     return res
 
@@ -358,6 +382,9 @@ def run_ours(args):
         },
         "e2e": {"value": round(e2e_us / world, 3), "unit": UNIT, "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": m["d2h"], "api": "ssa_decode_host (pinned host q in, out/lse back)"},
+        "append_step": {"value": round(statistics.fmean(m["append_us"]), 3), "unit": UNIT,
+                        "api": "ssa_decode_append (the new token's K/V and summary rows written by the chain's "
+                               "first kernel, then the step over all tokens)"},
         "gpu_launches": 4 * args.steps,
         "clocks": m["clocks"],
         "wall_s": round(wall, 2),
