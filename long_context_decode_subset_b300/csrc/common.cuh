@@ -85,6 +85,7 @@ struct Plan {
     int32_t ntile;       // K2 tiles per unit
     int64_t np;          // ntile * tt: padded tokens per unit
     int32_t P;           // K3 CTAs per unit
+    int32_t hist_run;    // K1: stages of one unit per shared-histogram buffer (1..127)
     // workspace byte offsets
     size_t o_status, o_ctrl, o_hist1, o_zpart, o_scount, o_kept, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf,
         o_part, o_hq, o_hout, o_hlse, total;

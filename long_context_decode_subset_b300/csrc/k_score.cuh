@@ -163,7 +163,7 @@ constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages +
 // bins to a word (the one being filled and the one warp 2 is adding to the
 // unit's global histogram); a buffer is handed over at every change of unit
 // and after kHistRun stages of one unit, so that no count passes 65535.
-constexpr int kHistRun = 127;    // 127 stages x 512 tokens = 65024 counts at most
+constexpr int kHistRun = 127;    // 127 stages x 512 tokens = 65024 counts at most (Plan::hist_run <= this)
 template <int DSEL, bool HIST>
 struct K1Cfg {
     static constexpr uint32_t ROW = DSEL * 2;                        // bytes per token row
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
             if (in.x < 0) break;
             const int u = in.x, j = in.y;
             if (c == 0 && warp == 4) SSA_MARKW(21);
-            if (u != cur_u || (HIST && run == kHistRun)) {
+            if (u != cur_u || (HIST && run == pl.hist_run)) {
                 if constexpr (HIST) {
                     if (cur_u >= 0) {
                         // hand the filled buffer to warp 2 and take the other one

@@ -44,7 +44,8 @@ int device_sms()
 // Plan and workspace layout.  The layout does not depend on the device; the
 // K1 grid and the K3 split do (the workspace is sized for the largest split).
 // SSA_FORCE_TILE / SSA_FORCE_SPLIT override the tile size and the split (the
-// tests use them to cover many tiles and splits on small inputs).
+// tests use them to cover many tiles and splits on small inputs), and
+// SSA_FORCE_HIST_RUN the score kernel's histogram hand-over period.
 ssa::Plan make_plan(const ssa_shape& s, bool with_device)
 {
     ssa::Plan pl{};
@@ -71,6 +72,12 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.ntile = (int32_t)((N + tt - 1) / tt);
     pl.np = (int64_t)pl.ntile * tt;
     pl.P = 1;   // set at launch (attend_split)
+    // K1's histogram buffers are handed over after at most kHistRun stages of
+    // one unit; SSA_FORCE_HIST_RUN lowers that (the tests use it to hand
+    // buffers over at every stage or two)
+    pl.hist_run = kHistRun;
+    const int forced_run = env_int("SSA_FORCE_HIST_RUN", 0);
+    if (forced_run >= 1 && forced_run <= kHistRun) pl.hist_run = forced_run;
 
     const int64_t G = pl.G, D = s.head_dim;
     const int64_t heads = (int64_t)s.batch * s.n_q_heads;

@@ -1,6 +1,8 @@
 """GPU end-to-end decode parity at small sizes, every plan, and the special
 cases the pages name (dense limit, pure top-k, uniform hybrid)."""
+import contextlib
 import math
+import os
 
 import numpy as np
 import pytest
@@ -145,3 +147,51 @@ def test_strided_cache_layout(oracle_mod):
     ref = gpu_decode(w, cfg.top_k, cfg.budget, 4)
     out, lse = ssa.ssa_decode(w["q"], K, V, Ks, w["sel_ch"], cfg.top_k, cfg.budget, 4, cfg.scale)
     assert torch.equal(out, ref["out"]) and torch.equal(lse, ref["lse"])
+
+
+@contextlib.contextmanager
+def hist_run_env(run):
+    old = os.environ.get("SSA_FORCE_HIST_RUN")
+    os.environ["SSA_FORCE_HIST_RUN"] = str(run)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("SSA_FORCE_HIST_RUN", None)
+        else:
+            os.environ["SSA_FORCE_HIST_RUN"] = old
+
+
+_LONG = {}
+
+
+def _long_case():
+    """Two units of 160K tokens: ~4 score stages per CTA, runs of ~3 stages of one unit."""
+    if not _LONG:
+        cfg = workloads.make_config("ministral8b_32k", batch=1, n_q_heads=8, n_kv_heads=2, ctx_len=163840,
+                                    top_k=1638, budget=1638.0, n_needles=8)
+        w = workloads.generate(cfg, 0, DEV)
+        w["Ks"] = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+        torch.cuda.synchronize()
+        _LONG["w"] = w
+    return _LONG["w"]
+
+
+@pytest.mark.parametrize("name", ["g4_d128", "long"])
+@pytest.mark.parametrize("run", [1, 2])
+def test_decode_parity_with_frequent_histogram_handover(oracle_mod, name, run):
+    """The score kernel hands its shared histogram buffer to the flush warps at a change of unit and
+    after every `run` stages of one unit (at most 127 normally, which only contexts of millions of
+    tokens with few units reach): forcing a hand-over every stage or two must not change the result."""
+    w = _long_case() if name == "long" else case(name)
+    cfg = w["cfg"]
+    with hist_run_env(run):
+        g = gpu_decode(w, cfg.top_k, cfg.budget, 3)
+    assert g["status"] == 0, hex(g["flags"])
+    stats = {}
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            check_unit(oracle_mod, w, g, b, h, cfg.top_k, cfg.budget, 3, stats)
+    assert stats.get("units_differing", 0) <= max(1, stats["units"] // 8), stats
+    ref = gpu_decode(w, cfg.top_k, cfg.budget, 3)
+    assert torch.equal(g["out"], ref["out"]) and torch.equal(g["count"], ref["count"])
