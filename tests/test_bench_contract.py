@@ -1,0 +1,37 @@
+"""bench.py's reference arm (the CPU oracle, the one arm that runs without a
+GPU) prints the JSON line the benchmark contract asks for; the roofline
+traffic figure is reported only for the kernel sources it was measured on."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_the_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "1",
+                        "--workload", "tiny"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["higher_is_better"] is False and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["config"]["workload"] == "tiny"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_traffic_is_reported_only_for_the_measured_sources(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({"w": {"source_sha": bench.source_sha(), "dram_bytes_per_launch": 123.0},
+                             "v": {"source_sha": "0" * 16, "dram_bytes_per_launch": 456.0}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_for("w") == 123.0
+    assert bench.traffic_for("v") is None
+    assert bench.traffic_for("missing") is None
