@@ -206,3 +206,22 @@ def test_attend_empty_and_dense(oracle_mod):
     count.zero_()
     out, lse = ssa.ssa_attend(w["q"], w["K"], w["V"], idx, p, count, cfg.scale)
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), float("-inf")])
+def test_select_flags_nonfinite_scores(bad):
+    """A non-finite score is an error the device reports (SSA_DEV_NONFINITE / SSA_ERR_NONFINITE); the
+    selection's content is then unspecified, but the call completes and its lists stay in bounds."""
+    s = torch.randn((1, 2, 1000), device=DEV)
+    s[0, 1, 123] = bad
+    shape = ssa.make_shape(1, 2, 2, 64, 16, 1000)
+    ws = ssa.workspace(shape, 1000)
+    idx, p, count = ssa.ssa_select(s, 10, 10.0, 0, list_cap=1000, ws=ws)
+    st, flags = ssa.ssa_get_device_status(ws)
+    assert flags & ssa.ssa.DEV_NONFINITE and st == 6, (st, hex(flags))
+    c = count.cpu()
+    assert torch.all((c >= 0) & (c <= 1000))
+    for h in range(2):
+        n = int(c[0, h])
+        ids = idx[0, h, :n].cpu()
+        assert torch.all((ids >= 0) & (ids < 1000))
