@@ -197,6 +197,60 @@ def select_unit(s: np.ndarray, top_k: int, budget: float, seed: int, b: int, h_k
     return res
 
 
+def select_unit_uniform(s: np.ndarray, top_k: int, budget: float, seed: int, b: int, h_kv: int):
+    """The top-k + uniform hybrid ("Stratified Sparse Attention speeds up
+    decoding 2.96x on a 1M context", section "How SSA splits the cache into
+    strata": top-k and hybrids are special cases of the strata).  T is the
+    same top-k stratum as select_unit; every other token j is kept with the
+    same probability p = min(1, fl32(B / fl32(N - k))) (p = 1 for B = +inf),
+    drawn with the same Philox uniform u_j < p.  Returns (idx int32
+    ascending, p fp32)."""
+    s = _c(s, np.float32)
+    N = s.size
+    t_idx = select_unit(s, top_k, 0.0, seed, b, h_kv)[0]
+    n_r = N - t_idx.size
+    if n_r == 0:
+        return t_idx, np.ones(t_idx.size, np.float32)
+    if np.isinf(budget):
+        p_r = np.float32(1.0)
+    else:
+        p_r = min(np.float32(1.0), np.float32(np.float32(budget) / np.float32(n_r)))
+    in_t = np.zeros(N, bool)
+    in_t[t_idx] = True
+    keep = [j for j in range(N) if in_t[j] or uniform(seed, j, h_kv, b) < p_r]
+    idx = np.array(keep, np.int32)
+    return idx, np.where(in_t[idx], np.float32(1.0), p_r).astype(np.float32)
+
+
+def top_p_count(s: np.ndarray, top_p: float) -> int:
+    """Size of the top-p stratum (same section: top-p is another special
+    case): the fewest tokens, taken in the top-k order (score descending,
+    then index ascending), whose share of the softmax of s over all N tokens
+    (computed in double) reaches top_p.  0 for top_p <= 0, N for top_p >= 1."""
+    s = _c(s, np.float32)
+    N = s.size
+    if top_p <= 0.0 or N == 0:
+        return 0
+    if top_p >= 1.0:
+        return N
+    if not np.all(np.isfinite(s)):
+        raise FloatingPointError("non-finite score")
+    bits = s.view(np.uint32).astype(np.uint64)
+    key = np.where(bits >> 31, (~bits) & 0xFFFFFFFF, bits | 0x80000000)   # order key, -0 below +0
+    order = np.lexsort((np.arange(N), -key.astype(np.int64)))
+    w = np.exp(s.astype(np.float64) - float(np.max(s)))
+    mass = np.cumsum(w[order]) / np.sum(w)
+    return int(min(N, np.searchsorted(mass, top_p, side="left") + 1))
+
+
+def select_unit_top_p(s: np.ndarray, top_p: float, budget: float, seed: int, b: int, h_kv: int):
+    """The top-p stratum with the SSA sampler on the rest: T is the top-p set
+    (top_p_count tokens in the top-k order, i.e. the top-k stratum with
+    k = top_p_count) and the remainder is sampled exactly as select_unit
+    samples it.  Returns (idx, p, m, Z) as select_unit does."""
+    return select_unit(s, top_p_count(s, top_p), budget, seed, b, h_kv)
+
+
 def select(s_hat: np.ndarray, top_k: int, budget: float, seed: int, cap: int | None = None):
     """Selection for every unit of s_hat [Bt][Hkv][N].
 
