@@ -46,11 +46,38 @@ def parse_args():
     return ap.parse_args()
 
 
+def _code_only(src: str) -> str:
+    """C/CUDA source with its comments removed and whitespace runs collapsed (string and character
+    literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_sha() -> str:
+    """Hash of the kernel sources, comments and layout excluded: any change that can alter the compiled
+    kernels changes it, a comment does not.  Keys the DRAM traffic recorded in profiles/traffic.json."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

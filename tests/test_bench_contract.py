@@ -35,3 +35,13 @@ def test_traffic_is_reported_only_for_the_measured_sources(tmp_path, monkeypatch
     assert bench.traffic_for("w") == 123.0
     assert bench.traffic_for("v") is None
     assert bench.traffic_for("missing") is None
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    a = 'int f(int x) { return x + 1; } // one\n/* block\n comment */ const char* s = "a // b";\n'
+    b = 'int f(int x)   {\n  return x + 1;   /* other */ }\nconst char* s = "a // b";'
+    c = 'int f(int x) { return x + 2; }\nconst char* s = "a // b";'
+    d = 'int f(int x) { return x + 1; }\nconst char* s = "a // c";'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only(a) != bench._code_only(d)
