@@ -31,7 +31,9 @@
 //   warps 4-19 (four warpgroups, one per 128-token tile) read the
 //            accumulators back (tcgen05.ld), take the max over the G heads,
 //            write the scores, count the top 12 order-key bits per unit, and
-//            draw the 16-bit Philox prefixes.
+//            draw the 16-bit Philox prefixes;
+//   warps 20-23 (decode chain only) add the shared histogram buffers the
+//            epilogue hands over to the units' global histograms.
 #pragma once
 #include "common.cuh"
 
@@ -160,7 +162,7 @@ constexpr int kPreIssue = 1;     // stages issued before the set-up barrier
 constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages + accumulator buffers)
 
 // HIST: the histogram is kept in two shared buffers of 16-bit counts, two
-// bins to a word (the one being filled and the one warp 2 is adding to the
+// bins to a word (the one being filled and the one warps 20-23 are adding to the
 // unit's global histogram); a buffer is handed over at every change of unit
 // and after kHistRun stages of one unit, so that no count passes 65535.
 constexpr int kHistRun = 127;    // 127 stages x 512 tokens = 65024 counts at most (Plan::hist_run <= this)
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
     uint64_t* tempty = tfull + NB;
     uint64_t* ready = tempty + NB;   // a stage's (unit, j) is published
     uint64_t* hdone = ready + S;     // [2] the epilogue has left histogram buffer b
-    uint64_t* hfree = hdone + 2;     // [2] warp 2 has added buffer b to global memory and zeroed it
+    uint64_t* hfree = hdone + 2;     // [2] warps 20-23 have added buffer b to global memory and zeroed it
     uint32_t* tslot = reinterpret_cast<uint32_t*>(hfree + 2);
     int* hctl = reinterpret_cast<int*>(smem + CF::OFF_HCTL);   // unit of buffer 0, of buffer 1, hand-overs + 1
 
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
             if (u != cur_u || (HIST && run == pl.hist_run)) {
                 if constexpr (HIST) {
                     if (cur_u >= 0) {
-                        // hand the filled buffer to warp 2 and take the other one
+                        // hand the filled buffer to warps 20-23 and take the other one
                         if (warp == 4 && lane == 0) hc[hb] = cur_u;
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&hdone[hb]);
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
         }
         if (warp == 4) SSA_MARKW(23);
         if constexpr (HIST) {
-            // warp 2 stops at the hand-over it waits for; the buffer in use is
+            // warps 20-23 stop at the hand-over they wait for; the buffer in use is
             // added to global memory here, by all the epilogue warps
             if (warp == 4 && lane == 0) hc[2] = nuse + 1;
             __syncwarp();
