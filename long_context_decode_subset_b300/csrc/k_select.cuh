@@ -12,8 +12,9 @@
 //   p is independent of m; m is the lower edge of the 12-bit order-key
 //   bucket f that holds the k-th score (the largest when k = 0).
 //
-// One CTA of 512 threads per (unit, tile); each warp owns a 512-token slice
-// of the tile and walks it in index order:
+// One CTA of 512 threads per (unit, tile); each of its 16 warps owns a
+// contiguous slice of the tile (tile / 16 tokens: 512 at 128K, 2048 at 1M),
+// staged through shared memory, and walks it in index order:
 //   * a token above bucket f is in T: it joins the slice's list (p = 1);
 //   * a token of bucket f is a candidate: it joins the slice's list (with
 //     its score) and the unit's candidate array (for the exact k-th);
