@@ -173,6 +173,18 @@ class ClockSampler:
                 "source": self.source}
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over the ranks (the slowest rank's time is the job's time);
+    the values themselves when there is one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def algorithmic_bytes(cfg, rows_selected: float) -> float:
     """Key summary + selected K and V rows + q in + out/lse out (bytes per step)."""
     summary = cfg.batch * cfg.n_kv_heads * cfg.ctx_len * cfg.d_sel * 2
@@ -360,10 +372,7 @@ def run_ours(args):
 
     mean_us = statistics.fmean(m["times_us"])
     e2e_us = statistics.fmean(m["e2e_us"])
-    if world > 1:
-        tt = torch.tensor([mean_us, e2e_us], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_us, e2e_us = tt.tolist()
+    mean_us, e2e_us = max_over_ranks([mean_us, e2e_us], dev)
     peak, peak_kind = measured_peaks()
     abytes = algorithmic_bytes(cfg, m["rows"])
     achieved = abytes / (mean_us * 1e-6) / 1e9

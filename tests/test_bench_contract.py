@@ -45,3 +45,33 @@ def test_source_hash_ignores_comments_but_not_code():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
     assert bench._code_only(a) != bench._code_only(d)
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.max_over_ranks([10.0 + rank, 5.0 - rank, 7.5], "cpu")))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_times_are_the_maximum_over_ranks():
+    """The multi-rank bench reports the slowest rank's times (gloo on CPU, world size 2)."""
+    import socket
+
+    import torch.multiprocessing as mp
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: [11.0, 5.0, 7.5], 1: [11.0, 5.0, 7.5]}
+    assert bench.max_over_ranks([3.0, 4.0], "cpu") == [3.0, 4.0]   # no process group: unchanged
