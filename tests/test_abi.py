@@ -144,3 +144,31 @@ def test_append_entry_points_validate():
                                  ctypes.byref(s), None) == 1
     assert lib.ssa_decode_append(f, f, f, f, f, f, f, -5, 1.0, 0, 0.1, f, f, f, 1 << 40, ctypes.byref(s),
                                  None) == 1
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
+    """include/ssa.h compiles as C99 with warnings as errors, and a C program linked against libssa.so
+    gets the host-side validation statuses (no GPU needed)."""
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include "ssa.h"
+#include <stdio.h>
+int main(void) {
+    ssa_shape s = {2, 32, 8, 128, 32, 0, 4096, 8 * 4096 * 128, 4096 * 128, 8 * 4096 * 32, 4096 * 32};
+    size_t n = ssa_workspace_bytes(&s, 0);
+    ssa_status st = ssa_decode(NULL, NULL, NULL, NULL, NULL, 5, 1.0f, 0, 0.1f, NULL, NULL, NULL, NULL, NULL,
+                               NULL, 0, NULL, 0, &s, 0);
+    printf("%zu %d %s\n", n, (int)st, ssa_status_string(st));
+    return (n > 0 && st == SSA_ERR_INVALID_ARG) ? 0 : 1;
+}
+''')
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(binding.LIB_PATH)
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, "-o", str(exe), str(src), "-L", libdir, "-lssa", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "invalid argument" in r.stdout
