@@ -455,6 +455,19 @@ def run_ours(args):
             "value": round(statistics.fmean(times) * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full decode steps of {cfg.name} (all {cfg.units} units), seeds 0..{len(times) - 1}",
         }
+        # and dense attention over every cached token on the same cores, for context
+        import oracle
+        dense = []
+        t_end = time.perf_counter() + min(5.0, args.cpu_seconds)
+        while not dense or (time.perf_counter() < t_end and len(dense) < 20):
+            t1 = time.perf_counter()
+            oracle.dense_attention(h["q"], h["K"], h["V"], cfg.scale)
+            dense.append(time.perf_counter() - t1)
+        line["cpu_dense"] = {
+            "value": round(statistics.fmean(dense) * 1e6, 1), "unit": UNIT, "cores": cores,
+            "kind": "oracle dense attention (every token, double accumulation)",
+            "sample": f"{len(dense)} full steps of {cfg.name}",
+        }
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
