@@ -32,7 +32,7 @@
  *         counter-based generator (round function, multipliers and Weyl key
  *         schedule), 10 rounds.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - score: s_i = fl32(scale * max_g sum_j q[g][S_ch[j]] * Ks[i][j]), the
  *    dot products taken in double from exact bf16 inputs;
  *  - the deterministic stratum T is the top-k under the total order
