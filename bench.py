@@ -8,8 +8,14 @@ ssa_decode call (four kernels: initialise, score, threshold bucket, attend);
 the seed changes every step.  L2 is flushed (a 256 MiB write) before every
 timed step and each step is timed alone with CUDA events on its stream.
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle
-instead (the reference arm for this method has no runnable upstream code).
+Prints one JSON line (rank 0): value (us per step), roofline (the score
+pass alone against the measured copy bandwidth, with the DRAM traffic
+recorded for these kernel sources), e2e (through ssa_decode_host, host
+memory in and out), append_step (ssa_decode_append, the serving form),
+secondary (the 1M-context workload), cpu_baseline (the oracle on the host
+cores) and cpu_dense (dense attention on the same cores).  --impl reference
+times the CPU oracle instead (the reference arm for this method has no
+runnable upstream code).
 """
 from __future__ import annotations
 
