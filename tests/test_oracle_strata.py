@@ -102,3 +102,39 @@ def test_top_p_stratum_is_the_topk_stratum_of_its_size(oracle_mod):
     a = oracle_mod.select_unit_top_p(s, 0.6, 12.0, 5, 0, 1)
     b = oracle_mod.select_unit(s, kp, 12.0, 5, 0, 1)
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_uniform_hybrid_is_unbiased_by_enumeration(oracle_mod):
+    # with one p on R the corrected numerator and denominator are still exactly unbiased
+    import itertools
+    from test_oracle_attend import _bf16, _dense_sums
+    rng = np.random.default_rng(21)
+    N, d, G, k, B = 12, 16, 2, 3, 4.0
+    qh = _bf16(rng.standard_normal((G, d)) * 0.7)
+    K = _bf16(rng.standard_normal((N, d)))
+    V = _bf16(rng.standard_normal((N, d)))
+    s = rng.standard_normal(N).astype(np.float32)
+    scale = 0.25
+    T = sorted(oracle_mod.select_unit(s, k, 0.0, 0, 0, 0)[0].tolist())
+    R = [j for j in range(N) if j not in T]
+    p_r = float(np.float32(B) / np.float32(N - k))
+    idx, p = oracle_mod.select_unit_uniform(s, k, B, 0, 0, 0)
+    assert set(T) <= set(idx.tolist()) and np.all(p[~np.isin(idx, T)] == np.float32(p_r))
+    num = np.zeros((G, d))
+    den = np.zeros(G)
+    for x in itertools.product([0, 1], repeat=len(R)):
+        prob = 1.0
+        S = list(T)
+        for j, xi in zip(R, x):
+            prob *= p_r if xi else 1.0 - p_r
+            if xi:
+                S.append(j)
+        S.sort()
+        pw = np.array([1.0 if j in T else p_r for j in S], np.float32)
+        out, lse = oracle_mod.attend_unit(qh, K, V, np.array(S, np.int32), pw, scale)
+        w = np.exp(lse.astype(np.float64))
+        num += prob * w[:, None] * out.astype(np.float64)
+        den += prob * w
+    want_num, want_den = _dense_sums(qh, K, V, scale)
+    assert np.allclose(den, want_den, rtol=2e-6)
+    assert np.allclose(num, want_num, rtol=2e-5, atol=2e-5 * np.abs(want_num).max())
