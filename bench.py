@@ -191,6 +191,15 @@ def max_over_ranks(values, device):
     return t.tolist()
 
 
+def replica_figures(step_us: float, e2e_us: float, world: int, device):
+    """The job's figures for `world` replicas each timing its own steps: the step time is the slowest
+    rank's (a replica's step takes that long; it is not divided by the replica count), and the aggregate
+    throughput is `world` steps per that time."""
+    step_us, e2e_us = max_over_ranks([step_us, e2e_us], device)
+    return {"step_us": step_us, "e2e_us": e2e_us, "aggregate_steps_per_s": world * 1e6 / step_us,
+            "aggregate_e2e_steps_per_s": world * 1e6 / e2e_us}
+
+
 def algorithmic_bytes(cfg, rows_selected: float) -> float:
     """Key summary + selected K and V rows + q in + out/lse out (bytes per step)."""
     summary = cfg.batch * cfg.n_kv_heads * cfg.ctx_len * cfg.d_sel * 2
@@ -217,8 +226,13 @@ def u16(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def host_inputs(w, Ks):
-    return dict(q=u16(w["q"]), K=u16(w["K"]), V=u16(w["V"]), Ks=u16(Ks), sel=w["sel_ch"].cpu().numpy())
+def oracle_host_inputs(w, cfg):
+    """Host copies of a workload for the oracle, its key summary packed by the oracle itself (nothing the
+    oracle reads comes from the CUDA library)."""
+    import oracle
+    K = u16(w["K"])
+    sel = w["sel_ch"].cpu().numpy()
+    return dict(q=u16(w["q"]), K=K, V=u16(w["V"]), Ks=oracle.pack_summary(K, sel, cfg.d_sel), sel=sel)
 
 
 def time_oracle(h, cfg, seconds: float, max_steps: int | None = None):
@@ -376,9 +390,8 @@ def run_ours(args):
         dist.barrier()
     wall = time.perf_counter() - t0
 
-    mean_us = statistics.fmean(m["times_us"])
-    e2e_us = statistics.fmean(m["e2e_us"])
-    mean_us, e2e_us = max_over_ranks([mean_us, e2e_us], dev)
+    rep = replica_figures(statistics.fmean(m["times_us"]), statistics.fmean(m["e2e_us"]), world, dev)
+    mean_us, e2e_us = rep["step_us"], rep["e2e_us"]
     peak, peak_kind = measured_peaks()
     abytes = algorithmic_bytes(cfg, m["rows"])
     achieved = abytes / (mean_us * 1e-6) / 1e9
@@ -387,7 +400,7 @@ def run_ours(args):
     score_gbs = score_bytes / (score_us * 1e-6) / 1e9
     line = {
         "metric": METRIC,
-        "value": round(mean_us / world, 3),
+        "value": round(mean_us, 3),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -422,7 +435,9 @@ def run_ours(args):
                      "frac_of_8000": round(achieved / 8000.0, 4),
                      "note": "whole decode step: summary + selected K/V rows + q/out over the step time"},
         },
-        "e2e": {"value": round(e2e_us / world, 3), "unit": UNIT, "h2d_bytes_per_step": m["h2d"],
+        "aggregate_steps_per_s": round(rep["aggregate_steps_per_s"], 1),
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": m["h2d"],
+                "aggregate_steps_per_s": round(rep["aggregate_e2e_steps_per_s"], 1),
                 "d2h_bytes_per_step": m["d2h"], "api": "ssa_decode_host (pinned host q in, out/lse back)"},
         "append_step": {"value": round(statistics.fmean(m["append_us"]), 3), "unit": UNIT,
                         "api": "ssa_decode_append (the new token's K/V and summary rows written by the chain's "
@@ -452,10 +467,8 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle as it stands, on this host's cores, on a bounded sample of the same workload
         w = workloads.generate(cfg, 0, dev)
-        import long_context_decode_subset_b300 as ssa
-        Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
-        h = host_inputs(w, Ks)
-        del w, Ks
+        h = oracle_host_inputs(w, cfg)
+        del w
         times, cores = time_oracle(h, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": round(statistics.fmean(times) * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -492,17 +505,10 @@ def run_reference(args):
     cfg = workloads.CONFIGS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = workloads.generate(cfg, 0, dev)
-    if dev == "cuda":
-        import long_context_decode_subset_b300 as ssa
-        Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
-    else:
-        import oracle
-        Ks = torch.from_numpy(oracle.pack_summary(u16(w["K"]), w["sel_ch"].numpy(), cfg.d_sel).view("int16"))
-        Ks = Ks.view(torch.bfloat16)
-    h = host_inputs(w, Ks)
-    del w, Ks
     import oracle
     oracle.build()
+    h = oracle_host_inputs(w, cfg)
+    del w
     # one untimed step to estimate the cost, then K timed steps within a few minutes:
     # if K full steps would take too long, each step runs the oracle on a subset of
     # units and is scaled to the full step.

@@ -63,9 +63,15 @@
  *
  * Memory and ownership: every buffer, the workspace included, is allocated
  * and owned by the caller.  Device pointers unless stated otherwise.  The
- * library allocates no device memory and keeps no state between calls (the
- * workspace needs no initialisation: each call resets what it uses);
- * calls on different streams need different workspaces.
+ * library allocates no device memory (ssa_decode_static's built-in array,
+ * below, is part of the loaded module).  The results of a call depend only
+ * on its arguments: the workspace needs no initialisation (each call resets
+ * what it uses) and carries nothing from one call to the next.  What the
+ * library does keep, per process, is launch bookkeeping that never changes
+ * a result: the kernels' raised shared-memory limits and occupancy queries
+ * (per kernel and device), the driver entry point that encodes tensor maps,
+ * and the device address of ssa_decode_static's array (per CUDA context).
+ * Calls on different streams need different workspaces.
  *
  * Errors: every entry point validates its arguments on the host and returns
  * a status before launching anything.  All launches are asynchronous on the
@@ -154,12 +160,25 @@ ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_
                       ssa_bf16* K, ssa_bf16* V, ssa_bf16* Ks, void* ws, size_t ws_bytes,
                       const ssa_shape* shape, cudaStream_t stream);
 
-/* Step (a): s_hat[b][h][i] for every token (FASA section 3, Stage 1). */
+/* Worst-case list length per unit: ctx_len (every cached token selected, as
+ * when top_k >= ctx_len or budget = +inf).  A list_cap of at least this
+ * never overflows.  0 on invalid input. */
+size_t ssa_select_capacity(const ssa_shape* shape);
+
+/* Step (a): s_hat[b][h][i] for every token ("FASA: Frequency-Aware Sparse
+ * Attention", section 3, Stage 1 "Token Importance Prediction": each token
+ * scored from the dominant channels only; the query heads of a GQA group
+ * combined by max). */
 ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_ch, float scale,
                      float* s_hat, void* ws, size_t ws_bytes, const ssa_shape* shape,
                      cudaStream_t stream);
 
-/* Step (b): stratified selection from given scores.  Writes idx / p (the
+/* Step (b): stratified selection from given scores ("Stratified Sparse
+ * Attention speeds up decoding 2.96x on a 1M context", section "How SSA
+ * splits the cache into strata": the top-k tokens read deterministically,
+ * the rest sampled with probability proportional to the approximate
+ * attention exp(s), each kept token carrying its inclusion probability p).
+ * Writes idx / p (the
  * first count[u] entries of each unit's row of length list_cap, ascending
  * token order) and count.  A unit whose count exceeds list_cap keeps the
  * first list_cap entries and sets SSA_DEV_OVERFLOW; count still holds the
@@ -169,13 +188,22 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
                       void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
 
 /* Step (c): corrected attention over given selections (rows idx[u][0..min(count[u],
- * list_cap)) with probabilities p > 0). */
+ * list_cap)) with probabilities p > 0): softmax over the logits
+ * scale * q.K_i - log p_i ("FASA", section 3, Stage 2 "Focused Attention
+ * Computation": exact attention over the selected rows at their original
+ * positions; SSA strata section: each kept token corrected by its inclusion
+ * probability, numerator and denominator alike).  An index outside
+ * [0, ctx_len) or a p outside (0, 1] sets SSA_DEV_BAD_INDEX and the entry is
+ * skipped. */
 ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       const int32_t* idx, const float* p, const int32_t* count, int64_t list_cap,
                       float scale, float* out, float* lse,
                       void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
 
-/* The whole step, (a) -> (b) -> (c), enqueued on `stream` as a chain of
+/* The whole step, (a) -> (b) -> (c) ("Stratified Sparse Attention speeds up
+ * decoding 2.96x on a 1M context": estimate, stratify, sample, correct; the
+ * arguments follow its problem statement: query, KV cache, k, budget B,
+ * seed), enqueued on `stream` as a chain of
  * kernels (initialise, score, threshold bucket, decide, attend; each after
  * the first is a programmatic dependent launch).  s_hat_opt, idx_opt,
  * p_opt, count_opt may be NULL; when given they receive the intermediate
@@ -224,9 +252,10 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
  * SSA_STATIC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU that
  * loads the library holds until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture.
+ *   - The first call in a CUDA context (with that context current) looks
+ *     up the array's device address once and remembers it for that context;
+ *     make that first call before any stream capture.  A context created
+ *     anew (after cudaDeviceReset, say) looks it up again.
  *   - Shapes whose scratch (ssa_workspace_bytes(shape, 0)) exceeds the array
  *     are rejected with SSA_ERR_WORKSPACE before anything is enqueued.
  *   - All calls share the one array and it keeps the previous call's

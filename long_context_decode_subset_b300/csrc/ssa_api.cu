@@ -415,6 +415,28 @@ static __device__ __align__(256) unsigned char g_static_scratch[SSA_STATIC_SCRAT
 
 namespace {
 
+// The current CUDA context (driver entry point looked up once), or null.
+CUcontext current_context()
+{
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        else
+            cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
+// The array's device address in the current context, looked up once per
+// context (a context created anew, e.g. after cudaDeviceReset, gets its own
+// entry: the module and its array are loaded again there).
 void* static_scratch_address()
 {
     int dev = 0;
@@ -422,17 +444,28 @@ void* static_scratch_address()
         cudaGetLastError();
         return nullptr;
     }
+    CUcontext ctx = current_context();
+    if (!ctx) {   // no context yet: the symbol lookup makes the device's primary context current
+        void* tmp = nullptr;
+        if (cudaGetSymbolAddress(&tmp, g_static_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        ctx = current_context();
+        if (!ctx) return nullptr;
+    }
     static std::mutex mu;
-    static std::map<int, void*> addr;
+    static std::map<std::pair<CUcontext, int>, void*> addr;
     std::lock_guard<std::mutex> lk(mu);
-    auto it = addr.find(dev);
+    const auto key = std::make_pair(ctx, dev);
+    auto it = addr.find(key);
     if (it != addr.end()) return it->second;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
         cudaGetLastError();
         return nullptr;
     }
-    addr[dev] = ptr;
+    addr[key] = ptr;
     return ptr;
 }
 
@@ -463,6 +496,12 @@ size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap)
     (void)list_cap;
     if (check_shape(shape) != SSA_OK) return 0;
     return make_plan(*shape, false).total;
+}
+
+size_t ssa_select_capacity(const ssa_shape* shape)
+{
+    if (check_shape(shape) != SSA_OK) return 0;
+    return (size_t)shape->ctx_len;
 }
 
 ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* Ks, void* ws, size_t ws_bytes,

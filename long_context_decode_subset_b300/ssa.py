@@ -28,7 +28,7 @@ DEV_NONFINITE, DEV_OVERFLOW, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8
 EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
-    "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append",
+    "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append", "ssa_select_capacity",
 ]
 
 
@@ -66,6 +66,7 @@ def load_library():
         "ssa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "ssa_version": ([], ctypes.c_int),
         "ssa_workspace_bytes": ([SP, i64], sz),
+        "ssa_select_capacity": ([SP], sz),
         "ssa_pack_summary": ([P, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_append": ([P, P, P, i64, P, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_decode_append": ([P, P, P, P, P, P, P, i64, f32, u64, f32, P, P, P, sz, SP, P], ctypes.c_int),
@@ -144,6 +145,11 @@ def ssa_version() -> int:
 
 def ssa_workspace_bytes(shape: ssa_shape, list_cap: int = 0) -> int:
     return int(load_library().ssa_workspace_bytes(ctypes.byref(shape), int(list_cap)))
+
+
+def ssa_select_capacity(shape: ssa_shape) -> int:
+    """Worst-case selected rows per unit (ctx_len): a list capacity that never overflows."""
+    return int(load_library().ssa_select_capacity(ctypes.byref(shape)))
 
 
 def workspace(shape: ssa_shape, list_cap: int = 0, device="cuda") -> torch.Tensor:

@@ -65,12 +65,10 @@ def _load():
             lib.oracle_pack_summary.restype = None
             lib.oracle_score.argtypes = [P, P, P, i32, i32, i32, i32, i32, i64, i64, i64, f32, P]
             lib.oracle_score.restype = None
-            lib.oracle_select_unit.argtypes = [P, i64, i64, f32, u64, i32, i32, P, P, i64, P, P, P]
-            lib.oracle_select_unit.restype = i64
+            lib.oracle_select_unit_m.argtypes = [P, i64, i64, f32, u64, i32, i32, P, P, i64, P, P, P, i32]
+            lib.oracle_select_unit_m.restype = i64
             lib.oracle_attend_unit.argtypes = [P, P, P, i32, i32, P, P, i64, f32, P, P]
             lib.oracle_attend_unit.restype = None
-            lib.oracle_attend.argtypes = [P, P, P, i32, i32, i32, i32, i64, i64, P, P, P, i64, f32, P, P]
-            lib.oracle_attend.restype = None
             lib.oracle_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i64, i64, i64, i64,
                                           i64, i64, f32, u64, f32, P, P, P, P, P, P, i64, P, P]
             lib.oracle_decode.restype = ctypes.c_int
@@ -174,8 +172,13 @@ def score(q: np.ndarray, Ks: np.ndarray, sel_ch: np.ndarray, scale: float) -> np
 
 
 def select_unit(s: np.ndarray, top_k: int, budget: float, seed: int, b: int, h_kv: int,
-                cap: int | None = None, want_p_all: bool = False):
-    """Selection for one unit.  Returns (idx int32, p fp32, m, Z[, p_all]) or raises."""
+                cap: int | None = None, want_p_all: bool = False, m_at_kth: bool = False):
+    """Selection for one unit.  Returns (idx int32, p fp32, m, Z[, p_all]) or raises.
+
+    m_at_kth=False (the library's reading): the reference point m of the
+    exponentials is the lower edge of the 12-bit order-key bucket of the k-th
+    score; True: m is the k-th score itself.  p does not depend on m in exact
+    arithmetic; the pins compare the two readings."""
     s = _c(s, np.float32)
     N = s.size
     cap = N if cap is None else cap
@@ -184,9 +187,10 @@ def select_unit(s: np.ndarray, top_k: int, budget: float, seed: int, b: int, h_k
     m = ctypes.c_float()
     z = ctypes.c_float()
     p_all = np.zeros(max(N, 1), np.float32) if want_p_all else None
-    cnt = _load().oracle_select_unit(_ptr(s), N, int(top_k), float(budget), int(seed), int(b),
-                                     int(h_kv), _ptr(idx), _ptr(p), cap,
-                                     ctypes.addressof(m), ctypes.addressof(z), _ptr(p_all))
+    cnt = _load().oracle_select_unit_m(_ptr(s), N, int(top_k), float(budget), int(seed), int(b),
+                                       int(h_kv), _ptr(idx), _ptr(p), cap,
+                                       ctypes.addressof(m), ctypes.addressof(z), _ptr(p_all),
+                                       1 if m_at_kth else 0)
     if cnt == -1:
         raise FloatingPointError("non-finite score")
     if cnt == -2:
@@ -251,28 +255,6 @@ def select_unit_top_p(s: np.ndarray, top_p: float, budget: float, seed: int, b: 
     return select_unit(s, top_p_count(s, top_p), budget, seed, b, h_kv)
 
 
-def select(s_hat: np.ndarray, top_k: int, budget: float, seed: int, cap: int | None = None):
-    """Selection for every unit of s_hat [Bt][Hkv][N].
-
-    Returns (idx [Bt][Hkv][cap] int32, p [Bt][Hkv][cap] fp32, count [Bt][Hkv] int64, m, Z)."""
-    Bt, Hkv, N = s_hat.shape
-    cap = N if cap is None else cap
-    idx = np.zeros((Bt, Hkv, max(cap, 1)), np.int32)
-    p = np.zeros((Bt, Hkv, max(cap, 1)), np.float32)
-    count = np.zeros((Bt, Hkv), np.int64)
-    m = np.zeros((Bt, Hkv), np.float32)
-    Z = np.zeros((Bt, Hkv), np.float32)
-    for b in range(Bt):
-        for h in range(Hkv):
-            i_, p_, m_, z_ = select_unit(s_hat[b, h], top_k, budget, seed, b, h, cap)
-            idx[b, h, :i_.size] = i_
-            p[b, h, :p_.size] = p_
-            count[b, h] = i_.size
-            m[b, h] = m_
-            Z[b, h] = z_
-    return idx, p, count, m, Z
-
-
 def attend_unit(q_heads, Kb, Vb, idx, p, scale: float):
     """q_heads uint16 [G][d]; Kb/Vb uint16 [N][d]; idx/p lists -> out fp32 [G][d], lse fp32 [G]."""
     q_heads = _c(q_heads, np.uint16)
@@ -285,24 +267,6 @@ def attend_unit(q_heads, Kb, Vb, idx, p, scale: float):
     lse = np.zeros(G, np.float32)
     _load().oracle_attend_unit(_ptr(q_heads), _ptr(Kb), _ptr(Vb), G, d, _ptr(idx), _ptr(p),
                                idx.size, float(scale), _ptr(out), _ptr(lse))
-    return out, lse
-
-
-def attend(q, K, V, idx, p, count, scale: float):
-    """q uint16 [Bt][Hq][d]; K/V uint16 [Bt][Hkv][N][d]; lists [Bt][Hkv][cap]."""
-    q = _c(q, np.uint16)
-    K = _c(K, np.uint16)
-    V = _c(V, np.uint16)
-    idx = _c(idx, np.int32)
-    p = _c(p, np.float32)
-    count = _c(count, np.int64)
-    Bt, Hq, d = q.shape
-    _, Hkv, N, _ = K.shape
-    cap = idx.shape[-1]
-    out = np.zeros((Bt, Hq, d), np.float32)
-    lse = np.zeros((Bt, Hq), np.float32)
-    _load().oracle_attend(_ptr(q), _ptr(K), _ptr(V), Bt, Hq, Hkv, d, Hkv * N * d, N * d,
-                          _ptr(idx), _ptr(p), _ptr(count), cap, float(scale), _ptr(out), _ptr(lse))
     return out, lse
 
 

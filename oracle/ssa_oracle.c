@@ -298,11 +298,17 @@ static int ranked_cmp(const void* pa, const void* pb)
  * Output: the selected indices in ascending order with their p (1 on T).
  * Returns the count, or -1 on non-finite input, -2 when the list would
  * exceed cap.  m_out / z_out report m and the rounded normaliser; p_all
- * (may be NULL) receives p for every token. */
-int64_t oracle_select_unit(const float* s, int64_t N, int64_t top_k, float budget,
-                           uint64_t seed, int32_t b, int32_t h_kv,
-                           int32_t* idx, float* p, int64_t cap,
-                           float* m_out, float* z_out, float* p_all)
+ * (may be NULL) receives p for every token.
+ *
+ * m_mode chooses the reference point m of the exponentials, which the
+ * method leaves free (p is the same for every m in exact arithmetic):
+ * 0 = the lower edge of the 12-bit order-key bucket of the k-th score (the
+ * reading the library follows), 1 = the k-th score itself.  The oracle's
+ * pins compare the two readings. */
+int64_t oracle_select_unit_m(const float* s, int64_t N, int64_t top_k, float budget,
+                             uint64_t seed, int32_t b, int32_t h_kv,
+                             int32_t* idx, float* p, int64_t cap,
+                             float* m_out, float* z_out, float* p_all, int32_t m_mode)
 {
     for (int64_t i = 0; i < N; ++i)
         if (!isfinite(s[i])) return -1;
@@ -318,7 +324,8 @@ int64_t oracle_select_unit(const float* s, int64_t N, int64_t top_k, float budge
     /* in_T[i] = 1 for the top-k stratum */
     unsigned char* in_T = (unsigned char*)calloc((size_t)N, 1);
     for (int64_t r = 0; r < k; ++r) in_T[order[r].idx] = 1;
-    const float m = oracle_bucket_floor(s[order[(k > 0 ? k : 1) - 1].idx]);
+    const float s_k = s[order[(k > 0 ? k : 1) - 1].idx];   /* the k-th score (the largest if k = 0) */
+    const float m = (m_mode == 1) ? s_k : oracle_bucket_floor(s_k);
 
     /* normaliser over the remainder, summed exactly */
     float* e = (float*)malloc(sizeof(float) * (size_t)N);
@@ -359,6 +366,15 @@ int64_t oracle_select_unit(const float* s, int64_t N, int64_t top_k, float budge
     }
     free(e); free(in_T); free(order);
     return overflow ? -2 : count;
+}
+
+/* The selection with the library's reading of m (bucket edge). */
+int64_t oracle_select_unit(const float* s, int64_t N, int64_t top_k, float budget,
+                           uint64_t seed, int32_t b, int32_t h_kv,
+                           int32_t* idx, float* p, int64_t cap,
+                           float* m_out, float* z_out, float* p_all)
+{
+    return oracle_select_unit_m(s, N, top_k, budget, seed, b, h_kv, idx, p, cap, m_out, z_out, p_all, 0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -403,25 +419,6 @@ void oracle_attend_unit(const uint16_t* q_heads /* [G][d] */, const uint16_t* Kb
         lse[g] = (float)(mx + log(den));
     }
     free(acc); free(logit);
-}
-
-/* Attention for every unit from given per-unit lists ([Bt][Hkv][cap]). */
-void oracle_attend(const uint16_t* q, const uint16_t* K, const uint16_t* V,
-                   int32_t Bt, int32_t Hq, int32_t Hkv, int32_t d,
-                   int64_t kv_sb, int64_t kv_sh,
-                   const int32_t* idx, const float* p, const int64_t* count, int64_t cap,
-                   float scale, float* out, float* lse)
-{
-    const int32_t G = Hq / Hkv;
-    const int64_t units = (int64_t)Bt * Hkv;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t unit = 0; unit < units; ++unit) {
-        const int32_t b = (int32_t)(unit / Hkv), h = (int32_t)(unit % Hkv);
-        const int64_t head0 = (int64_t)b * Hq + (int64_t)h * G;
-        oracle_attend_unit(q + head0 * d, K + b * kv_sb + h * kv_sh, V + b * kv_sb + h * kv_sh,
-                           G, d, idx + unit * cap, p + unit * cap, count[unit], scale,
-                           out + head0 * d, lse + head0);
-    }
 }
 
 /* ------------------------------------------------------------------ */

@@ -51,13 +51,15 @@ def _rank(rank, world, port, q):
     import torch.distributed as dist
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
     try:
-        q.put((rank, bench.max_over_ranks([10.0 + rank, 5.0 - rank, 7.5], "cpu")))
+        q.put((rank, (bench.max_over_ranks([10.0 + rank, 5.0 - rank, 7.5], "cpu"),
+                      bench.replica_figures(40.0 + 10.0 * rank, 50.0 - 2.0 * rank, world, "cpu"))))
     finally:
         dist.destroy_process_group()
 
 
 def test_times_are_the_maximum_over_ranks():
-    """The multi-rank bench reports the slowest rank's times (gloo on CPU, world size 2)."""
+    """The multi-rank bench reports the slowest rank's times as the step time and world / that time as
+    the aggregate throughput (gloo on CPU, world size 2)."""
     import socket
 
     import torch.multiprocessing as mp
@@ -73,5 +75,11 @@ def test_times_are_the_maximum_over_ranks():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert got == {0: [11.0, 5.0, 7.5], 1: [11.0, 5.0, 7.5]}
+    for r in (0, 1):
+        times, rep = got[r]
+        assert times == [11.0, 5.0, 7.5]
+        # the replicas' step time is the slowest rank's, never divided by the replica count; the aggregate
+        # throughput counts every replica's steps
+        assert rep == {"step_us": 50.0, "e2e_us": 50.0, "aggregate_steps_per_s": 2 * 1e6 / 50.0,
+                       "aggregate_e2e_steps_per_s": 2 * 1e6 / 50.0}
     assert bench.max_over_ranks([3.0, 4.0], "cpu") == [3.0, 4.0]   # no process group: unchanged

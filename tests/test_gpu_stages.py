@@ -20,6 +20,7 @@ import pytest
 import torch
 
 import long_context_decode_subset_b300 as ssa
+import oracle
 import workloads
 from _util import compare_unit_lists, score_bound, u16
 
@@ -77,7 +78,9 @@ def case(name, seed=0):
 
 
 def oracle_inputs(w):
-    return u16(w["q"]), u16(w["K"]), u16(w["V"]), u16(w["Ks"]), w["sel_ch"].cpu().numpy()
+    """Host copies for the oracle; its key summary is packed by the oracle, not taken from the GPU."""
+    K, sel = u16(w["K"]), w["sel_ch"].cpu().numpy()
+    return u16(w["q"]), K, u16(w["V"]), oracle.pack_summary(K, sel, w["cfg"].d_sel), sel
 
 
 @pytest.mark.parametrize("name", list(SMALL))

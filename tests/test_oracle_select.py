@@ -176,3 +176,59 @@ def test_cap_overflow_is_reported(oracle_mod):
     s = np.zeros(10, np.float32)
     with pytest.raises(OverflowError):
         oracle_mod.select_unit(s, 5, 0.0, 0, 0, 0, cap=3)
+
+
+def _pinned_score_cases():
+    """The selection's pinned input families: ties, constant scores, k = 0, pure top-k, k = N - 1, a
+    single token, signed zeros, clipping, scores spanning many octaves, needles."""
+    rng = np.random.default_rng(11)
+    for N, k, B, kind in [(3000, 40, 40.0, "ties"), (3000, 40, 40.0, "constant"), (2500, 0, 30.0, "normal"),
+                          (2500, 25, 0.0, "normal"), (700, 699, 10.0, "normal"), (1, 0, 5.0, "normal"),
+                          (513, 5, 5.0, "signed_zero"), (4097, 60, 1e6, "normal"), (2000, 30, 30.0, "wide"),
+                          (20000, 200, 200.0, "normal"), (20000, 200, 200.0, "needles")]:
+        if kind == "ties":
+            s = np.round(rng.standard_normal(N) * 2) / 4
+        elif kind == "constant":
+            s = np.full(N, 0.375)
+        elif kind == "signed_zero":
+            s = np.where(rng.random(N) < 0.5, 0.0, -0.0)
+            s[::7] = rng.standard_normal(s[::7].shape)
+        elif kind == "wide":
+            s = rng.standard_normal(N) * np.exp2(rng.integers(-20, 6, N))
+        elif kind == "needles":
+            s = rng.standard_normal(N) * 1.5
+            s[rng.choice(N, 16, replace=False)] += 8
+        else:
+            s = rng.standard_normal(N) * 1.5
+        yield kind, s.astype(np.float32), k, B
+
+
+def test_reference_point_reading_changes_nothing_beyond_rounding(oracle_mod):
+    """The reference point m is free ("How SSA splits the cache into strata" defines p only through the
+    normalised estimate).  Selecting with m = the lower edge of the k-th score's 12-bit key bucket (the
+    library's reading) and with m = the k-th score itself gives the same index sets (apart from tokens
+    with |u - p| <= 1e-6), and p differs only by the roundings that depend on m: fl32(s_j - m) (at most
+    2^-24 |s_j - m| absolute, i.e. that relative error in e_j), the exp and the binary32 product and
+    quotient (2^-24 each), and Z, whose relative error is a weighted mean of its terms' and so at most
+    the largest of them."""
+    eps = 2.0 ** -24
+    for kind, s, k, B in _pinned_score_cases():
+        N = s.size
+        for seed in range(3):
+            ia, pa, ma, Za, pall_a = oracle_mod.select_unit(s, k, B, seed, 0, 1, want_p_all=True)
+            ib, pb, mb, Zb, pall_b = oracle_mod.select_unit(s, k, B, seed, 0, 1, want_p_all=True, m_at_kth=True)
+            assert ma <= mb, (kind, ma, mb)   # the bucket edge lies at or below the k-th score
+            for j in set(ia.tolist()) ^ set(ib.tolist()):
+                u = oracle_mod.uniform(seed, j, 1, 0)
+                assert min(abs(u - float(pall_a[j])), abs(u - float(pall_b[j]))) <= 1e-6, (kind, j)
+            top = set(_order(s)[:min(k, N)])
+            R = np.array([j for j in range(N) if j not in top], np.int64)
+            if R.size == 0 or B == 0.0:
+                assert np.array_equal(pall_a, pall_b)
+                continue
+            da = np.abs(s.astype(np.float64) - float(ma))
+            db = np.abs(s.astype(np.float64) - float(mb))
+            zrel = eps * (da[R].max() + db[R].max() + 2)
+            bound = pall_a.astype(np.float64) * (eps * (da + db + 6) + zrel)
+            diff = np.abs(pall_a.astype(np.float64) - pall_b.astype(np.float64))
+            assert np.all(diff <= bound + 1e-45), (kind, seed, float(np.max(diff / (bound + 1e-45))))
