@@ -2,19 +2,22 @@
 // workspace layout, the per-unit control block and small device helpers.
 //
 // A "unit" is one (batch b, KV head h_kv) pair; u = b * Hkv + h_kv.  One
-// decode step runs four kernels on the caller's stream (programmatic
+// decode step runs three kernels on the caller's stream (programmatic
 // dependent launch lets each start while the previous one drains):
 //   K0 init     zero the per-unit counters and histograms (K1 starts at
 //               once and waits for K0 only before its first histogram flush);
 //   K1 score    every SM streams the key summary (TMA) and scores it on the
 //               tensor cores; order-key histogram; 16-bit Philox prefixes;
-//   K2 bucket   find the bucket of the k-th score; list every token above it,
-//               its members (candidates) and the remainder tokens that can
-//               still be drawn; sum the normaliser over the tokens below it;
-//               the last tile of a unit resolves the exact k-th token and Z;
-//   K3 attend   decide every listed token (top-k stratum or the draw u < p),
-//               split-K gather of the kept K/V rows with the corrected online
-//               softmax; the last CTA of a unit merges the partials.
+//   K2 unit     one thread-block cluster per unit, one CTA per tile of the
+//               unit's tokens: each CTA finds the bucket of the k-th score,
+//               lists every token above it, its members (candidates) and the
+//               remainder tokens that can still be drawn, and sums its share
+//               of the normaliser; after a cluster barrier rank 0 resolves
+//               the exact k-th token and Z; after another, every CTA decides
+//               its listed tokens (top-k stratum, or the draw u < p), gathers
+//               the kept K/V rows and runs the corrected attention on the
+//               tensor cores; rank 0 merges the CTAs' (m, l, acc) through
+//               distributed shared memory.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,28 +50,23 @@ constexpr uint32_t DEV_BAD_INDEX = 0x8u;
 
 constexpr int kBins = 4096;            // 12-bit order-key buckets
 constexpr int kStageTok = 512;         // K1: tokens per pipeline stage (4 MMA tiles of 128)
-constexpr int kTileAlign = 512;       // K2: tiles are multiples of 512 tokens (32 per warp slice)
-constexpr int kSelSlots = 256;         // K2: CTAs the tiles aim at in all
-constexpr int kMaxTiles = 1024;        // K2: tiles per unit at most (the tile grows with N)
-constexpr int kSelThreads = 512;       // K2a / K2c block size; each warp owns a slice (a list) of a tile
+constexpr int kTileAlign = 512;        // K2: tiles are multiples of 512 tokens (32 per warp slice)
+constexpr int kMaxTiles = 16;          // K2: tiles (CTAs of a unit's cluster) per unit at most
+constexpr int kSelThreads = 512;       // K2 block size; in the selection each warp owns a slice (a list) of the tile
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int k3Threads = 256;         // K3 block size
-constexpr int kMaxSplit = 64;          // K3 CTAs per unit at most (the workspace is sized for it)
-constexpr int k3Warps = k3Threads / 32;
+constexpr int kInThreads = 256;        // score_input_kernel block size
 constexpr int kQselBytes = 1024;       // B operand: 16 rows x d_sel bf16, swizzled
 
 // Per-unit control block (zeroed by K0).
 struct UnitCtrl {
-    uint32_t k2a_done;   // K2 tiles finished
-    uint32_t k3_done;    // K3 CTAs finished
+    uint32_t pad0[2];
     uint32_t ncand;      // members of the threshold bucket (the candidate array's length)
     uint32_t theta;      // order key of the k-th largest score
     int32_t idx_cut;     // key == theta and index <= idx_cut: top-k stratum (-1: none)
     float m;             // reference point of the exponentials
     float Z;             // normaliser over the remainder
     uint32_t k1_next;    // unit 0 only: K1's shared stage queue (stages taken)
-    uint32_t k3_cdone;   // K3 clusters finished
-    uint32_t pad[7];
+    uint32_t pad[8];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 
@@ -82,13 +80,12 @@ struct Plan {
     int64_t stages;      // K1 stages in all
     int32_t k1_grid;     // K1 CTAs (persistent)
     int32_t tt;          // K2 tile tokens (multiple of kTileAlign)
-    int32_t ntile;       // K2 tiles per unit
+    int32_t ntile;       // K2 tiles per unit = CTAs of the unit's cluster (1..kMaxTiles)
     int64_t np;          // ntile * tt: padded tokens per unit
-    int32_t P;           // K3 CTAs per unit
     int32_t hist_run;    // K1: stages of one unit per shared-histogram buffer (1..127)
     // workspace byte offsets
-    size_t o_status, o_ctrl, o_hist1, o_zpart, o_scount, o_kept, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf,
-        o_part, o_hq, o_hout, o_hlse, total;
+    size_t o_status, o_ctrl, o_hist1, o_zpart, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
+        o_hout, o_hlse, total;
 };
 
 // ---------------------------------------------------------------------------

@@ -1,5 +1,6 @@
-// k_attend.cuh -- K3: exact softmax attention over the selected rows with
-// the inclusion correction.
+// k_attend.cuh -- K2, the unit kernel: the stratified selection's decisions
+// and the exact softmax attention over the selected rows with the inclusion
+// correction, one thread-block cluster per (batch, KV head) unit.
 //
 // Sources (page title, section):
 //  * "FASA: Frequency-Aware Sparse Attention", section 3, Stage 2 "Focused
@@ -15,30 +16,24 @@
 //    in HBM is kept; section 3: the online-softmax state (m, l, acc), merged
 //    across splits.
 //
-// P CTAs per unit each take an even share of the unit's selected list
-// (positions [r * R / P, (r + 1) * R / P)), staged in shared memory in
-// chunks; every CTA first takes the final keep decisions for its entries
-// (top-k stratum, or the draw u < p with the exact p) and keeps the chosen
-// rows in list order.  Two kernels then do the attention:
-//  * attend_tc_kernel (head_dim 128): the rows go through the tensor cores
-//    128 at a time -- S = K Q^T and O^T = V^T P with tcgen05.mma, fp32
-//    accumulators in tensor memory, P split into two bf16 terms (hi + lo) so
-//    that the products keep fp32-level accuracy -- and the P CTAs of a unit,
-//    in clusters of 4, merge their (m, l, acc) through distributed shared
-//    memory (then the clusters' partials through global memory);
-//  * attend_kernel (head_dim 64): CUDA cores, every warp streaming its rows
-//    with cp.async; the last CTA of a unit merges the P partials.
+// The C CTAs of a unit's cluster each own one tile of its tokens.  With the
+// selection (source 0) every CTA runs the tile pass (k_select.cuh), rank 0
+// resolves the k-th token and Z between two cluster barriers, and every CTA
+// then decides its own tile's listed tokens (top-k stratum, or the draw
+// u < p with the exact p) and keeps the chosen rows in index order.  With
+// every token kept (source 1) a CTA takes its tile's tokens with p = 1; with
+// the caller's lists (source 2) an even share of the unit's list.  The kept
+// rows go through the tensor cores 128 at a time -- S = K Q^T and
+// O^T = V^T P with tcgen05.mma, fp32 accumulators in tensor memory, P split
+// into two bf16 terms (hi + lo) so that the products keep fp32-level
+// accuracy -- and rank 0 merges the CTAs' (m, l, acc) through distributed
+// shared memory.
 #pragma once
 #include "k_select.cuh"
 
 namespace ssa {
 
-
-// ---------------------------------------------------------------------------
-// shared pieces: the unit's list, the final decisions, the compact list
-// ---------------------------------------------------------------------------
-
-// What the decisions need from the selection (per-tile lists only).
+// What the decisions need from the selection (source 0 only).
 struct UnitSel {
     uint32_t theta;
     int64_t cut;
@@ -60,54 +55,17 @@ __device__ __forceinline__ UnitSel load_unit_sel(const Params& p, int u)
     return s;
 }
 
-// The unit's list length.  For per-tile lists (source 0) also the exclusive
-// prefix of the per-slice counts, pre[0..nlists] in shared memory (counts
-// staged with cp.async).  NT threads; ends with a block barrier.
-template <int NT>
-__device__ int64_t list_total(const Params& p, int u, int nlists, uint32_t* pre, uint32_t* scan)
-{
-    const int tid = threadIdx.x;
-    int64_t total = 0;
-    if (p.src_mode == 0) {
-        const uint32_t* sc = ws_scount(p) + (size_t)u * nlists;
-#pragma unroll 1
-        for (int l = tid; l < nlists; l += NT) cp_async_4(pre + l, sc + l);
-        cp_async_commit();
-        cp_async_wait<0>();
-        __syncthreads();
-        const int l0 = nlists * tid / NT, l1 = nlists * (tid + 1) / NT;
-        uint32_t mine = 0;
-#pragma unroll 1
-        for (int l = l0; l < l1; ++l) {
-            const uint32_t c = pre[l];
-            pre[l] = mine;
-            mine += c;
-        }
-        uint32_t tot;
-        const uint32_t before = block_excl_scan<NT>(mine, scan, tot);
-#pragma unroll 1
-        for (int l = l0; l < l1; ++l) pre[l] += before;
-        if (tid == 0) pre[nlists] = tot;
-        total = tot;
-    } else if (p.src_mode == 1) {
-        total = p.pl.N;
-    } else {
-        const int64_t c = p.count_in[u];
-        total = c < 0 ? 0 : (c > p.cap ? p.cap : c);
-    }
-    __syncthreads();
-    return total;
-}
-
-// Entries [c0, c0 + n) of the unit's list (n <= LIST): staged through
+// Entries [c0, c0 + n) of this CTA's list (n <= LIST): staged through
 // ridx / rval (cp.async, one wave), decided, and the kept ones written in
 // list order to cidx / clp (log p) [0, nk).  Returns nk (every thread).
-// With a compact list requested, the kept (index, p) pairs also go to the
-// unit's staging area at stage_at.  NT threads; ends with a block barrier.
+// Source 0: the list is the concatenation of the tile's warp slices, pre[]
+// their exclusive prefix (pre[kSelWarps] = length).  With a compact list
+// requested, the kept (index, p) pairs also go to the unit's staging area at
+// stage_at.  NT threads; ends with a block barrier.
 template <int LIST, int NT>
-__device__ int stage_decide(const Params& p, int u, int b, int h, int64_t c0, int n, int64_t stage_at,
-                            const uint32_t* pre, int nlists, const UnitSel& us, int32_t* ridx, float* rval,
-                            int32_t* cidx, float* clp, uint32_t* scan)
+__device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int64_t c0, int n, int64_t stage_at,
+                            const uint32_t* pre, const UnitSel& us, int32_t* ridx, float* rval, int32_t* cidx,
+                            float* clp, uint32_t* scan)
 {
     constexpr int PER = (LIST + NT - 1) / NT;   // entries per thread at most
     static_assert(PER <= 32, "one keep bit per entry in a word");
@@ -121,12 +79,12 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int64_t c0, in
 #pragma unroll 1
         for (int i = tid; i < n; i += NT) {
             const int64_t pos = c0 + i;
-            int lo_l = 0, hi_l = nlists;   // pre[lo_l] <= pos < pre[hi_l]
+            int lo_l = 0, hi_l = kSelWarps;   // pre[lo_l] <= pos < pre[hi_l]
             while (hi_l - lo_l > 1) {
                 const int mid = (lo_l + hi_l) >> 1;
                 if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
             }
-            const size_t at = (size_t)(lo_l / kSelWarps) * pl.tt + (size_t)(lo_l % kSelWarps) * W2 + (pos - pre[lo_l]);
+            const size_t at = (size_t)tile * pl.tt + (size_t)lo_l * W2 + (size_t)(pos - pre[lo_l]);
             cp_async_4(ridx + i, sidx + at);
             cp_async_4(rval + i, sp + at);
         }
@@ -203,8 +161,12 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int64_t c0, in
         const float pv = (p.src_mode == 1) ? 1.0f : rval[i];
         cidx[at] = j;
         clp[at] = logf(pv);
-        if (p.idx_out)
-            ws_cand(p)[(size_t)u * pl.N + (size_t)(stage_at + at)] = make_uint2((uint32_t)j, __float_as_uint(pv));
+        if (p.idx_out) {
+            if (stage_at + at < pl.N)
+                ws_cand(p)[(size_t)u * pl.N + (size_t)(stage_at + at)] = make_uint2((uint32_t)j, __float_as_uint(pv));
+            else
+                flag(status, DEV_OVERFLOW);
+        }
         ++at;
     }
     __syncthreads();
@@ -212,137 +174,20 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int64_t c0, in
     return (int)nk;
 }
 
-// Records this CTA's kept count; the last CTA of the unit (returned true)
-// writes the count and, if asked, the compact list in list order (copied
-// from the per-CTA staging).  `koff` is shared scratch of at least
-// kMaxSplit + 1 words.  NT threads.
-template <int NT>
-__device__ bool finish_lists(const Params& p, int u, int P, int r, int64_t kept, int64_t total, uint32_t* koff,
-                             uint32_t* flag_smem)
-{
-    const Plan& pl = p.pl;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t* kept_all = ws_kept(p) + (size_t)u * kMaxSplit;
-    __syncthreads();   // the CTA's writes, then one fence and the count (cumulative)
-    if (tid == 0) {
-        kept_all[r] = (uint32_t)kept;
-        __threadfence();
-        *flag_smem = (atomicAdd(&ws_ctrl(p)[u].k3_done, 1u) == (uint32_t)(P - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    const bool last = *flag_smem != 0u;
-    if (!last) return false;
-    __threadfence();
-    if (p.count_out || p.idx_out) {
-        if (warp == 0) {
-            uint32_t run = 0;
-#pragma unroll 1
-            for (int r0 = 0; r0 < P; r0 += 32) {
-                const uint32_t v = (r0 + lane < P) ? __ldcg(kept_all + r0 + lane) : 0u;
-                const uint32_t x = warp_incl_scan(v);
-                if (r0 + lane < P) koff[r0 + lane] = run + x - v;
-                run += __shfl_sync(0xffffffffu, x, 31);
-            }
-            if (lane == 0) koff[P] = run;
-        }
-        __syncthreads();
-        const uint32_t kept_total = koff[P];
-        if (p.count_out && tid == 0) p.count_out[u] = (int32_t)kept_total;
-        if (p.idx_out) {
-            const uint2* stage = ws_cand(p) + (size_t)u * pl.N;
-#pragma unroll 1
-            for (uint32_t o = tid; o < kept_total; o += NT) {
-                int lo_r = 0, hi_r = P;   // koff[lo_r] <= o < koff[hi_r]
-                while (hi_r - lo_r > 1) {
-                    const int mid = (lo_r + hi_r) >> 1;
-                    if (koff[mid] <= o) lo_r = mid; else hi_r = mid;
-                }
-                const int64_t src = total * lo_r / P + (int64_t)(o - koff[lo_r]);
-                const uint2 v = __ldcg(stage + src);
-                if ((int64_t)o < p.cap) {
-                    p.idx_out[(int64_t)u * p.cap + o] = (int32_t)v.x;
-                    p.p_out[(int64_t)u * p.cap + o] = __uint_as_float(v.y);
-                } else {
-                    flag(ws_status(p), DEV_OVERFLOW);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    return true;
-}
-
-// Merge NP partials [NP][G * D + 2G] (acc, then m, then l) in a fixed order
-// (index ascending) and write the unit's output rows and log-sum-exp.  One
-// wave of loads per thread: each of the first 256 threads owns
-// G * D / 256 elements of one head and reads that head's (m, l) of all
-// partials itself.
-template <int G, int D>
-__device__ void merge_partials(const Params& p, int b, int h, const float* parts, int NP)
-{
-    constexpr int MT = 256;   // merging threads
-    constexpr int PS = G * D + 2 * G;   // floats per partial
-    constexpr int EPT = (G * D + MT - 1) / MT;   // elements per thread (same head)
-    static_assert((G * D) % MT == 0 || G * D < MT, "elements split evenly");
-    if (threadIdx.x >= MT) return;
-    const int e0 = threadIdx.x * EPT;
-    if (e0 >= G * D) return;
-    const int g = e0 / D;
-    float M = -INFINITY;
-#pragma unroll 1
-    for (int r0 = 0; r0 < NP; r0 += 16) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (r0 + j < NP) M = fmaxf(M, __ldcg(parts + (size_t)(r0 + j) * PS + G * D + g));
-    }
-    float Ls = 0.0f, A[EPT];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll 1
-        for (int r0 = 0; r0 < NP; r0 += 8) {
-            float mr[8], lr[8], ar[8][EPT];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float* pr = parts + (size_t)(r0 + j) * PS;
-                const bool ok = r0 + j < NP;
-                mr[j] = ok ? __ldcg(pr + G * D + g) : -INFINITY;
-                lr[j] = ok ? __ldcg(pr + G * D + G + g) : 0.0f;
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) ar[j][e] = ok ? __ldcg(pr + e0 + e) : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float wgt = (mr[j] == -INFINITY) ? 0.0f : expf(mr[j] - M);
-                Ls = fmaf(lr[j], wgt, Ls);
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) A[e] = fmaf(ar[j][e], wgt, A[e]);
-            }
-        }
-    }
-    const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + g;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-        const int c = (e0 + e) % D;
-        p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
-        if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
-    }
-}
-
 // ---------------------------------------------------------------------------
-// attend_tc_kernel: head_dim 128, tensor cores, clusters of kClusterCtas CTAs
+// the unit kernel
 // ---------------------------------------------------------------------------
 
-constexpr int kClusterCtas = 4;   // attend_tc_kernel: the CTAs of a unit merged on chip
-constexpr int kTcGatherWarps = 7;                       // warps 5 .. 11
-constexpr int kTcThreads = (5 + kTcGatherWarps) * 32;   // 384
+constexpr int kUGatherWarps = 11;   // warps 5 .. 15 gather the K and V rows
+static_assert((5 + kUGatherWarps) * 32 == kSelThreads, "the attention roles fill the block");
 
 // A chunk is one 128-row MMA operand of K (and one of V) rows in the
 // 128-byte swizzled layout: row i's 16-byte piece c at piece c ^ (i & 7) of
-// the row's 64-dim plane.
-template <int G, int LIST>   // LIST: list entries staged at a time (1024 or 4096)
-struct KTCfg {
-    static constexpr int D = 128;
+// the row's 64-dim plane.  At head_dim 64 only the first plane is gathered:
+// S reads only it, and O's rows for dims 64..127 (from the second plane,
+// whatever it holds) are never read back.
+template <int G, int D, int LIST>   // LIST: list entries staged at a time (1024 or 4096)
+struct UCfg {
     static constexpr int CH = 128;                                 // listed rows per chunk
     static constexpr uint32_t PLANE = CH * 128u;                   // 64 dims x 128 rows, 128-byte swizzle
     static constexpr uint32_t KV = 2u * PLANE;                     // one K or V chunk (32 KB)
@@ -350,41 +195,44 @@ struct KTCfg {
     static constexpr uint32_t OFF_K = 0;                           // 2 chunks
     static constexpr uint32_t OFF_V = OFF_K + 2u * KV;             // 2 chunks
     static constexpr uint32_t OFF_Q = OFF_V + 2u * KV;             // query operand: 16 x 128, 4 KB
+    // before the attention, [0, OFF_Q) holds the selection pass's staging
+    // (and the resolve's) and its shared state
+    static constexpr uint32_t OFF_SEL = kSelStageBytes;
     static constexpr uint32_t OFF_P = OFF_Q + 2u * QPLANE;         // 2 x P operand: 16 columns x 128 rows
     static constexpr uint32_t OFF_LIST = OFF_P + 2u * 2u * QPLANE; // cidx, clp
     static constexpr uint32_t OFF_RAW = OFF_LIST + (uint32_t)LIST * 8u;       // raw list staging
-    static constexpr uint32_t OFF_PART = OFF_RAW + (uint32_t)LIST * 8u;       // (acc, m, l): G * D + 2G floats
-    static constexpr uint32_t OFF_RED = OFF_PART + (uint32_t)(G * D + 2 * G) * 4u;   // [2][2][4][G] floats
+    static constexpr uint32_t PS = (uint32_t)(G * D + 2 * G);                 // (acc, m, l) floats
+    static constexpr uint32_t OFF_PART = OFF_RAW + (uint32_t)LIST * 8u;
+    static constexpr uint32_t OFF_RED = OFF_PART + PS * 4u;                   // [2][2][4][G] floats
     static constexpr uint32_t OFF_BAR = (OFF_RED + 2u * 2u * 4u * G * 4u + 7u) & ~7u;
     static constexpr uint32_t NBAR = 10;                           // kv_full, kv_free, s_full, p_ready, o_full (x2)
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;      // tensor-memory slot, flags
-    static constexpr uint32_t OFF_PRE = OFF_MISC + 64u;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;      // tensor-memory slot, counts
+    static constexpr uint32_t OFF_PRE = OFF_MISC + 64u;            // the tile list's slice prefix
+    static constexpr uint32_t SMEM = OFF_PRE + (uint32_t)(kSelWarps + 1) * 4u + 1024u;   // + alignment slack
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 16);       // S = K Q^T
     static constexpr uint32_t IDESC_O = idesc_bf16_f32_amn(128, 16);   // O^T = V^T P
     static constexpr uint32_t TCOLS = 64;                          // S x2 (cols 0-31), O x2 (cols 32-63)
     static_assert(2 * G <= 16, "P's hi and lo columns fit in N = 16");
+    static_assert(OFF_SEL % 16 == 0 && OFF_SEL + sizeof(SelShared) <= OFF_Q, "selection state fits the K/V chunks");
+    static_assert(D == 64 || D == 128, "head_dim");
 };
 
-template <int G, int LIST>
-constexpr uint32_t ktc_smem_bytes(int nlists)
-{
-    return KTCfg<G, LIST>::OFF_PRE + (uint32_t)(nlists + 1) * 4u + 1024u;   // + alignment slack
-}
+template <int G, int D, int LIST>
+constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST>::SMEM; }
 
-// Thread roles (kTcThreads): warps 0-3 epilogue (tensor-memory lanes =
-// chunk rows for S, = head dims for O), warp 4 issues the MMAs (and owns the
-// tensor memory), warps 5 .. 11 gather the K and V rows.  Chunk g uses buffers
-// g & 1; barrier phases count chunks over the whole CTA.
-template <int G, int LIST>
-__global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_constant__ Params p)
+// Thread roles in the attention (kSelThreads): warps 0-3 epilogue
+// (tensor-memory lanes = chunk rows for S, = head dims for O), warp 4 issues
+// the MMAs (and owns the tensor memory), warps 5 .. 15 gather the K and V
+// rows.  Chunk g uses buffers g & 1; barrier phases count chunks over the
+// whole CTA.  Grid: U * C CTAs, clusters of C = pl.ntile.
+template <int G, int D, int LIST>
+__global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_constant__ Params p)
 {
-    using CF = KTCfg<G, LIST>;
-    constexpr int CL = kClusterCtas;
-    constexpr int D = CF::D;
+    using CF = UCfg<G, D, LIST>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    __shared__ uint32_t scan[kTcThreads / 32];
+    __shared__ uint32_t scan[kSelWarps];
     int32_t* cidx = reinterpret_cast<int32_t*>(smem + CF::OFF_LIST);
     float* clp = reinterpret_cast<float*>(smem + CF::OFF_LIST + LIST * 4);
     float* part = reinterpret_cast<float*>(smem + CF::OFF_PART);
@@ -395,20 +243,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
     uint64_t* s_full = bars + 4;
     uint64_t* p_ready = bars + 6;
     uint64_t* o_full = bars + 8;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + CF::OFF_MISC);   // [0] tensor memory, [1], [2] flags
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + CF::OFF_MISC);   // [0] tensor memory, [3] kept, [4..5] offsets
     uint32_t* pre = reinterpret_cast<uint32_t*>(smem + CF::OFF_PRE);
 
     const Plan& pl = p.pl;
-    const int P = pl.P;
-    const int u = blockIdx.x / P, r = blockIdx.x % P;
+    const int C = pl.ntile;
+    const int u = blockIdx.x / C, r = blockIdx.x % C;   // r is the CTA's rank in the unit's cluster
     const int b = u / p.Hkv, h = u % p.Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nlists = pl.ntile * kSelWarps;
     uint32_t* status = ws_status(p);
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 32 * kTcGatherWarps);   // every gather thread's copies
+            mbar_init(&kv_full[i], 32 * kUGatherWarps);   // every gather thread's copies
             mbar_init(&kv_free[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_ready[i], 4);   // one arrive per epilogue warp
@@ -416,13 +263,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
         }
         fence_mbar_init();
     }
-    if (warp == 4) tmem_alloc(&misc[0], CF::TCOLS);
+    if (warp == 4 && p.attend) tmem_alloc(&misc[0], CF::TCOLS);
     // the query operand: head slot n < G = q_n (the scale is applied to S),
     // slots G..15 zero; K-major, 128-byte swizzle, two 64-dim planes
     if (tid < 256) {
         const int n = tid >> 4, pc = tid & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < G && p.attend)
+        if (n < G && p.attend && pc < D / 8)
             v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + (int64_t)h * G + n) * D + pc * 8);
         *reinterpret_cast<uint4*>(smem + CF::OFF_Q + (pc >> 3) * CF::QPLANE + n * 128 + (((pc & 7) ^ (n & 7)) << 4)) = v;
         fence_proxy_async_smem();
@@ -436,10 +283,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
     SSA_MARK(7);
     SSA_GT(5);
 
-    const int64_t total = list_total<kTcThreads>(p, u, nlists, pre, scan);
+    // this CTA's list: [lo, hi)
+    int64_t lo = 0, hi = 0;
+    if (p.src_mode == 0) {
+        SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
+        const TileSel ts = tile_pass(p, u, r, sh, smem);
+        if (tid == 0) {
+            uint32_t run = 0;
+            for (int w = 0; w < kSelWarps; ++w) {
+                pre[w] = run;
+                run += sh.wcnt[w];
+            }
+            pre[kSelWarps] = run;
+        }
+        // the unit's tiles have written their lists, candidates, level-2
+        // counts and shares of Z: rank 0 resolves the k-th token and Z
+        __threadfence();
+        cluster_sync();
+        SSA_MARK(3);
+        if (r == 0) resolve_unit(p, u, ts.f1, ts.above1, ts.target, ts.m, sh, reinterpret_cast<uint2*>(smem));
+        __threadfence();
+        cluster_sync();
+        SSA_MARK(4);
+        hi = pre[kSelWarps];
+    } else if (p.src_mode == 1) {
+        lo = min(pl.N, (int64_t)r * pl.tt);
+        hi = min(pl.N, lo + pl.tt);
+    } else {
+        const int64_t c = p.count_in[u];
+        const int64_t total = c < 0 ? 0 : (c > p.cap ? p.cap : c);
+        lo = total * r / C;
+        hi = total * (r + 1) / C;
+    }
     SSA_MARK(11);
-    const int64_t lo = total * r / P, hi = total * (r + 1) / P;
     const UnitSel us = load_unit_sel(p, u);
+    const int64_t stage_base = (p.src_mode == 0) ? (int64_t)r * pl.tt : lo;   // the compact list's staging
     const uint16_t* Kb = p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
     const uint16_t* Vb = p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
 
@@ -461,14 +339,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
         const int n = (int)min((int64_t)LIST, hi - c0);
         int32_t* ridx = reinterpret_cast<int32_t*>(smem + CF::OFF_RAW);
         float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4);
-        const int nk = stage_decide<LIST, kTcThreads>(p, u, b, h, c0, n, lo + kept, pre, nlists, us, ridx, rval, cidx,
-                                                         clp, scan);
+        const int nk = stage_decide<LIST, kSelThreads>(p, u, b, h, r, c0, n, stage_base + kept, pre, us, ridx, rval,
+                                                       cidx, clp, scan);
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
             // gather: 16-byte pieces of the chunk's K and V rows into the
             // 128-byte swizzled planes (rows past the list read as zeros)
-            const int gt = tid - 160;   // 0 .. 32 * kTcGatherWarps - 1
+            const int gt = tid - 160;   // 0 .. 32 * kUGatherWarps - 1
+            constexpr int PPR = D / 8;  // pieces per row
             // each thread's copies of chunk c arrive on kv_full when they land
             // (cp.async.mbarrier.arrive), so publishing never waits on a later
             // chunk's buffer
@@ -482,8 +361,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
                 unsigned char* kd = smem + CF::OFF_K + bf * CF::KV;
                 unsigned char* vd = smem + CF::OFF_V + bf * CF::KV;
 #pragma unroll 1
-                for (int q = gt; q < CF::CH * 16; q += 32 * kTcGatherWarps) {
-                    const int i = q >> 4, pc = q & 15;
+                for (int q = gt; q < CF::CH * PPR; q += 32 * kUGatherWarps) {
+                    const int i = q / PPR, pc = q % PPR;
                     const int row = c * CF::CH + i;
                     const bool valid = row < nk;
                     const int64_t j = valid ? (int64_t)cidx[row] : 0;
@@ -636,8 +515,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
 
     // this CTA's partial: acc per head dim, then (m, l) per head
     if (warp < 4) {
+        if (tid < D) {
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) part[gg * D + tid] = acc[gg];
+            for (int gg = 0; gg < G; ++gg) part[gg * D + tid] = acc[gg];
+        }
         if (tid == 0) {
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
@@ -648,320 +529,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(const __grid_c
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 4 && p.attend) {
         tc_fence_after();
         tmem_dealloc(tbase, CF::TCOLS);
     }
-    if (p.count_out || p.idx_out)   // the merge below needs no "last CTA"
-        finish_lists<kTcThreads>(p, u, P, r, kept, total, reinterpret_cast<uint32_t*>(smem + CF::OFF_K), &misc[1]);
+
+    // the compact list: every CTA's kept entries are in index order and the
+    // CTAs' tiles (or list shares) are in rank order, so CTA r's entries go
+    // after those of ranks < r
+    if (p.count_out || p.idx_out) {
+        if (tid == 0) misc[3] = (uint32_t)kept;
+        cluster_sync();
+        if (warp == 0) {
+            const uint32_t v = lane < C ? ld_dsmem_u32(&misc[3], (uint32_t)lane) : 0u;
+            const uint32_t x = warp_incl_scan(v);
+            const uint32_t before = __shfl_sync(0xffffffffu, x - v, r);
+            const uint32_t all = __shfl_sync(0xffffffffu, x, 31);
+            if (lane == 0) {
+                misc[4] = before;
+                misc[5] = all;
+            }
+        }
+        __syncthreads();
+        const uint32_t before = misc[4];
+        if (r == 0 && tid == 0 && p.count_out) p.count_out[u] = (int32_t)misc[5];
+        if (p.idx_out) {
+            const uint2* stage = ws_cand(p) + (size_t)u * pl.N + (size_t)stage_base;
+#pragma unroll 1
+            for (int64_t o = tid; o < kept; o += kSelThreads) {
+                const int64_t dst = (int64_t)before + o;
+                if (stage_base + o >= pl.N) break;   // flagged when staged
+                const uint2 v = __ldcg(stage + o);
+                if (dst < p.cap) {
+                    p.idx_out[(int64_t)u * p.cap + dst] = (int32_t)v.x;
+                    p.p_out[(int64_t)u * p.cap + dst] = __uint_as_float(v.y);
+                } else {
+                    flag(status, DEV_OVERFLOW);
+                }
+            }
+        }
+    }
     SSA_MARK(12);
     SSA_GT(6);
-    // merge the cluster's partials on chip (rank order); with one cluster
-    // per unit it writes the output, with several each writes a cluster
-    // partial and the last cluster to finish merges them in cluster order
-    cluster_sync();
-    if (p.attend && cluster_rank() == 0) {
-        const int ncl = P / CL, cl = r / CL;
-        constexpr int PS = G * D + 2 * G;
-        float* cpart = ws_part(p) + ((size_t)u * kMaxSplit + cl) * PS;
-        constexpr int EPT = (G * D + 255) / 256;
+    // rank 0 merges the cluster's partials in rank order and writes the
+    // unit's output rows and log-sum-exp
+    if (p.attend) cluster_sync();   // every partial is written (and every kept count read)
+    if (p.attend && r == 0) {
+        constexpr int EPT = (G * D + 255) / 256;   // elements per merging thread (one head)
         const int e0 = tid * EPT;
         if (tid < 256 && e0 < G * D) {
             const int gg = e0 / D;
-            float mr[CL], M = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < CL; ++k) {
-                mr[k] = ld_dsmem_f32(part + G * D + gg, (uint32_t)k);
-                M = fmaxf(M, mr[k]);
-            }
+            float M = -INFINITY;
+#pragma unroll 1
+            for (int k = 0; k < C; ++k) M = fmaxf(M, ld_dsmem_f32(part + G * D + gg, (uint32_t)k));
             float Ls = 0.0f, A[EPT];
 #pragma unroll
             for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
             if (M != -INFINITY) {
-#pragma unroll
-                for (int k = 0; k < CL; ++k) {
-                    const float wgt = (mr[k] == -INFINITY) ? 0.0f : expf(mr[k] - M);
+#pragma unroll 1
+                for (int k = 0; k < C; ++k) {
+                    const float mk = ld_dsmem_f32(part + G * D + gg, (uint32_t)k);
+                    const float wgt = (mk == -INFINITY) ? 0.0f : expf(mk - M);
                     Ls = fmaf(ld_dsmem_f32(part + G * D + G + gg, (uint32_t)k), wgt, Ls);
 #pragma unroll
                     for (int e = 0; e < EPT; ++e) A[e] = fmaf(ld_dsmem_f32(part + e0 + e, (uint32_t)k), wgt, A[e]);
                 }
             }
-            if (ncl == 1) {
-                const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + gg;
+            const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + gg;
 #pragma unroll
-                for (int e = 0; e < EPT; ++e) {
-                    const int c = (e0 + e) % D;
-                    p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
-                    if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) cpart[e0 + e] = A[e];
-                if (e0 % D == 0) {
-                    cpart[G * D + gg] = M;
-                    cpart[G * D + G + gg] = Ls;
-                }
-            }
-        }
-        if (ncl > 1) {
-            __syncthreads();   // the cluster partial's writes, then one fence and the count
-            if (tid == 0) {
-                __threadfence();
-                misc[2] = (atomicAdd(&ws_ctrl(p)[u].k3_cdone, 1u) == (uint32_t)(ncl - 1)) ? 1u : 0u;
-            }
-            __syncthreads();
-            if (misc[2]) {
-                __threadfence();
-                merge_partials<G, D>(p, b, h, ws_part(p) + (size_t)u * kMaxSplit * PS, ncl);
+            for (int e = 0; e < EPT; ++e) {
+                const int c = (e0 + e) % D;
+                p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
+                if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
             }
         }
     }
-    cluster_sync();   // the cluster's shared memory stays until rank 0 has read it
-    SSA_MARK(9);
-    SSA_GT(7);
-}
-
-// ---------------------------------------------------------------------------
-// attend_kernel: CUDA cores (head_dim 64)
-// ---------------------------------------------------------------------------
-
-template <int G, int D>
-struct K3Cfg {
-    static constexpr int DPL = (G <= 4) ? 8 : 4;              // dims per lane (16 or 8 bytes)
-    static constexpr int LPR = D / DPL;                       // lanes per row
-    static constexpr int RPW = 32 / LPR;                      // rows per warp per step
-    static constexpr int RPS = k3Warps * RPW;                 // rows per CTA step
-    static constexpr int NS = 8;                              // steps in flight per warp
-    static constexpr uint32_t ROWB = D * 2u;
-    static constexpr uint32_t STAGE_W = (uint32_t)RPW * 2u * ROWB;    // K and V rows of one warp step
-    static constexpr uint32_t RING = (uint32_t)k3Warps * NS * STAGE_W;
-    static constexpr uint32_t MERGE = (uint32_t)k3Warps * G * D * 4u;
-    static constexpr uint32_t OFF_CHUNK = RING > MERGE ? RING : MERGE;
-    static constexpr int CHUNK = 1024;                        // list entries staged at a time
-    static constexpr uint32_t OFF_PRE = OFF_CHUNK + (uint32_t)CHUNK * 8u;
-    static_assert(OFF_CHUNK >= (uint32_t)CHUNK * 8u, "the raw chunk staging fits in front of the kept lists");
-};
-
-// Dynamic shared memory of attend_kernel for nlists per-tile lists.
-template <int G, int D>
-constexpr uint32_t k3_smem_bytes(int nlists)
-{
-    return K3Cfg<G, D>::OFF_PRE + (uint32_t)(nlists + 1) * 4u + 128u;
-}
-
-struct K3Shared {
-    uint32_t scan[k3Warps];
-    float wm[k3Warps][8], wl[k3Warps][8];
-    uint32_t is_last;
-};
-
-template <int G, int D>
-__global__ void __launch_bounds__(k3Threads) attend_kernel(const __grid_constant__ Params p)
-{
-    using CF = K3Cfg<G, D>;
-    constexpr int DPL = CF::DPL;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                                           ~static_cast<uintptr_t>(127));
-    __shared__ K3Shared ks;
-    int32_t* cidx = reinterpret_cast<int32_t*>(smem + CF::OFF_CHUNK);
-    float* clp = reinterpret_cast<float*>(smem + CF::OFF_CHUNK + CF::CHUNK * 4);
-    uint32_t* pre = reinterpret_cast<uint32_t*>(smem + CF::OFF_PRE);
-
-    const Plan& pl = p.pl;
-    const int P = pl.P;
-    const int u = blockIdx.x / P, r = blockIdx.x % P;
-    const int b = u / p.Hkv, h = u % p.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nlists = pl.ntile * kSelWarps;   // K2 writes one list per warp slice of a tile
-    SSA_GT(4);
-    grid_dep_wait();
-    SSA_MARK(7);
-    SSA_GT(5);
-
-    const int64_t total = list_total<k3Threads>(p, u, nlists, pre, ks.scan);
-    SSA_MARK(11);
-    const int64_t lo = total * r / P, hi = total * (r + 1) / P;
-    const uint16_t* Kb = p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
-    const uint16_t* Vb = p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
-    const UnitSel us = load_unit_sel(p, u);
-
-    const int sub = lane / CF::LPR, li = lane % CF::LPR;
-    float qv[G][DPL];
-    float mrun[G], lrun[G], acc[G][DPL];
-    if (p.attend) {
-        const uint16_t* qb = p.q + ((int64_t)b * p.Hq + (int64_t)h * G) * D + li * DPL;
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int c = 0; c < DPL; ++c) qv[g][c] = bf16_at(qb + (int64_t)g * D + c);
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        mrun[g] = -INFINITY;
-        lrun[g] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < DPL; ++c) acc[g][c] = 0.0f;
-    }
-    unsigned char* wring = smem + (size_t)warp * CF::NS * CF::STAGE_W + (size_t)sub * 2u * CF::ROWB + li * DPL * 2;
-    int64_t kept = 0;   // entries this CTA keeps
-
-#pragma unroll 1
-    for (int64_t c0 = lo; c0 < hi; c0 += CF::CHUNK) {
-        const int n = (int)min((int64_t)CF::CHUNK, hi - c0);
-        __syncthreads();   // the previous chunk is consumed
-        int32_t* ridx = reinterpret_cast<int32_t*>(smem);
-        float* rval = reinterpret_cast<float*>(smem + CF::CHUNK * 4);
-        const int nk = stage_decide<CF::CHUNK, k3Threads>(p, u, b, h, c0, n, lo + kept, pre, nlists, us, ridx, rval,
-                                                          cidx, clp, ks.scan);
-        kept += nk;
-        if (!p.attend) continue;
-        const int nsteps = (nk + CF::RPS - 1) / CF::RPS;
-        auto issue = [&](int step) {
-            const int row = step * CF::RPS + warp * CF::RPW + sub;
-            if (step < nsteps && row < nk) {
-                const int32_t j = cidx[row];
-                if (j >= 0) {
-                    unsigned char* dst = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
-                    if constexpr (DPL == 8) {
-                        cp_async_16(dst, Kb + (int64_t)j * D + li * DPL);
-                        cp_async_16(dst + CF::ROWB, Vb + (int64_t)j * D + li * DPL);
-                    } else {
-                        cp_async_8(dst, Kb + (int64_t)j * D + li * DPL);
-                        cp_async_8(dst + CF::ROWB, Vb + (int64_t)j * D + li * DPL);
-                    }
-                }
-            }
-            cp_async_commit();
-        };
-#pragma unroll
-        for (int s = 0; s < CF::NS - 1; ++s) issue(s);
-#pragma unroll 1
-        for (int step = 0; step < nsteps; ++step) {
-            issue(step + CF::NS - 1);
-            cp_async_wait<CF::NS - 1>();
-            const int row = step * CF::RPS + warp * CF::RPW + sub;
-            const bool valid = row < nk;
-            const float lp = valid ? clp[row] : 0.0f;
-            const unsigned char* src = wring + (size_t)(step % CF::NS) * CF::STAGE_W;
-            float kf[DPL], vf[DPL];
-            if constexpr (DPL == 8) {
-                const uint4 kw = *reinterpret_cast<const uint4*>(src);
-                const uint4 vw = *reinterpret_cast<const uint4*>(src + CF::ROWB);
-                const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w}, va[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    kf[2 * i] = bf16_lo(ka[i]);
-                    kf[2 * i + 1] = bf16_hi(ka[i]);
-                    vf[2 * i] = bf16_lo(va[i]);
-                    vf[2 * i + 1] = bf16_hi(va[i]);
-                }
-            } else {
-                const uint2 kw = *reinterpret_cast<const uint2*>(src);
-                const uint2 vw = *reinterpret_cast<const uint2*>(src + CF::ROWB);
-                kf[0] = bf16_lo(kw.x); kf[1] = bf16_hi(kw.x); kf[2] = bf16_lo(kw.y); kf[3] = bf16_hi(kw.y);
-                vf[0] = bf16_lo(vw.x); vf[1] = bf16_hi(vw.x); vf[2] = bf16_lo(vw.y); vf[3] = bf16_hi(vw.y);
-            }
-            float dot[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float sacc = 0.0f;
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) sacc = fmaf(qv[g][c], kf[c], sacc);
-                dot[g] = sacc;
-            }
-#pragma unroll
-            for (int o = CF::LPR / 2; o > 0; o >>= 1)
-#pragma unroll
-                for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], o);
-            if (valid) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float x = dot[g] * p.scale - lp;
-                    if (x > mrun[g]) {
-                        const float a = expf(mrun[g] - x);
-                        lrun[g] *= a;
-#pragma unroll
-                        for (int c = 0; c < DPL; ++c) acc[g][c] *= a;
-                        mrun[g] = x;
-                    }
-                    const float w = expf(x - mrun[g]);
-                    lrun[g] += w;
-#pragma unroll
-                    for (int c = 0; c < DPL; ++c) acc[g][c] = fmaf(w, vf[c], acc[g][c]);
-                }
-            }
-        }
-        cp_async_wait<0>();
-    }
-    SSA_MARK(8);
-
-    float* part = ws_part(p) + ((size_t)u * P + r) * (size_t)(G * D + 2 * G);
-    if (p.attend) {
-        // merge the row streams of a warp (lanes li, li + LPR, ...)
-#pragma unroll
-        for (int o = CF::LPR; o < 32; o <<= 1) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float mo = __shfl_xor_sync(0xffffffffu, mrun[g], o);
-                const float lo_ = __shfl_xor_sync(0xffffffffu, lrun[g], o);
-                const float M = fmaxf(mrun[g], mo);
-                const float a = (mrun[g] == -INFINITY) ? 0.0f : expf(mrun[g] - M);
-                const float ao = (mo == -INFINITY) ? 0.0f : expf(mo - M);
-                lrun[g] = lrun[g] * a + lo_ * ao;
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) {
-                    const float xo = __shfl_xor_sync(0xffffffffu, acc[g][c], o);
-                    acc[g][c] = acc[g][c] * a + xo * ao;
-                }
-                mrun[g] = M;
-            }
-        }
-        __syncthreads();   // the ring is reused for the warp partials
-        float* wpart = reinterpret_cast<float*>(smem);   // [k3Warps][G][D]
-        if (lane < CF::LPR) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) wpart[((size_t)warp * G + g) * D + li * DPL + c] = acc[g][c];
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                ks.wm[warp][g] = mrun[g];
-                ks.wl[warp][g] = lrun[g];
-            }
-        }
-        __syncthreads();
-#pragma unroll 1
-        for (int i = tid; i < G * D; i += k3Threads) {
-            const int g = i / D, c = i % D;
-            float M = -INFINITY;
-            for (int w = 0; w < k3Warps; ++w) M = fmaxf(M, ks.wm[w][g]);
-            float A = 0.0f, Ls = 0.0f;
-            if (M != -INFINITY) {
-                for (int w = 0; w < k3Warps; ++w) {
-                    const float mw = ks.wm[w][g];
-                    if (mw == -INFINITY) continue;
-                    const float e = expf(mw - M);
-                    A = fmaf(wpart[((size_t)w * G + g) * D + c], e, A);
-                    Ls = fmaf(ks.wl[w][g], e, Ls);
-                }
-            }
-            part[i] = A;
-            if (c == 0) {
-                part[G * D + g] = M;
-                part[G * D + G + g] = Ls;
-            }
-        }
-    }
-    __syncthreads();
-    const bool last = finish_lists<k3Threads>(p, u, P, r, kept, total, reinterpret_cast<uint32_t*>(smem), &ks.is_last);
-    SSA_MARK(12);
-    SSA_GT(6);
-    if (!last || !p.attend) return;
-    SSA_MARK(14);
-    merge_partials<G, D>(p, b, h, ws_part(p) + (size_t)u * P * (size_t)(G * D + 2 * G), P);
+    cluster_sync();   // a CTA's shared memory stays until every remote read of it is done
     SSA_MARK(9);
     SSA_GT(7);
 }

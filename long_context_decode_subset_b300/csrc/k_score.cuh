@@ -44,8 +44,8 @@ struct Params {
     Plan pl;
     int32_t Bt, Hq, Hkv, d, d_sel;
     int32_t dense;             // every token selected with p = 1 (top_k >= N or budget = +inf)
-    int32_t attend;            // K3 computes attention (else it only writes the compact list)
-    int32_t src_mode;          // K3 rows: 0 per-tile lists, 1 all tokens, 2 the caller's compact list
+    int32_t attend;            // K2 computes attention (else it only writes the compact list)
+    int32_t src_mode;          // K2 rows: 0 the selection, 1 all tokens, 2 the caller's compact list
     const uint16_t* q;         // [Bt][Hq][d]
     const uint16_t* K;         // [Bt][Hkv][N][d] with the strides below
     const uint16_t* V;
@@ -57,8 +57,8 @@ struct Params {
     uint64_t seed;
     char* ws;                  // workspace base
     float* s_dst;              // K1 writes the scores here ([U][N])
-    const float* s_src;        // K2a / K2c read the scores here ([U][N])
-    const int32_t* idx_in;     // K3 source 2: [U][cap] / count [U]
+    const float* s_src;        // K2 reads the scores here ([U][N])
+    const int32_t* idx_in;     // K2 source 2: [U][cap] / count [U]
     const float* p_in;
     const int32_t* count_in;
     int32_t* idx_out;          // compact list out (may be null): [U][cap] / count [U]
@@ -84,13 +84,10 @@ __device__ __forceinline__ uint32_t* ws_hist1(const Params& p) { return reinterp
 // level-2 histogram (the next 12 key bits of the threshold bucket's members), [U][kBins]
 __device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return ws_hist1(p) + (size_t)p.pl.U * kBins; }
 __device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
-__device__ __forceinline__ uint32_t* ws_kept(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_kept); }
-__device__ __forceinline__ uint32_t* ws_scount(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_scount); }
 __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
 __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
-__device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
 
 // ---------------------------------------------------------------------------
 // K0: zero the unit's control block and histograms.  One CTA per unit.  It
@@ -596,7 +593,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
 
 // K1 for ssa_select (scores given): per-unit histogram of the top 12 key bits
 // and the 16-bit Philox prefixes.  One CTA per (unit, tile).
-__global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kInThreads) score_input_kernel(const __grid_constant__ Params p)
 {
     __shared__ uint32_t hist[kBins];
     const Plan& pl = p.pl;
@@ -607,10 +604,10 @@ __global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_con
     const int b = u / p.Hkv, h = u % p.Hkv;
     const uint32_t k0 = (uint32_t)(p.seed & 0xffffffffu), k1 = (uint32_t)(p.seed >> 32);
     uint32_t* status = ws_status(p);
-    for (int i = tid; i < kBins; i += k3Threads) hist[i] = 0u;
+    for (int i = tid; i < kBins; i += kInThreads) hist[i] = 0u;
     __syncthreads();
     grid_dep_wait();
-    for (int i = tid; i < n; i += k3Threads) {
+    for (int i = tid; i < n; i += kInThreads) {
         const int64_t t = t0 + i;
         const float s = p.s_src[(int64_t)u * pl.N + t];
         if (!isfinite(s)) flag(status, DEV_NONFINITE);
@@ -620,7 +617,7 @@ __global__ void __launch_bounds__(k3Threads) score_input_kernel(const __grid_con
     }
     __syncthreads();
     uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
-    for (int i = tid; i < kBins; i += k3Threads)
+    for (int i = tid; i < kBins; i += kInThreads)
         if (hist[i]) atomicAdd(hist1 + i, hist[i]);
     grid_dep_launch();
 }

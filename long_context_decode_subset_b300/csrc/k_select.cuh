@@ -12,9 +12,10 @@
 //   p is independent of m; m is the lower edge of the 12-bit order-key
 //   bucket f that holds the k-th score (the largest when k = 0).
 //
-// One CTA of 512 threads per (unit, tile); each of its 16 warps owns a
-// contiguous slice of the tile (tile / 16 tokens: 512 at 128K, 2048 at 1M),
-// staged through shared memory, and walks it in index order:
+// Selection pass of the unit kernel (K2): one CTA of 512 threads per (unit,
+// tile), the unit's tiles forming a thread-block cluster; each of its 16
+// warps owns a contiguous slice of the tile (tile / 16 tokens), staged
+// through shared memory, and walks it in index order:
 //   * a token above bucket f is in T: it joins the slice's list (p = 1);
 //   * a token of bucket f is a candidate: it joins the slice's list (with
 //     its score) and the unit's candidate array (for the exact k-th);
@@ -24,15 +25,14 @@
 //     of Z read off the histogram (every term of bucket c is at least
 //     exp(floor_c - m)), and u is at least its 16-bit prefix (drawn by the
 //     score kernel), so prefix >= B e / Z_lb rules it out for good.
-// The last tile of a unit to finish (a counter in the unit's control block)
-// resolves the exact k-th token among the candidates -- in shared memory:
-// a 12-bit histogram, then the few members sharing 24 key bits ranked
-// exactly (key desc, index asc) -- and completes Z: the tiles' shares in
-// tile order plus the remainder candidates' terms, summed exactly as 128-bit
-// integers (every such term is an fp32 value of at least one; terms of
-// 2^81 and more, i.e. scores more than 450 apart from m, are flagged as
-// out of range).  The
-// attention kernel makes the final decision for every listed token.
+// After a cluster barrier, rank 0 resolves the exact k-th token among the
+// candidates -- in shared memory: a 12-bit histogram, then the few members
+// sharing 24 key bits ranked exactly (key desc, index asc) -- and completes
+// Z: the tiles' shares in tile order plus the remainder candidates' terms,
+// summed exactly as 128-bit integers (every such term is an fp32 value of at
+// least one; terms of 2^81 and more, i.e. scores more than 450 apart from m,
+// are flagged as out of range).  Every CTA then makes the final decision for
+// its own listed tokens (k_attend.cuh).
 #pragma once
 #include "k_score.cuh"
 
@@ -53,6 +53,7 @@ struct SelShared {
     uint2 bound[256];
     unsigned long long zi[kSelWarps][2];
     uint32_t coff[kMaxTiles + 1];   // per-tile candidate offsets
+    uint32_t wcnt[kSelWarps];       // the tile pass: list length of each warp slice
 };
 
 // What each (unit, tile) CTA leaves for the resolve: its share of Z
@@ -65,10 +66,8 @@ struct TilePart {
 
 constexpr int kSlice = 512;           // tokens a warp stages at a time
 constexpr int kResStage = kSelWarps * kSlice * 6 / 8;   // candidates the resolve stages at a time (same memory)
+static_assert(kResStage * 8 <= kSelWarps * kSlice * 6, "the resolve's staging fits the pass's");
 
-// Dynamic shared memory of K2: the warps' staged chunks (scores and Philox
-// prefixes).
-inline uint32_t k2_smem_bytes() { return (uint32_t)kSelWarps * kSlice * 6u; }
 
 __device__ __forceinline__ void zacc(float& zh, float& zl, float v)
 {
@@ -394,26 +393,28 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
 }
 
 // ---------------------------------------------------------------------------
-// K2: per (unit, tile)
+// The selection pass of one (unit, tile): block-wide, kSelThreads threads.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_constant__ Params p)
+// What the pass leaves for the resolve (rank 0): the bucket of the k-th
+// score, the number of tokens above it, the rank sought and the reference
+// point m.
+struct TileSel {
+    uint32_t f1, above1, target;
+    float m;
+};
+
+// Dynamic shared memory the pass stages its warps' chunks in (scores and
+// Philox prefixes); the resolve stages candidates in the same bytes.
+constexpr uint32_t kSelStageBytes = (uint32_t)kSelWarps * kSlice * 6u;
+
+__device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelShared& sh, unsigned char* k2dyn)
 {
-    extern __shared__ __align__(16) unsigned char k2dyn[];
-    __shared__ SelShared sh;
     const Plan& pl = p.pl;
-    const int u = blockIdx.x / pl.ntile, tile = blockIdx.x % pl.ntile;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W2 = pl.tt / kSelWarps;
     uint32_t* status = ws_status(p);
-    SSA_MARK(20);
-    SSA_GT(1);
-    grid_dep_wait();
-    // the attention kernel may be scheduled now: its CTAs take SMs as this
-    // grid's CTAs leave, set up, and wait for this grid to complete
-    grid_dep_launch();
     SSA_MARK(2);
-    SSA_GT(2);
 
     const int64_t base = (int64_t)tile * pl.tt + (int64_t)warp * W2;   // this warp's first token
     const float* S = p.s_src + (int64_t)u * pl.N;
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         }
         cp_async_commit();
     };
-    stage(0);
+    stage(0);   // the caller runs the pass only when N > 0
 
     // bucket f1 of the k-th score (the largest when k = 0): each thread reads
     // 8 bins of the unit's histogram, top bin first
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
     SSA_MARK(18);
     float zh = zq[0][0], zl = zq[0][1];
     comp_add(zh, zl, zq[1][0], zq[1][1]);
-    if (lane == 0) ws_scount(p)[((size_t)u * pl.ntile + tile) * kSelWarps + warp] = cnt;
+    if (lane == 0) sh.wcnt[warp] = cnt;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float h2 = __shfl_xor_sync(0xffffffffu, zh, o);
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
         sh.zw[warp][0] = zh;
         sh.zw[warp][1] = zl;
     }
-    __syncthreads();   // the CTA's list and candidate writes; one fence below covers them (cumulative)
+    __syncthreads();   // the CTA's list and candidate writes; the caller's fence covers them (cumulative)
     SSA_MARK(19);
     if (warp == 0) {   // the warps' shares, a fixed tree over 16 lanes
         float hh = lane < kSelWarps ? sh.zw[lane][0] : 0.0f, ll = lane < kSelWarps ? sh.zw[lane][1] : 0.0f;
@@ -593,20 +594,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) bucket_kernel(const __grid_con
             tpo.ncand = sh.ncand_cta;
             tpo.pad = 0;
             reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.ntile + tile] = tpo;
-            __threadfence();
-            const uint32_t prev = atomicAdd(&ws_ctrl(p)[u].k2a_done, 1u);
-            sh.is_last = (prev == (uint32_t)(pl.ntile - 1)) ? 1u : 0u;
         }
     }
-    __syncthreads();
-    SSA_MARK(10);
-    if (sh.is_last) {
-        __threadfence();
-        SSA_MARK(3);
-        resolve_unit(p, u, f1.bin, f1.above, target, m, sh, reinterpret_cast<uint2*>(k2dyn));
-        SSA_MARK(4);
-    }
-    SSA_GT(3);
+    return TileSel{f1.bin, f1.above, target, m};
 }
 
 }  // namespace ssa

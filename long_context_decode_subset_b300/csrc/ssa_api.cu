@@ -41,12 +41,19 @@ int device_sms()
     return n > 0 ? n : 148;
 }
 
-// Plan and workspace layout.  The layout does not depend on the device; the
-// K1 grid and the K3 split do (the workspace is sized for the largest split).
-// SSA_FORCE_TILE / SSA_FORCE_SPLIT override the tile size and the split (the
-// tests use them to cover many tiles and splits on small inputs), and
-// SSA_FORCE_HIST_RUN the score kernel's histogram hand-over period.
-ssa::Plan make_plan(const ssa_shape& s, bool with_device)
+// Plan and workspace layout.  The layout does not depend on the device: the
+// per-unit token arrays are sized for the largest tiling (at most kMaxTiles
+// tiles of 512-token multiples pad a unit by less than kMaxTiles * 512
+// tokens).  The tiling itself -- the unit kernel's cluster size -- and the
+// score kernel's grid do depend on the device; `tiles` > 0 gives the tile
+// count (the tiles are then the fewest 512-token multiples that cover N in
+// that many pieces).  SSA_FORCE_TILE (tokens per tile) and SSA_FORCE_SPLIT
+// (tiles per unit) override the choice (the tests use them to cover many
+// tilings on small inputs), and SSA_FORCE_HIST_RUN the score kernel's
+// histogram hand-over period.
+constexpr int64_t kPadTokens = (int64_t)kMaxTiles * kTileAlign;
+
+ssa::Plan make_plan(const ssa_shape& s, int tiles)
 {
     ssa::Plan pl{};
     pl.U = s.batch * s.n_kv_heads;
@@ -56,22 +63,19 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.nst = (int32_t)((N + kStageTok - 1) / kStageTok);
     pl.stages = U * pl.nst;
     pl.sf = (int32_t)((int64_t)pl.nst * 3 / 4);   // the rest of each unit goes to K1's shared queue
-    const int sms = with_device ? device_sms() : 148;
+    const int sms = tiles > 0 ? device_sms() : 148;
     pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
-    // K2 tiles: about kSelSlots CTAs in all (two per SM on 128 SMs; filling
-    // all 148 measured slower, its last CTAs finishing later; the workspace
-    // layout must not depend on the device), 512-token multiples
-    const int64_t want = std::max<int64_t>(1, kSelSlots / std::max<int64_t>(U, 1));
-    int64_t tt = std::max<int64_t>(1, (N + want - 1) / want);
-    tt = std::max<int64_t>(kTileAlign, (tt + kTileAlign - 1) / kTileAlign * kTileAlign);
-    if ((N + tt - 1) / tt > kMaxTiles) tt = ((N + kMaxTiles - 1) / kMaxTiles + kTileAlign - 1) / kTileAlign * kTileAlign;
+    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, (N + kTileAlign - 1) / kTileAlign));
+    int64_t c = std::max<int64_t>(1, std::min<int64_t>(tiles > 0 ? tiles : 1, cmax));
+    int64_t tt = std::max<int64_t>(kTileAlign, ((N + c - 1) / c + kTileAlign - 1) / kTileAlign * kTileAlign);
     const int forced_tile = env_int("SSA_FORCE_TILE", 0);
-    if (forced_tile >= 512 && forced_tile % 512 == 0 && (N + forced_tile - 1) / forced_tile <= kMaxTiles)
+    if (tiles > 0 && forced_tile >= kTileAlign && forced_tile % kTileAlign == 0 &&
+        (N + forced_tile - 1) / forced_tile <= kMaxTiles &&
+        (N + forced_tile - 1) / forced_tile * forced_tile < N + kPadTokens)   // within the sized padding
         tt = forced_tile;
     pl.tt = (int32_t)tt;
-    pl.ntile = (int32_t)((N + tt - 1) / tt);
+    pl.ntile = (int32_t)std::max<int64_t>(1, (N + tt - 1) / tt);
     pl.np = (int64_t)pl.ntile * tt;
-    pl.P = 1;   // set at launch (attend_split)
     // K1's histogram buffers are handed over after at most kHistRun stages of
     // one unit; SSA_FORCE_HIST_RUN lowers that (the tests use it to hand
     // buffers over at every stage or two)
@@ -79,9 +83,9 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     const int forced_run = env_int("SSA_FORCE_HIST_RUN", 0);
     if (forced_run >= 1 && forced_run <= kHistRun) pl.hist_run = forced_run;
 
-    const int64_t G = pl.G, D = s.head_dim;
+    const int64_t D = s.head_dim;
     const int64_t heads = (int64_t)s.batch * s.n_q_heads;
-    const int64_t nl = (int64_t)pl.ntile * kSelWarps;
+    const int64_t npmax = N + kPadTokens;
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -91,15 +95,12 @@ ssa::Plan make_plan(const ssa_shape& s, bool with_device)
     pl.o_status = take(kStatusBytes);
     pl.o_ctrl = take((size_t)U * sizeof(UnitCtrl));
     pl.o_hist1 = take((size_t)U * kBins * 4 * 2);   // level-1 then level-2 histograms
-    pl.o_zpart = take((size_t)U * pl.ntile * 16);
-    pl.o_scount = take((size_t)U * nl * 4);
-    pl.o_kept = take((size_t)U * kMaxSplit * 4);
+    pl.o_zpart = take((size_t)U * kMaxTiles * 16);
     pl.o_cand = take((size_t)U * N * 8);
-    pl.o_sel_idx = take((size_t)U * pl.np * 4);
-    pl.o_sel_p = take((size_t)U * pl.np * 4);
+    pl.o_sel_idx = take((size_t)U * npmax * 4);
+    pl.o_sel_p = take((size_t)U * npmax * 4);
     pl.o_scores = take((size_t)U * N * 4);
-    pl.o_ubuf = take((size_t)U * pl.np * 2);
-    pl.o_part = take((size_t)U * kMaxSplit * (size_t)(G * D + 2 * G) * 4);
+    pl.o_ubuf = take((size_t)U * npmax * 2);
     pl.o_hq = take((size_t)heads * D * 2);
     pl.o_hout = take((size_t)heads * D * 4);
     pl.o_hlse = take((size_t)heads * 4);
@@ -117,7 +118,7 @@ ssa_status check_shape(const ssa_shape* s)
     if (s->head_dim != 64 && s->head_dim != 128) return SSA_ERR_UNSUPPORTED;
     if (s->d_sel != 16 && s->d_sel != 32) return SSA_ERR_UNSUPPORTED;
     if (s->ctx_len < 0 || s->ctx_len > (int64_t)INT32_MAX - 4096) return SSA_ERR_INVALID_ARG;
-    if ((int64_t)s->batch * s->n_kv_heads > (int64_t)INT32_MAX / (kMaxSplit * 2)) return SSA_ERR_UNSUPPORTED;
+    if ((int64_t)s->batch * s->n_kv_heads > (int64_t)INT32_MAX / (kMaxTiles * 2)) return SSA_ERR_UNSUPPORTED;
     const int64_t N = s->ctx_len;
     if (s->kv_stride_h < N * s->head_dim || s->ks_stride_h < N * s->d_sel) return SSA_ERR_INVALID_ARG;
     if (s->kv_stride_b < (int64_t)(s->n_kv_heads - 1) * s->kv_stride_h + N * s->head_dim) return SSA_ERR_INVALID_ARG;
@@ -192,30 +193,24 @@ kfn_t pick_score(int G, int dsel, bool hist)
 }
 
 template <int G>
-kfn_t att_fn(int d, uint32_t* smem, int nlists, bool* tc)
+kfn_t unit_fn(int d, uint32_t* smem)
 {
-    *tc = (d == 128);
-    if (d == 128) {   // the larger list staging when it fits
-        if (ktc_smem_bytes<G, 4096>(nlists) <= 227u * 1024u) {
-            *smem = ktc_smem_bytes<G, 4096>(nlists);
-            return &attend_tc_kernel<G, 4096>;
-        }
-        *smem = ktc_smem_bytes<G, 1024>(nlists);
-        return &attend_tc_kernel<G, 1024>;
+    if (d == 128) {
+        *smem = unit_smem_bytes<G, 128, 4096>();
+        return &unit_kernel<G, 128, 4096>;
     }
-    *smem = k3_smem_bytes<G, 64>(nlists);
-    return &attend_kernel<G, 64>;
+    *smem = unit_smem_bytes<G, 64, 4096>();
+    return &unit_kernel<G, 64, 4096>;
 }
 
-// K3 for this shape: the tensor-core kernel (clusters of kClusterCtas) at
-// head_dim 128, the CUDA-core kernel at 64.
-kfn_t pick_attend(int G, int d, uint32_t* smem, int nlists, bool* tc)
+// The unit kernel for this group size and head_dim, and its dynamic shared memory.
+kfn_t pick_unit(int G, int d, uint32_t* smem)
 {
     switch (G) {
-        case 1: return att_fn<1>(d, smem, nlists, tc);
-        case 2: return att_fn<2>(d, smem, nlists, tc);
-        case 4: return att_fn<4>(d, smem, nlists, tc);
-        default: return att_fn<8>(d, smem, nlists, tc);
+        case 1: return unit_fn<1>(d, smem);
+        case 2: return unit_fn<2>(d, smem);
+        case 4: return unit_fn<4>(d, smem);
+        default: return unit_fn<8>(d, smem);
     }
 }
 
@@ -247,9 +242,11 @@ bool allow_dynamic_smem(kfn_t fn, uint32_t smem)
 
 // Launch `fn` on `stream`.  Every kernel of a step after the first is a
 // programmatic dependent launch: it may start while its predecessor drains
-// and waits (griddepcontrol.wait) before reading its results.
+// and waits (griddepcontrol.wait) before reading its results.  The first
+// kernel of a step is an ordinary launch: it starts after everything before
+// it on the stream (the caller's writes of the query, say) has completed.
 ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::Params& prm, cudaStream_t stream,
-                  bool dependent, int cluster = 1)
+                  bool dependent, int cluster = 0)
 {
     if (grid <= 0) return SSA_OK;
     if (grid > INT32_MAX) return SSA_ERR_UNSUPPORTED;
@@ -266,7 +263,7 @@ ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::P
         at[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
-    if (cluster > 1) {
+    if (cluster > 0) {   // a thread-block cluster launch (a cluster of one CTA included)
         at[na].id = cudaLaunchAttributeClusterDimension;
         at[na].val.clusterDim.x = (unsigned)cluster;
         at[na].val.clusterDim.y = 1;
@@ -310,41 +307,38 @@ ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cud
     return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1_threads(hist), smem, p, stream, dependent);
 }
 
-ssa_status launch_select(const ssa::Params& p, cudaStream_t stream)
-{
-    return launch(&bucket_kernel, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, k2_smem_bytes(), p, stream, true);
-}
-
-// CTAs of `fn` resident per SM (cached per kernel and shared-memory size).
-int blocks_per_sm(kfn_t fn, int block, uint32_t smem)
+// Clusters of more than 8 CTAs are allowed for `fn` (once per kernel, per device).
+bool allow_big_clusters(kfn_t fn)
 {
     static std::mutex mu;
-    static std::map<std::pair<void*, uint32_t>, int> cache;
-    const auto key = std::make_pair((void*)fn, smem);
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    int n = 0;
-    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)fn, block, smem) != cudaSuccess) {
+    static std::map<std::pair<void*, int>, bool> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
-        n = 1;
+        return false;
     }
-    n = std::max(n, 1);
+    const auto key = std::make_pair((void*)fn, dev);
     std::lock_guard<std::mutex> lk(mu);
-    cache[key] = n;
-    return n;
+    if (done.count(key)) return done[key];
+    const bool ok = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    done[key] = ok;
+    return ok;
 }
 
 // Clusters of `cl` CTAs of `fn` (`threads` threads, `smem` bytes) resident
-// on the device at once (cached per kernel and size).
+// on the device at once (cached per kernel, cluster size and device; 0 if
+// the size cannot be launched).
 int64_t active_clusters(kfn_t fn, int cl, int threads, uint32_t smem)
 {
     static std::mutex mu;
-    static std::map<std::pair<void*, uint32_t>, int64_t> cache;
-    const auto key = std::make_pair((void*)fn, smem);
+    static std::map<std::tuple<void*, int, int>, int64_t> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const auto key = std::make_tuple((void*)fn, cl, dev);
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -362,48 +356,40 @@ int64_t active_clusters(kfn_t fn, int cl, int threads, uint32_t smem)
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) || cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
+    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) || (cl > 8 && !allow_big_clusters(fn)) ||
+        cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
         cudaGetLastError();
-        n = 1;
+        n = 0;
     }
-    const int64_t v = std::max(n, 1);
     std::lock_guard<std::mutex> lk(mu);
-    cache[key] = v;
-    return v;
+    cache[key] = n;
+    return n;
 }
 
-// K3's split: P CTAs per unit (at most kMaxSplit): as many as fit in one
-// wave with every unit getting the same number (for the tensor-core kernel
-// a whole number of clusters), unless SSA_FORCE_SPLIT says otherwise
-// (rounded up to whole clusters).
-int attend_split(const ssa::Plan& pl, const ssa_shape& s)
+// Tiles per unit, i.e. the unit kernel's cluster size: SSA_FORCE_SPLIT if
+// set, else the largest c <= kMaxTiles for which the clusters of every unit
+// are resident at once (one wave; the plan also caps c at the 512-token
+// pieces of the context).
+int unit_tiles(const ssa_shape& s)
 {
-    uint32_t smem = 0;
-    bool tc = false;
     const int forced = env_int("SSA_FORCE_SPLIT", 0);
-    const int64_t U = std::max<int64_t>(pl.U, 1);
-    kfn_t fn = pick_attend(pl.G, s.head_dim, &smem, pl.ntile * kSelWarps, &tc);
-    if (tc) {
-        int64_t ncl = forced > 0 ? (forced + kClusterCtas - 1) / kClusterCtas
-                                 : active_clusters(fn, kClusterCtas, kTcThreads, smem) / U;
-        ncl = std::max<int64_t>(1, std::min<int64_t>(ncl, kMaxSplit / kClusterCtas));
-        return (int)ncl * kClusterCtas;
-    }
-    if (forced > 0) return std::min(forced, kMaxSplit);
-    const int64_t slots = (int64_t)blocks_per_sm(fn, k3Threads, smem) * device_sms();
-    return (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, slots / U));
+    if (forced > 0) return std::min(forced, kMaxTiles);
+    const int64_t U = std::max<int64_t>(1, (int64_t)s.batch * s.n_kv_heads);
+    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, (s.ctx_len + kTileAlign - 1) / kTileAlign));
+    uint32_t smem = 0;
+    kfn_t fn = pick_unit(s.n_q_heads / s.n_kv_heads, s.head_dim, &smem);
+    for (int64_t c = cmax; c >= 2; --c)
+        if (active_clusters(fn, (int)c, kSelThreads, smem) >= U) return (int)c;
+    return 1;
 }
 
-ssa_status launch_attend(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream)
+ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream, bool dependent)
 {
     uint32_t smem = 0;
-    bool tc = false;
-    kfn_t fn = pick_attend(p.pl.G, s.head_dim, &smem, p.pl.ntile * kSelWarps, &tc);
+    kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
-    ssa::Params q = p;
-    q.pl.P = attend_split(p.pl, s);
-    return launch(fn, (int64_t)q.pl.U * q.pl.P, tc ? kTcThreads : k3Threads, smem, q, stream, true,
-                  tc ? kClusterCtas : 1);
+    if (p.pl.ntile > 8 && !allow_big_clusters(fn)) return SSA_ERR_CUDA;
+    return launch(fn, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, smem, p, stream, dependent, p.pl.ntile);
 }
 
 }  // namespace
@@ -495,7 +481,7 @@ size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap)
 {
     (void)list_cap;
     if (check_shape(shape) != SSA_OK) return 0;
-    return make_plan(*shape, false).total;
+    return make_plan(*shape, 0).total;
 }
 
 size_t ssa_select_capacity(const ssa_shape* shape)
@@ -510,7 +496,7 @@ ssa_status ssa_pack_summary(const ssa_bf16* K, const int32_t* sel_ch, ssa_bf16* 
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!K || !sel_ch || !Ks) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, false);
+    const ssa::Plan pl = make_plan(*shape, 0);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     const int64_t total = (int64_t)shape->batch * shape->n_kv_heads * shape->ctx_len * shape->d_sel;
     if (total == 0) return SSA_OK;
@@ -534,7 +520,7 @@ ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_c
     if (!q || !Ks || !sel_ch || !s_hat) return SSA_ERR_INVALID_ARG;
     if (!aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, true);
+    const ssa::Plan pl = make_plan(*shape, 1);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (shape->ctx_len == 0 || pl.U == 0) return SSA_OK;
     ssa::Params p = base_params(*shape, pl, ws);
@@ -555,7 +541,7 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
     if (st != SSA_OK) return st;
     if (!s_hat || !idx || !p || !count) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, true);
+    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
@@ -570,13 +556,13 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
     prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
     prm.src_mode = prm.dense ? 1 : 0;
     prm.attend = 0;
+    if (prm.dense) return launch_unit(prm, *shape, stream, false);   // every token, p = 1
+    // K0 zeroes the histograms, the input kernel counts the scores and draws
+    // the Philox prefixes, the unit kernel selects
     if ((st = launch_init(prm, stream)) != SSA_OK) return st;
-    if (!prm.dense) {
-        if ((st = launch(&score_input_kernel, (int64_t)pl.U * pl.ntile, k3Threads, 0, prm, stream, true)) != SSA_OK)
-            return st;
-        if ((st = launch_select(prm, stream)) != SSA_OK) return st;
-    }
-    return launch_attend(prm, *shape, stream);
+    if ((st = launch(&score_input_kernel, (int64_t)pl.U * pl.ntile, kInThreads, 0, prm, stream, true)) != SSA_OK)
+        return st;
+    return launch_unit(prm, *shape, stream, true);
 }
 
 ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const int32_t* idx, const float* p,
@@ -586,9 +572,9 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!q || !idx || !p || !count || !out || !lse || (shape->ctx_len > 0 && (!K || !V))) return SSA_ERR_INVALID_ARG;
-    if (!aligned(K, 16) || !aligned(V, 16)) return SSA_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, true);
+    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
@@ -604,9 +590,7 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     prm.lse = lse;
     prm.src_mode = 2;
     prm.attend = 1;
-    // K0 zeroes the merge counters (sel_ch is not given, so no query operand is built)
-    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
-    return launch_attend(prm, *shape, stream);
+    return launch_unit(prm, *shape, stream, false);   // one kernel: nothing to zero first
 }
 
 }  // extern "C"
@@ -647,7 +631,7 @@ ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16*
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget) || bad_scale(scale)) return SSA_ERR_INVALID_ARG;
     if ((idx_opt == nullptr) != (p_opt == nullptr)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, true);
+    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     char* w = static_cast<char*>(ws);
@@ -681,12 +665,14 @@ ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16*
         if (pl.sf >= pl.nst) return SSA_ERR_UNSUPPORTED;
         set_append(prm, *app, shape->ctx_len - 1, *shape);
     }
-    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
-    if (!empty && (!prm.dense || s_hat_opt)) {
-        if ((st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
-        if (!prm.dense && (st = launch_select(prm, stream)) != SSA_OK) return st;
-    }
-    return launch_attend(prm, *shape, stream);
+    // K0 zeroes the score kernel's queue and the histograms (and writes the
+    // appended token); a step that keeps every token and wants no scores
+    // runs the unit kernel alone
+    const bool score = !empty && (!prm.dense || s_hat_opt);
+    const bool init = score || app;
+    if (init && (st = launch_init(prm, stream)) != SSA_OK) return st;
+    if (score && (st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
+    return launch_unit(prm, *shape, stream, init);
 }
 
 }  // namespace
@@ -725,7 +711,7 @@ ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_
     if (!k_new || !v_new || !sel_ch || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
     if (pos < 0 || pos >= shape->ctx_len) return SSA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(K, 16) || !aligned(V, 16)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, false);
+    const ssa::Plan pl = make_plan(*shape, 0);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
@@ -742,7 +728,7 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!q_host || !out_host || !lse_host) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, false);
+    const ssa::Plan pl = make_plan(*shape, 0);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     char* w = static_cast<char*>(ws);
     const size_t heads = (size_t)shape->batch * shape->n_q_heads;
@@ -772,7 +758,7 @@ ssa_status ssa_decode_static(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
 {
     const ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    const ssa::Plan pl = make_plan(*shape, false);
+    const ssa::Plan pl = make_plan(*shape, 0);
     if (pl.total > (size_t)SSA_STATIC_SCRATCH_BYTES) return SSA_ERR_WORKSPACE;
     void* ws = static_scratch_address();
     if (!ws) return SSA_ERR_CUDA;
@@ -815,10 +801,10 @@ ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* 
 {
     const ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    const ssa::Plan pl = make_plan(*shape, true);
+    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
     if (score_ctas) *score_ctas = pl.k1_grid;
     if (tiles_per_unit) *tiles_per_unit = pl.ntile;
-    if (attend_ctas_per_unit) *attend_ctas_per_unit = attend_split(pl, *shape);
+    if (attend_ctas_per_unit) *attend_ctas_per_unit = pl.ntile;
     return SSA_OK;
 }
 
