@@ -8,16 +8,18 @@
 //               once and waits for K0 only before its first histogram flush);
 //   K1 score    every SM streams the key summary (TMA) and scores it on the
 //               tensor cores; order-key histogram; 16-bit Philox prefixes;
-//   K2 unit     one thread-block cluster per unit, one CTA per tile of the
-//               unit's tokens: each CTA finds the bucket of the k-th score,
-//               lists every token above it, its members (candidates) and the
-//               remainder tokens that can still be drawn, and sums its share
-//               of the normaliser; after a cluster barrier rank 0 resolves
-//               the exact k-th token and Z; after another, every CTA decides
-//               its listed tokens (top-k stratum, or the draw u < p), gathers
-//               the kept K/V rows and runs the corrected attention on the
-//               tensor cores; rank 0 merges the CTAs' (m, l, acc) through
-//               distributed shared memory.
+//   K2 unit     a group of CTAs per unit, one per tile of the unit's tokens:
+//               each CTA finds the bucket of the k-th score, lists every
+//               token above it, its members (candidates) and the remainder
+//               tokens that can still be drawn, and sums its share of the
+//               normaliser; once every tile has arrived (a counter in the
+//               unit's control block) every CTA resolves the exact k-th token
+//               and Z (the same computation in each), decides its listed
+//               tokens (top-k stratum, or the draw u < p), gathers the
+//               kept K/V rows and runs the corrected attention on the tensor
+//               cores; the last CTA of the unit merges the (m, l, acc)
+//               partials.  The grid is one wave (every unit's CTAs resident
+//               at once) and every wait has a time limit.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -26,8 +28,8 @@
 #include "ptx.cuh"
 
 // Phase markers: no-ops unless a profiling build defines SSA_MARK(k) to
-// record a timestamp for phase boundary k (and SSA_NOTE(k, v) to record a
-// value).
+// record a timestamp for phase boundary k (SSA_MARKG(k) inside a loop, and
+// SSA_NOTE(k, v) to record a value).
 #ifndef SSA_MARK
 #define SSA_MARK(k) ((void)0)
 #endif
@@ -40,6 +42,9 @@
 #ifndef SSA_NOTE
 #define SSA_NOTE(k, v) ((void)0)
 #endif
+#ifndef SSA_MARKG
+#define SSA_MARKG(k) ((void)0)
+#endif
 
 namespace ssa {
 
@@ -51,7 +56,7 @@ constexpr uint32_t DEV_BAD_INDEX = 0x8u;
 constexpr int kBins = 4096;            // 12-bit order-key buckets
 constexpr int kStageTok = 512;         // K1: tokens per pipeline stage (4 MMA tiles of 128)
 constexpr int kTileAlign = 512;        // K2: tiles are multiples of 512 tokens (32 per warp slice)
-constexpr int kMaxTiles = 16;          // K2: tiles (CTAs of a unit's cluster) per unit at most
+constexpr int kMaxTiles = 64;          // K2: tiles (CTAs) per unit at most
 constexpr int kSelThreads = 512;       // K2 block size; in the selection each warp owns a slice (a list) of the tile
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kInThreads = 256;        // score_input_kernel block size
@@ -59,14 +64,11 @@ constexpr int kQselBytes = 1024;       // B operand: 16 rows x d_sel bf16, swizz
 
 // Per-unit control block (zeroed by K0).
 struct UnitCtrl {
-    uint32_t pad0[2];
-    uint32_t ncand;      // members of the threshold bucket (the candidate array's length)
-    uint32_t theta;      // order key of the k-th largest score
-    int32_t idx_cut;     // key == theta and index <= idx_cut: top-k stratum (-1: none)
-    float m;             // reference point of the exponentials
-    float Z;             // normaliser over the remainder
+    uint32_t arrive;     // K2 tiles whose selection pass is done
     uint32_t k1_next;    // unit 0 only: K1's shared stage queue (stages taken)
-    uint32_t pad[8];
+    uint32_t karrive;    // K2 CTAs whose kept count is written
+    uint32_t done;       // K2 CTAs whose attention partial is written
+    uint32_t pad[12];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 
@@ -80,11 +82,12 @@ struct Plan {
     int64_t stages;      // K1 stages in all
     int32_t k1_grid;     // K1 CTAs (persistent)
     int32_t tt;          // K2 tile tokens (multiple of kTileAlign)
-    int32_t ntile;       // K2 tiles per unit = CTAs of the unit's cluster (1..kMaxTiles)
+    int32_t ntile;       // K2 tiles per unit = its CTAs (1..kMaxTiles)
     int64_t np;          // ntile * tt: padded tokens per unit
     int32_t hist_run;    // K1: stages of one unit per shared-histogram buffer (1..127)
     // workspace byte offsets
-    size_t o_status, o_ctrl, o_hist1, o_zpart, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
+    int32_t tcap;        // tiles the per-tile arrays hold per unit (>= ntile)
+    size_t o_status, o_ctrl, o_hist1, o_zpart, o_kcnt, o_part, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
         o_hout, o_hlse, total;
 };
 

@@ -1,6 +1,6 @@
 // k_attend.cuh -- K2, the unit kernel: the stratified selection's decisions
 // and the exact softmax attention over the selected rows with the inclusion
-// correction, one thread-block cluster per (batch, KV head) unit.
+// correction, a group of CTAs per (batch, KV head) unit.
 //
 // Sources (page title, section):
 //  * "FASA: Frequency-Aware Sparse Attention", section 3, Stage 2 "Focused
@@ -16,44 +16,34 @@
 //    in HBM is kept; section 3: the online-softmax state (m, l, acc), merged
 //    across splits.
 //
-// The C CTAs of a unit's cluster each own one tile of its tokens.  With the
-// selection (source 0) every CTA runs the tile pass (k_select.cuh), rank 0
-// resolves the k-th token and Z between two cluster barriers, and every CTA
-// then decides its own tile's listed tokens (top-k stratum, or the draw
-// u < p with the exact p) and keeps the chosen rows in index order.  With
+// The C CTAs of a unit each own one tile of its tokens.  With the selection
+// (source 0) every CTA runs the tile pass (k_select.cuh) and arrives on the
+// unit's counter; once all C have arrived every CTA resolves the k-th token
+// and Z (the same deterministic computation in each), decides its own
+// tile's listed tokens (top-k stratum, or the draw u < p with the exact p)
+// and keeps the chosen rows in index order.  With
 // every token kept (source 1) a CTA takes its tile's tokens with p = 1; with
 // the caller's lists (source 2) an even share of the unit's list.  The kept
 // rows go through the tensor cores 128 at a time -- S = K Q^T and
 // O^T = V^T P with tcgen05.mma, fp32 accumulators in tensor memory, P split
 // into two bf16 terms (hi + lo) so that the products keep fp32-level
-// accuracy -- and rank 0 merges the CTAs' (m, l, acc) through distributed
-// shared memory.
+// accuracy -- and the last CTA of the unit to finish merges the CTAs'
+// (m, l, acc) partials in rank order.  Every wait on another CTA is bounded
+// in time (a timeout sets SSA_DEV_TIMEOUT); the grid is one wave, so every
+// CTA of a unit is resident together.
 #pragma once
 #include "k_select.cuh"
 
 namespace ssa {
 
-// What the decisions need from the selection (source 0 only).
+// What the decisions need from the selection (source 0 only): the resolve's
+// results.
 struct UnitSel {
     uint32_t theta;
     int64_t cut;
     float m, Z;
     bool sampling;
 };
-
-__device__ __forceinline__ UnitSel load_unit_sel(const Params& p, int u)
-{
-    UnitSel s{0u, -1, 0.0f, 0.0f, false};
-    if (p.src_mode == 0) {
-        const UnitCtrl* ctrl = ws_ctrl(p) + u;
-        s.theta = __ldcg(&ctrl->theta);
-        s.cut = __ldcg(&ctrl->idx_cut);
-        s.m = __ldcg(&ctrl->m);
-        s.Z = __ldcg(&ctrl->Z);
-    }
-    s.sampling = p.budget > 0.0f && s.Z > 0.0f;
-    return s;
-}
 
 // Entries [c0, c0 + n) of this CTA's list (n <= LIST): staged through
 // ridx / rval (cp.async, one wave), decided, and the kept ones written in
@@ -201,9 +191,7 @@ struct UCfg {
     static constexpr uint32_t OFF_P = OFF_Q + 2u * QPLANE;         // 2 x P operand: 16 columns x 128 rows
     static constexpr uint32_t OFF_LIST = OFF_P + 2u * 2u * QPLANE; // cidx, clp
     static constexpr uint32_t OFF_RAW = OFF_LIST + (uint32_t)LIST * 8u;       // raw list staging
-    static constexpr uint32_t PS = (uint32_t)(G * D + 2 * G);                 // (acc, m, l) floats
-    static constexpr uint32_t OFF_PART = OFF_RAW + (uint32_t)LIST * 8u;
-    static constexpr uint32_t OFF_RED = OFF_PART + PS * 4u;                   // [2][2][4][G] floats
+    static constexpr uint32_t OFF_RED = OFF_RAW + (uint32_t)LIST * 8u;        // [2][2][4][G] floats
     static constexpr uint32_t OFF_BAR = (OFF_RED + 2u * 2u * 4u * G * 4u + 7u) & ~7u;
     static constexpr uint32_t NBAR = 10;                           // kv_full, kv_free, s_full, p_ready, o_full (x2)
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;      // tensor-memory slot, counts
@@ -224,7 +212,7 @@ constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST>::SMEM; }
 // (tensor-memory lanes = chunk rows for S, = head dims for O), warp 4 issues
 // the MMAs (and owns the tensor memory), warps 5 .. 15 gather the K and V
 // rows.  Chunk g uses buffers g & 1; barrier phases count chunks over the
-// whole CTA.  Grid: U * C CTAs, clusters of C = pl.ntile.
+// whole CTA.  Grid: U * C CTAs, C = pl.ntile per unit, one wave.
 template <int G, int D, int LIST>
 __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_constant__ Params p)
 {
@@ -235,7 +223,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     __shared__ uint32_t scan[kSelWarps];
     int32_t* cidx = reinterpret_cast<int32_t*>(smem + CF::OFF_LIST);
     float* clp = reinterpret_cast<float*>(smem + CF::OFF_LIST + LIST * 4);
-    float* part = reinterpret_cast<float*>(smem + CF::OFF_PART);
     float* red = reinterpret_cast<float*>(smem + CF::OFF_RED);   // [parity][max | sum][warp][G]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
     uint64_t* kv_full = bars;
@@ -243,12 +230,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     uint64_t* s_full = bars + 4;
     uint64_t* p_ready = bars + 6;
     uint64_t* o_full = bars + 8;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + CF::OFF_MISC);   // [0] tensor memory, [3] kept, [4..5] offsets
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + CF::OFF_MISC);   // [0] tensor memory, [2] last, [4..5] offsets
     uint32_t* pre = reinterpret_cast<uint32_t*>(smem + CF::OFF_PRE);
 
     const Plan& pl = p.pl;
     const int C = pl.ntile;
-    const int u = blockIdx.x / C, r = blockIdx.x % C;   // r is the CTA's rank in the unit's cluster
+    const int u = blockIdx.x / C, r = blockIdx.x % C;   // r: the CTA's rank (tile) in its unit
     const int b = u / p.Hkv, h = u % p.Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
@@ -284,6 +271,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     SSA_GT(5);
 
     // this CTA's list: [lo, hi)
+    UnitCtrl* ctrl = ws_ctrl(p) + u;
+    UnitSel us{0u, -1, 0.0f, 0.0f, false};
     int64_t lo = 0, hi = 0;
     if (p.src_mode == 0) {
         SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
@@ -295,15 +284,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                 run += sh.wcnt[w];
             }
             pre[kSelWarps] = run;
+            // the tile's lists, candidates, level-2 counts and share of Z are written
+            __threadfence();
+            atomicAdd(&ctrl->arrive, 1u);
         }
-        // the unit's tiles have written their lists, candidates, level-2
-        // counts and shares of Z: rank 0 resolves the k-th token and Z
-        __threadfence();
-        cluster_sync();
         SSA_MARK(3);
-        if (r == 0) resolve_unit(p, u, ts.f1, ts.above1, ts.target, ts.m, sh, reinterpret_cast<uint2*>(smem));
-        __threadfence();
-        cluster_sync();
+        // every tile of the unit has arrived: resolve the k-th token and Z
+        // (every CTA computes the same result)
+        if (tid == 0 && !wait_geq_bounded(&ctrl->arrive, (uint32_t)C)) flag(status, DEV_TIMEOUT);
+        __syncthreads();
+        resolve_unit(p, u, ts.f1, ts.above1, ts.target, ts.m, sh, reinterpret_cast<uint2*>(smem));
+        __syncthreads();
+        us.theta = sh.r_theta;
+        us.cut = sh.r_cut;
+        us.m = sh.r_m;
+        us.Z = sh.r_Z;
         SSA_MARK(4);
         hi = pre[kSelWarps];
     } else if (p.src_mode == 1) {
@@ -316,7 +311,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         hi = total * (r + 1) / C;
     }
     SSA_MARK(11);
-    const UnitSel us = load_unit_sel(p, u);
+    us.sampling = p.budget > 0.0f && us.Z > 0.0f;
     const int64_t stage_base = (p.src_mode == 0) ? (int64_t)r * pl.tt : lo;   // the compact list's staging
     const uint16_t* Kb = p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
     const uint16_t* Vb = p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
@@ -513,17 +508,20 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     SSA_MARK(8);
 
-    // this CTA's partial: acc per head dim, then (m, l) per head
-    if (warp < 4) {
+    // this CTA's partial (acc per head dim, then (m, l) per head) in the
+    // unit's partials array
+    constexpr int PS = G * D + 2 * G;
+    float* gpart = ws_part(p) + ((size_t)u * pl.tcap + r) * PS;
+    if (warp < 4 && p.attend) {
         if (tid < D) {
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) part[gg * D + tid] = acc[gg];
+            for (int gg = 0; gg < G; ++gg) gpart[gg * D + tid] = acc[gg];
         }
         if (tid == 0) {
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
-                part[G * D + gg] = m_run[gg];
-                part[G * D + G + gg] = l_run[gg];
+                gpart[G * D + gg] = m_run[gg];
+                gpart[G * D + G + gg] = l_run[gg];
             }
         }
     }
@@ -538,13 +536,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     // CTAs' tiles (or list shares) are in rank order, so CTA r's entries go
     // after those of ranks < r
     if (p.count_out || p.idx_out) {
-        if (tid == 0) misc[3] = (uint32_t)kept;
-        cluster_sync();
+        uint32_t* kcnt = ws_kcnt(p) + (size_t)u * pl.tcap;
+        if (tid == 0) {
+            kcnt[r] = (uint32_t)kept;
+            __threadfence();
+            atomicAdd(&ctrl->karrive, 1u);
+            if (!wait_geq_bounded(&ctrl->karrive, (uint32_t)C)) flag(status, DEV_TIMEOUT);
+        }
+        __syncthreads();
         if (warp == 0) {
-            const uint32_t v = lane < C ? ld_dsmem_u32(&misc[3], (uint32_t)lane) : 0u;
-            const uint32_t x = warp_incl_scan(v);
-            const uint32_t before = __shfl_sync(0xffffffffu, x - v, r);
-            const uint32_t all = __shfl_sync(0xffffffffu, x, 31);
+            uint32_t before = 0, all = 0;
+#pragma unroll 1
+            for (int k = lane; k < C; k += 32) {
+                const uint32_t v = __ldcg(kcnt + k);
+                all += v;
+                before += (k < r) ? v : 0u;
+            }
+            before = warp_sum_u32(before);
+            all = warp_sum_u32(all);
             if (lane == 0) {
                 misc[4] = before;
                 misc[5] = all;
@@ -571,40 +580,69 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     SSA_MARK(12);
     SSA_GT(6);
-    // rank 0 merges the cluster's partials in rank order and writes the
-    // unit's output rows and log-sum-exp
-    if (p.attend) cluster_sync();   // every partial is written (and every kept count read)
-    if (p.attend && r == 0) {
-        constexpr int EPT = (G * D + 255) / 256;   // elements per merging thread (one head)
-        const int e0 = tid * EPT;
-        if (tid < 256 && e0 < G * D) {
-            const int gg = e0 / D;
-            float M = -INFINITY;
-#pragma unroll 1
-            for (int k = 0; k < C; ++k) M = fmaxf(M, ld_dsmem_f32(part + G * D + gg, (uint32_t)k));
-            float Ls = 0.0f, A[EPT];
+    if (!p.attend) return;
+    // the last CTA of the unit to finish merges the partials in rank order
+    // and writes the unit's output rows and log-sum-exp
+    if (tid == 0) {
+        __threadfence();
+        misc[2] = (atomicAdd(&ctrl->done, 1u) == (uint32_t)(C - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!misc[2]) return;
+    __threadfence();
+    // the partials are staged in shared memory (the K/V chunk buffers) a
+    // group at a time with one wave of copies, then merged in rank order
+    const float* parts = ws_part(p) + (size_t)u * pl.tcap * PS;
+    float* sp = reinterpret_cast<float*>(smem);
+    constexpr int KB = (int)(CF::OFF_Q / (PS * 4u));   // partials per group
+    static_assert(KB >= 1, "a partial fits the staging");
+    constexpr int EPT = (G * D + kSelThreads - 1) / kSelThreads;   // elements per thread (one head)
+    const int e0 = tid * EPT;
+    const bool mine = e0 < G * D;
+    const int gg = mine ? e0 / D : 0;
+    float M = -INFINITY, Ls = 0.0f, A[EPT];
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
-            if (M != -INFINITY) {
+    for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
 #pragma unroll 1
-                for (int k = 0; k < C; ++k) {
-                    const float mk = ld_dsmem_f32(part + G * D + gg, (uint32_t)k);
-                    const float wgt = (mk == -INFINITY) ? 0.0f : expf(mk - M);
-                    Ls = fmaf(ld_dsmem_f32(part + G * D + G + gg, (uint32_t)k), wgt, Ls);
+    for (int k0 = 0; k0 < C; k0 += KB) {
+        const int nk = min(KB, C - k0);
+        if (k0 > 0) __syncthreads();   // the previous group is consumed
+#pragma unroll 1
+        for (int i = tid; i < nk * PS; i += kSelThreads) cp_async_4(sp + i, parts + (size_t)k0 * PS + i);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        if (mine) {
+            float Mg = -INFINITY;
+#pragma unroll 1
+            for (int k = 0; k < nk; ++k) Mg = fmaxf(Mg, sp[k * PS + G * D + gg]);
+            if (Mg != -INFINITY) {
+                const float Mn = fmaxf(M, Mg);
+                const float a = (M == -INFINITY) ? 0.0f : expf(M - Mn);
+                Ls *= a;
 #pragma unroll
-                    for (int e = 0; e < EPT; ++e) A[e] = fmaf(ld_dsmem_f32(part + e0 + e, (uint32_t)k), wgt, A[e]);
+                for (int e = 0; e < EPT; ++e) A[e] *= a;
+#pragma unroll 1
+                for (int k = 0; k < nk; ++k) {
+                    const float mk = sp[k * PS + G * D + gg];
+                    const float wgt = (mk == -INFINITY) ? 0.0f : expf(mk - Mn);
+                    Ls = fmaf(sp[k * PS + G * D + G + gg], wgt, Ls);
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) A[e] = fmaf(sp[k * PS + e0 + e], wgt, A[e]);
                 }
-            }
-            const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + gg;
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-                const int c = (e0 + e) % D;
-                p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
-                if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
+                M = Mn;
             }
         }
     }
-    cluster_sync();   // a CTA's shared memory stays until every remote read of it is done
+    if (mine) {
+        const int64_t head = (int64_t)b * p.Hq + (int64_t)h * G + gg;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            const int c = (e0 + e) % D;
+            p.out[head * D + c] = (Ls > 0.0f) ? A[e] / Ls : 0.0f;
+            if (c == 0) p.lse[head] = (Ls > 0.0f) ? M + logf(Ls) : -INFINITY;
+        }
+    }
     SSA_MARK(9);
     SSA_GT(7);
 }

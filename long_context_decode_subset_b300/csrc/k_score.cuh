@@ -84,6 +84,8 @@ __device__ __forceinline__ uint32_t* ws_hist1(const Params& p) { return reinterp
 // level-2 histogram (the next 12 key bits of the threshold bucket's members), [U][kBins]
 __device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return ws_hist1(p) + (size_t)p.pl.U * kBins; }
 __device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
+__device__ __forceinline__ uint32_t* ws_kcnt(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_kcnt); }
+__device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
 __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
 constexpr int k1EpiThreads = 512;
 constexpr int kHistWarps = 4;
 __host__ __device__ constexpr int k1_threads(bool hist) { return hist ? 640 + 32 * kHistWarps : 640; }
-constexpr int kGrab = 2;         // stages a CTA takes from the shared queue at a time
+constexpr int kGrab = 1;         // stages a CTA takes from the shared queue at a time
 constexpr int kPreIssue = 1;     // stages issued before the set-up barrier
 constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages + accumulator buffers)
 

@@ -13,7 +13,7 @@
 //   bucket f that holds the k-th score (the largest when k = 0).
 //
 // Selection pass of the unit kernel (K2): one CTA of 512 threads per (unit,
-// tile), the unit's tiles forming a thread-block cluster; each of its 16
+// tile); each of its 16
 // warps owns a contiguous slice of the tile (tile / 16 tokens), staged
 // through shared memory, and walks it in index order:
 //   * a token above bucket f is in T: it joins the slice's list (p = 1);
@@ -25,8 +25,9 @@
 //     of Z read off the histogram (every term of bucket c is at least
 //     exp(floor_c - m)), and u is at least its 16-bit prefix (drawn by the
 //     score kernel), so prefix >= B e / Z_lb rules it out for good.
-// After a cluster barrier, rank 0 resolves the exact k-th token among the
-// candidates -- in shared memory: a 12-bit histogram, then the few members
+// Once every tile of the unit has arrived, each CTA resolves the exact k-th
+// token among the candidates (the same computation in every CTA of the unit,
+// so no CTA waits for another's result) -- in shared memory: a 12-bit histogram, then the few members
 // sharing 24 key bits ranked exactly (key desc, index asc) -- and completes
 // Z: the tiles' shares in tile order plus the remainder candidates' terms,
 // summed exactly as 128-bit integers (every such term is an fp32 value of at
@@ -54,6 +55,10 @@ struct SelShared {
     unsigned long long zi[kSelWarps][2];
     uint32_t coff[kMaxTiles + 1];   // per-tile candidate offsets
     uint32_t wcnt[kSelWarps];       // the tile pass: list length of each warp slice
+    // the resolve's results: order key of the k-th score, the tie cut, m and Z
+    uint32_t r_theta;
+    int32_t r_cut;
+    float r_m, r_Z;
 };
 
 // What each (unit, tile) CTA leaves for the resolve: its share of Z
@@ -64,9 +69,9 @@ struct TilePart {
     uint32_t ncand, pad;
 };
 
-constexpr int kSlice = 512;           // tokens a warp stages at a time
-constexpr int kResStage = kSelWarps * kSlice * 6 / 8;   // candidates the resolve stages at a time (same memory)
-static_assert(kResStage * 8 <= kSelWarps * kSlice * 6, "the resolve's staging fits the pass's");
+constexpr int kSlice = 512;           // tokens a warp stages at a time (two chunks in flight)
+constexpr int kResStage = kSelWarps * kSlice * 2 * 6 / 8;   // candidates the resolve stages at a time (same memory)
+static_assert(kResStage * 8 <= kSelWarps * kSlice * 2 * 6, "the resolve's staging fits the pass's");
 
 
 __device__ __forceinline__ void zacc(float& zh, float& zl, float v)
@@ -193,8 +198,7 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
     const bool want_z = p.budget > 0.0f;
-    UnitCtrl* ctrl = ws_ctrl(p) + u;
-    const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.ntile;
+    const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.tcap;
     // one wave of loads: the tiles' candidate counts and shares of Z (two
     // tiles per thread: at most kMaxTiles tiles) and the candidates' level-2
     // histogram (the next 12 key bits, counted by the tiles; 8 bins per
@@ -384,11 +388,10 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
         float c_hi, c_lo;
         u128_to_float2(shi, slo, c_hi, c_lo);
         comp_add(hh, ll, c_hi, c_lo);
-        ctrl->ncand = E;
-        ctrl->theta = theta;
-        ctrl->idx_cut = (int32_t)idx_cut;
-        ctrl->m = m;
-        ctrl->Z = __fadd_rn(hh, ll);
+        sh.r_theta = theta;
+        sh.r_cut = (int32_t)idx_cut;
+        sh.r_m = m;
+        sh.r_Z = __fadd_rn(hh, ll);
     }
 }
 
@@ -406,7 +409,7 @@ struct TileSel {
 
 // Dynamic shared memory the pass stages its warps' chunks in (scores and
 // Philox prefixes); the resolve stages candidates in the same bytes.
-constexpr uint32_t kSelStageBytes = (uint32_t)kSelWarps * kSlice * 6u;
+constexpr uint32_t kSelStageBytes = (uint32_t)kSelWarps * kSlice * 2u * 6u;
 
 __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelShared& sh, unsigned char* k2dyn)
 {
@@ -422,18 +425,28 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
     const float B = p.budget;
     const bool sampling = B > 0.0f;
     // Each warp stages its slice kSlice tokens at a time (scores and Philox
-    // prefixes, cp.async); the first chunk's copies go out before the
-    // histogram search.  The loop over the chunk is kept rolled: the code runs
+    // prefixes, cp.async) into two buffers: the next chunk's copies are in
+    // flight while the current one is walked.  The first chunk's copies go
+    // out before the histogram search.  Loops are kept rolled: the code runs
     // once per launch, so its size, not its instruction count, sets its time.
-    float* ssc = reinterpret_cast<float*>(k2dyn) + warp * kSlice;
-    uint16_t* su = reinterpret_cast<uint16_t*>(k2dyn + kSelWarps * kSlice * 4) + warp * kSlice;
+    float* ssc = reinterpret_cast<float*>(k2dyn) + warp * 2 * kSlice;
+    uint16_t* su = reinterpret_cast<uint16_t*>(k2dyn + kSelWarps * kSlice * 2 * 4) + warp * 2 * kSlice;
+    // whole 16-byte score copies when the unit's row and the warp's slice allow
+    const bool s16 = ((uint64_t)u * (uint64_t)pl.N) % 4 == 0 && base + W2 <= pl.N;
     auto stage = [&](int c0) {
         const int n = min(kSlice, W2 - c0);
+        float* dsc = ssc + ((c0 / kSlice) & 1) * kSlice;
+        uint16_t* dsu = su + ((c0 / kSlice) & 1) * kSlice;
+        if (s16) {
 #pragma unroll 1
-        for (int i = lane; i < n; i += 32) cp_async_4(ssc + i, S + min(base + c0 + i, pl.N - 1));
+            for (int i = lane * 4; i < n; i += 128) cp_async_16(dsc + i, S + base + c0 + i);
+        } else {
+#pragma unroll 1
+            for (int i = lane; i < n; i += 32) cp_async_4(dsc + i, S + min(base + c0 + i, pl.N - 1));
+        }
         if (sampling) {
 #pragma unroll 1
-            for (int i = lane * 8; i < n; i += 256) cp_async_16(su + i, ub + c0 + i);
+            for (int i = lane * 8; i < n; i += 256) cp_async_16(dsu + i, ub + c0 + i);
         }
         cp_async_commit();
     };
@@ -509,63 +522,94 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
     uint2* cseg = ws_cand(p) + (size_t)u * pl.N + (size_t)tile * pl.tt;
     uint32_t* hist2 = ws_hist2(p) + (size_t)u * kBins;   // level-2 histogram of the unit's candidates
     uint32_t cnt = 0;
-    float zq[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // two (hi, lo) Z accumulators
-    const uint32_t lt = lanemask_lt();
+    float zh4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, zl4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four (hi, lo) Z accumulators
     // the prefix test in units of 2^-16: prefix < B e / Z_lb * 2^16 (a power-of-two scale, exact)
     const float bound16 = __fmul_rn(bound_scale, 65536.0f);
 #pragma unroll 1
     for (int c0 = 0; c0 < W2; c0 += kSlice) {
-        if (c0 > 0) {
+        // the next chunk's copies go out before this one is walked
+        if (c0 / kSlice < 4) SSA_MARKG(16 + c0 / kSlice);
+        if (c0 + kSlice < W2) {
             __syncwarp();
-            stage(c0);
+            stage(c0 + kSlice);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        cp_async_wait<0>();
         __syncwarp();
-        const int n = min(kSlice, W2 - c0);   // a multiple of 32: the trip count is warp-uniform
+        const float* csc = ssc + ((c0 / kSlice) & 1) * kSlice;
+        const uint16_t* csu = su + ((c0 / kSlice) & 1) * kSlice;
+        const int n = min(kSlice, W2 - c0);   // a multiple of 32
         // tokens [0, nvalid) of the chunk are in the cache (the last tile's tail is not)
         const int nvalid = (int)min((int64_t)n, pl.N - (base + c0));
         const uint32_t t0 = (uint32_t)(base + c0);   // token indices fit 31 bits
-        // two tokens (i, i + 32) per step, each with its own Z accumulator
-        // (independent dependency chains); lists stay in index order
+        // each lane takes four consecutive tokens of a 128-token group; the
+        // group's kept tokens are listed in index order at the warp's
+        // running count plus the lane's exclusive prefix
 #pragma unroll 1
-        for (int i0 = lane; i0 < n; i0 += 64) {
+        for (int g0 = 0; g0 < n; g0 += 128) {
+            if ((c0 + g0) / 128 < 16) SSA_MARKG((c0 + g0) / 128);
+            const int i0 = g0 + 4 * lane;
+            float sv[4];
+            uint32_t pr[4] = {0u, 0u, 0u, 0u};
+            if (i0 < n) {
+                const float4 v = *reinterpret_cast<const float4*>(csc + i0);
+                sv[0] = v.x; sv[1] = v.y; sv[2] = v.z; sv[3] = v.w;
+                if (sampling) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(csu + i0);
+                    pr[0] = w.x & 0xffffu; pr[1] = w.x >> 16; pr[2] = w.y & 0xffffu; pr[3] = w.y >> 16;
+                }
+            } else {
+                sv[0] = sv[1] = sv[2] = sv[3] = 0.0f;
+            }
+            uint32_t kbits = 0;
+            float val[4];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int i = i0 + 32 * q;
-                if (i - lane < n) {   // warp-uniform (n is a multiple of 32)
-                const uint32_t t = t0 + (uint32_t)i;
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + q;
                 const bool valid = i < nvalid;
-                const float s = ssc[i];
-                const uint32_t k = okey(s);
+                const uint32_t k = okey(sv[q]);
                 const uint32_t b1 = k >> 20;
                 const bool above = valid && b1 > f1.bin;
                 const bool is_cand = valid && b1 == f1.bin;
                 bool keep = above || is_cand;
-                float val = above ? INFINITY : s;
+                val[q] = above ? INFINITY : sv[q];
                 if (sampling && valid && b1 < f1.bin) {
-                    const float e = expf(__fsub_rn(s, m));
-                    zacc(zq[q][0], zq[q][1], e);
-                    keep = __fmul_ru(e, bound16) > __uint2float_rn((uint32_t)su[i]);
-                    val = e;
+                    const float e = expf(__fsub_rn(sv[q], m));
+                    zacc(zh4[q], zl4[q], e);
+                    keep = __fmul_ru(e, bound16) > __uint2float_rn(pr[q]);
+                    val[q] = e;
                 }
-                const uint32_t km = __ballot_sync(0xffffffffu, keep);
-                if (keep) {
-                    const uint32_t o = cnt + __popc(km & lt);
-                    sidx[o] = (int32_t)(t | (is_cand ? kCandFlag : 0u));
-                    sval[o] = val;
-                }
-                cnt += __popc(km);
+                if (keep) kbits |= 1u << q;
                 if (is_cand) {
+                    const uint32_t t = t0 + (uint32_t)i;
                     cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(k, t);
                     atomicAdd(hist2 + ((k >> 8) & 0xfffu), 1u);
-                }
+                    kbits |= 0x10u << q;   // a candidate: flagged in the list
                 }
             }
+            const uint32_t nk = __popc(kbits & 0xfu);
+            const uint32_t incl = warp_incl_scan(nk);
+            uint32_t o = cnt + incl - nk;
+            if (kbits & 0xfu) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (kbits & (1u << q)) {
+                        const uint32_t t = t0 + (uint32_t)(i0 + q);
+                        sidx[o] = (int32_t)(t | ((kbits & (0x10u << q)) ? kCandFlag : 0u));
+                        sval[o] = val[q];
+                        ++o;
+                    }
+                }
+            }
+            cnt += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     SSA_MARK(18);
-    float zh = zq[0][0], zl = zq[0][1];
-    comp_add(zh, zl, zq[1][0], zq[1][1]);
+    float zh = zh4[0], zl = zl4[0];
+    comp_add(zh, zl, zh4[1], zl4[1]);
+    comp_add(zh, zl, zh4[2], zl4[2]);
+    comp_add(zh, zl, zh4[3], zl4[3]);
     if (lane == 0) sh.wcnt[warp] = cnt;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -593,7 +637,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
             tpo.zl = ll;
             tpo.ncand = sh.ncand_cta;
             tpo.pad = 0;
-            reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.ntile + tile] = tpo;
+            reinterpret_cast<TilePart*>(ws_zpart(p))[(size_t)u * pl.tcap + tile] = tpo;
         }
     }
     return TileSel{f1.bin, f1.above, target, m};

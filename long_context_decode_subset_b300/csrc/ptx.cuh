@@ -87,6 +87,34 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t 
     return true;
 }
 
+// Acquire load of a flag or counter other CTAs release (gpu scope).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Release store of a flag (gpu scope): earlier writes become visible first.
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait, for at most `limit_ns`, until *p >= target (one thread; it sleeps
+// between polls).  Returns false on timeout.
+__device__ __forceinline__ bool wait_geq_bounded(const uint32_t* p, uint32_t target,
+                                                 uint64_t limit_ns = 2000000000ull)
+{
+    if (ld_acquire_u32(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_u32(p) < target) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
 // L2 policy: evict-first, for data streamed once (the key summary).
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
@@ -343,35 +371,6 @@ __device__ __forceinline__ void cp_async_16_zfill(void* dst_smem, const void* sr
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)), "l"(src),
                  "r"(valid ? 16 : 0)
                  : "memory");
-}
-
-// Thread-block clusters: this CTA's rank, a full cluster barrier, and loads
-// from another CTA's shared memory (distributed shared memory).
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t ld_dsmem_u32(const void* local_smem, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return v;
-}
-__device__ __forceinline__ float ld_dsmem_f32(const void* local_smem, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local_smem)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
 }
 
 }  // namespace ssa

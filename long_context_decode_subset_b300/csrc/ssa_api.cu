@@ -44,16 +44,21 @@ int device_sms()
 // Plan and workspace layout.  The layout does not depend on the device: the
 // per-unit token arrays are sized for the largest tiling (at most kMaxTiles
 // tiles of 512-token multiples pad a unit by less than kMaxTiles * 512
-// tokens).  The tiling itself -- the unit kernel's cluster size -- and the
+// tokens).  The tiling itself -- the unit kernel's CTAs per unit -- and the
 // score kernel's grid do depend on the device; `tiles` > 0 gives the tile
 // count (the tiles are then the fewest 512-token multiples that cover N in
-// that many pieces).  SSA_FORCE_TILE (tokens per tile) and SSA_FORCE_SPLIT
-// (tiles per unit) override the choice (the tests use them to cover many
-// tilings on small inputs), and SSA_FORCE_HIST_RUN the score kernel's
-// histogram hand-over period.
+// that many pieces) and `fit` the most tiles per unit one wave of the unit
+// kernel holds.  SSA_FORCE_TILE (tokens per tile, if its tile count fits)
+// and SSA_FORCE_SPLIT (tiles per unit) override the choice (the tests use
+// them to cover many tilings on small inputs), and SSA_FORCE_HIST_RUN the
+// score kernel's histogram hand-over period.
 constexpr int64_t kPadTokens = (int64_t)kMaxTiles * kTileAlign;
 
-ssa::Plan make_plan(const ssa_shape& s, int tiles)
+// Tiles per unit the per-tile arrays are sized for: as many as two CTAs on
+// every SM of a 148-SM device could give a unit, at most kMaxTiles.
+int tile_cap(int64_t U) { return (int)std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, (296 + U - 1) / std::max<int64_t>(U, 1))); }
+
+ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
 {
     ssa::Plan pl{};
     pl.U = s.batch * s.n_kv_heads;
@@ -65,17 +70,18 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles)
     pl.sf = (int32_t)((int64_t)pl.nst * 3 / 4);   // the rest of each unit goes to K1's shared queue
     const int sms = tiles > 0 ? device_sms() : 148;
     pl.k1_grid = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sms, pl.stages));
-    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, (N + kTileAlign - 1) / kTileAlign));
+    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(tile_cap(U), (N + kTileAlign - 1) / kTileAlign));
     int64_t c = std::max<int64_t>(1, std::min<int64_t>(tiles > 0 ? tiles : 1, cmax));
     int64_t tt = std::max<int64_t>(kTileAlign, ((N + c - 1) / c + kTileAlign - 1) / kTileAlign * kTileAlign);
     const int forced_tile = env_int("SSA_FORCE_TILE", 0);
     if (tiles > 0 && forced_tile >= kTileAlign && forced_tile % kTileAlign == 0 &&
-        (N + forced_tile - 1) / forced_tile <= kMaxTiles &&
+        (N + forced_tile - 1) / forced_tile <= std::min<int64_t>(fit, tile_cap(U)) &&   // one wave
         (N + forced_tile - 1) / forced_tile * forced_tile < N + kPadTokens)   // within the sized padding
         tt = forced_tile;
     pl.tt = (int32_t)tt;
     pl.ntile = (int32_t)std::max<int64_t>(1, (N + tt - 1) / tt);
     pl.np = (int64_t)pl.ntile * tt;
+    pl.tcap = tile_cap(U);
     // K1's histogram buffers are handed over after at most kHistRun stages of
     // one unit; SSA_FORCE_HIST_RUN lowers that (the tests use it to hand
     // buffers over at every stage or two)
@@ -83,7 +89,7 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles)
     const int forced_run = env_int("SSA_FORCE_HIST_RUN", 0);
     if (forced_run >= 1 && forced_run <= kHistRun) pl.hist_run = forced_run;
 
-    const int64_t D = s.head_dim;
+    const int64_t D = s.head_dim, G = pl.G;
     const int64_t heads = (int64_t)s.batch * s.n_q_heads;
     const int64_t npmax = N + kPadTokens;
     size_t o = 0;
@@ -95,7 +101,9 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles)
     pl.o_status = take(kStatusBytes);
     pl.o_ctrl = take((size_t)U * sizeof(UnitCtrl));
     pl.o_hist1 = take((size_t)U * kBins * 4 * 2);   // level-1 then level-2 histograms
-    pl.o_zpart = take((size_t)U * kMaxTiles * 16);
+    pl.o_zpart = take((size_t)U * pl.tcap * 16);
+    pl.o_kcnt = take((size_t)U * pl.tcap * 4);
+    pl.o_part = take((size_t)U * pl.tcap * (size_t)(G * D + 2 * G) * 4);
     pl.o_cand = take((size_t)U * N * 8);
     pl.o_sel_idx = take((size_t)U * npmax * 4);
     pl.o_sel_p = take((size_t)U * npmax * 4);
@@ -246,7 +254,7 @@ bool allow_dynamic_smem(kfn_t fn, uint32_t smem)
 // kernel of a step is an ordinary launch: it starts after everything before
 // it on the stream (the caller's writes of the query, say) has completed.
 ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::Params& prm, cudaStream_t stream,
-                  bool dependent, int cluster = 0)
+                  bool dependent)
 {
     if (grid <= 0) return SSA_OK;
     if (grid > INT32_MAX) return SSA_ERR_UNSUPPORTED;
@@ -256,18 +264,11 @@ ssa_status launch(kfn_t fn, int64_t grid, int block, uint32_t smem, const ssa::P
     cfg.blockDim = dim3((unsigned)block, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute at[2];
+    cudaLaunchAttribute at[1];
     unsigned na = 0;
     if (dependent) {
         at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         at[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    if (cluster > 0) {   // a thread-block cluster launch (a cluster of one CTA included)
-        at[na].id = cudaLaunchAttributeClusterDimension;
-        at[na].val.clusterDim.x = (unsigned)cluster;
-        at[na].val.clusterDim.y = 1;
-        at[na].val.clusterDim.z = 1;
         ++na;
     }
     cfg.attrs = na ? at : nullptr;
@@ -307,80 +308,54 @@ ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cud
     return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1_threads(hist), smem, p, stream, dependent);
 }
 
-// Clusters of more than 8 CTAs are allowed for `fn` (once per kernel, per device).
-bool allow_big_clusters(kfn_t fn)
+// CTAs of `fn` resident per SM (cached per kernel, shared-memory size and device).
+int blocks_per_sm(kfn_t fn, int block, uint32_t smem)
 {
     static std::mutex mu;
-    static std::map<std::pair<void*, int>, bool> done;
+    static std::map<std::tuple<void*, uint32_t, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return 1;
     }
-    const auto key = std::make_pair((void*)fn, dev);
-    std::lock_guard<std::mutex> lk(mu);
-    if (done.count(key)) return done[key];
-    const bool ok = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    if (!ok) cudaGetLastError();
-    done[key] = ok;
-    return ok;
-}
-
-// Clusters of `cl` CTAs of `fn` (`threads` threads, `smem` bytes) resident
-// on the device at once (cached per kernel, cluster size and device; 0 if
-// the size cannot be launched).
-int64_t active_clusters(kfn_t fn, int cl, int threads, uint32_t smem)
-{
-    static std::mutex mu;
-    static std::map<std::tuple<void*, int, int>, int64_t> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    const auto key = std::make_tuple((void*)fn, cl, dev);
+    const auto key = std::make_tuple((void*)fn, smem, dev);
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
     int n = 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cl, 1, 1);
-    cfg.blockDim = dim3((unsigned)threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)cl;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) || (cl > 8 && !allow_big_clusters(fn)) ||
-        cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
+    if ((smem > 0 && !allow_dynamic_smem(fn, smem)) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)fn, block, smem) != cudaSuccess) {
         cudaGetLastError();
-        n = 0;
+        n = 1;
     }
+    n = std::max(n, 1);
     std::lock_guard<std::mutex> lk(mu);
     cache[key] = n;
     return n;
 }
 
-// Tiles per unit, i.e. the unit kernel's cluster size: SSA_FORCE_SPLIT if
-// set, else the largest c <= kMaxTiles for which the clusters of every unit
-// are resident at once (one wave; the plan also caps c at the 512-token
-// pieces of the context).
-int unit_tiles(const ssa_shape& s)
+// The most tiles (CTAs) per unit the device holds at once with every unit
+// getting the same number.  The CTAs of a unit wait on one another, so the
+// unit kernel's grid must be one wave: U * tiles never exceeds this.
+int unit_fit(const ssa_shape& s)
 {
-    const int forced = env_int("SSA_FORCE_SPLIT", 0);
-    if (forced > 0) return std::min(forced, kMaxTiles);
     const int64_t U = std::max<int64_t>(1, (int64_t)s.batch * s.n_kv_heads);
-    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, (s.ctx_len + kTileAlign - 1) / kTileAlign));
     uint32_t smem = 0;
     kfn_t fn = pick_unit(s.n_q_heads / s.n_kv_heads, s.head_dim, &smem);
-    for (int64_t c = cmax; c >= 2; --c)
-        if (active_clusters(fn, (int)c, kSelThreads, smem) >= U) return (int)c;
-    return 1;
+    const int64_t slots = (int64_t)blocks_per_sm(fn, kSelThreads, smem) * device_sms();
+    return (int)std::max<int64_t>(1, std::min<int64_t>(kMaxTiles, slots / U));
+}
+
+// The unit kernel's plan: as many tiles per unit as one wave holds, or
+// SSA_FORCE_SPLIT of them (at most that many); the plan also caps the tiles
+// at the 512-token pieces of the context and at the per-tile arrays.
+ssa::Plan unit_plan(const ssa_shape& s)
+{
+    const int fit = unit_fit(s);
+    const int forced = env_int("SSA_FORCE_SPLIT", 0);
+    return make_plan(s, forced > 0 ? std::min(forced, fit) : fit, fit);
 }
 
 ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream, bool dependent)
@@ -388,8 +363,7 @@ ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t st
     uint32_t smem = 0;
     kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
-    if (p.pl.ntile > 8 && !allow_big_clusters(fn)) return SSA_ERR_CUDA;
-    return launch(fn, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, smem, p, stream, dependent, p.pl.ntile);
+    return launch(fn, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, smem, p, stream, dependent);
 }
 
 }  // namespace
@@ -541,7 +515,7 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
     if (st != SSA_OK) return st;
     if (!s_hat || !idx || !p || !count) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
+    const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
@@ -574,7 +548,7 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     if (!q || !idx || !p || !count || !out || !lse || (shape->ctx_len > 0 && (!K || !V))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
+    const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
@@ -631,7 +605,7 @@ ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16*
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget) || bad_scale(scale)) return SSA_ERR_INVALID_ARG;
     if ((idx_opt == nullptr) != (p_opt == nullptr)) return SSA_ERR_INVALID_ARG;
-    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
+    const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     char* w = static_cast<char*>(ws);
@@ -801,7 +775,7 @@ ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* 
 {
     const ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
-    const ssa::Plan pl = make_plan(*shape, unit_tiles(*shape));
+    const ssa::Plan pl = unit_plan(*shape);
     if (score_ctas) *score_ctas = pl.k1_grid;
     if (tiles_per_unit) *tiles_per_unit = pl.ntile;
     if (attend_ctas_per_unit) *attend_ctas_per_unit = pl.ntile;
