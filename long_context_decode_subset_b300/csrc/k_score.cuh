@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
 constexpr int k1EpiThreads = 512;
 constexpr int kHistWarps = 4;
 __host__ __device__ constexpr int k1_threads(bool hist) { return hist ? 640 + 32 * kHistWarps : 640; }
-constexpr int kGrab = 1;         // stages a CTA takes from the shared queue at a time
+constexpr int kGrab = 2;         // stages a CTA takes from the shared queue at a time
 constexpr int kPreIssue = 1;     // stages issued before the set-up barrier
 constexpr int kInfo = 32;        // stage descriptors in flight (> ring stages + accumulator buffers)
 
