@@ -105,6 +105,21 @@ typedef enum {
     SSA_ERR_BAD_INDEX = 8        /* device: a selected index or summary channel out of range */
 } ssa_status;
 
+/* The strata of a step ("Stratified Sparse Attention speeds up decoding 2.96x
+ * on a 1M context", sections "Where sparse attention loses quality" and "How
+ * SSA splits the cache into strata": pure top-k, top-p and hybrids of a
+ * deterministic stratum with sampling are special cases of the strata). */
+typedef enum {
+    SSA_STRATA_SSA = 0,      /* top-k stratum; the remainder R drawn with p_j = min(1, B e_j / Z),
+                                e_j = exp(s_j - m) (the method; ssa_decode / ssa_select) */
+    SSA_STRATA_UNIFORM = 1,  /* top-k stratum; every remainder token drawn with the same
+                                p = min(1, fl32(B / fl32(N - min(k, N)))) (1 for B = +inf):
+                                the top-k + uniform-sampling hybrid */
+    SSA_STRATA_TOP_P = 2     /* top-p stratum: the fewest tokens, in the top-k order, whose share
+                                of the softmax of s over all N tokens reaches top_p; the
+                                remainder drawn as in SSA_STRATA_SSA */
+} ssa_strata;
+
 /* Device status bits (ssa_get_device_status). */
 #define SSA_DEV_NONFINITE 0x1u
 #define SSA_DEV_OVERFLOW 0x2u
@@ -187,6 +202,15 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
                       int32_t* idx, float* p, int32_t* count, int64_t list_cap,
                       void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
 
+/* ssa_select with a choice of strata (ssa_strata; top_p is read for
+ * SSA_STRATA_TOP_P only, top_k for the others).  The same Philox uniforms
+ * decide every draw.  SSA_STRATA_TOP_P is declared but not built: it returns
+ * SSA_ERR_UNSUPPORTED.  An unknown strata or a negative or NaN top_p is
+ * SSA_ERR_INVALID_ARG. */
+ssa_status ssa_select_strata(const float* s_hat, int strata, int64_t top_k, float top_p, float budget,
+                             uint64_t seed, int32_t* idx, float* p, int32_t* count, int64_t list_cap,
+                             void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
+
 /* Step (c): corrected attention over given selections (rows idx[u][0..min(count[u],
  * list_cap)) with probabilities p > 0): softmax over the logits
  * scale * q.K_i - log p_i ("FASA", section 3, Stage 2 "Focused Attention
@@ -216,6 +240,15 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
                       cudaStream_t stream);
+
+/* ssa_decode with a choice of strata (as ssa_select_strata); the attention
+ * corrects every kept token by its p whatever the strata. */
+ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                             const ssa_bf16* Ks, const int32_t* sel_ch, int strata, int64_t top_k,
+                             float top_p, float budget, uint64_t seed, float scale, float* out, float* lse,
+                             float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
+                             int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                             cudaStream_t stream);
 
 /* Append and decode in one chain: the new token (k_new, v_new, as in
  * ssa_append) is written at position ctx_len - 1 of K, V and Ks by the

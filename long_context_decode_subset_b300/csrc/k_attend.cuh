@@ -121,7 +121,7 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int6
                             keep = true;
                             pv = 1.0f;
                         }
-                        ev = expf(__fsub_rn(pv, us.m));
+                        ev = (p.strata == 1) ? 1.0f : expf(__fsub_rn(pv, us.m));
                     }
                     if (!keep) {
                         pv = us.sampling ? prob_from_term(ev, p.budget, us.Z) : 0.0f;

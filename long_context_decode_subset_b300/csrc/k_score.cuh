@@ -46,6 +46,8 @@ struct Params {
     int32_t dense;             // every token selected with p = 1 (top_k >= N or budget = +inf)
     int32_t attend;            // K2 computes attention (else it only writes the compact list)
     int32_t src_mode;          // K2 rows: 0 the selection, 1 all tokens, 2 the caller's compact list
+    int32_t strata;            // the remainder's sampler: 0 p proportional to exp(s), 1 uniform
+    float z_uniform;           // strata 1: the remainder's size N - min(k, N) as fp32
     const uint16_t* q;         // [Bt][Hq][d]
     const uint16_t* K;         // [Bt][Hkv][N][d] with the strides below
     const uint16_t* V;

@@ -197,7 +197,7 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
-    const bool want_z = p.budget > 0.0f;
+    const bool want_z = p.budget > 0.0f && p.strata == 0;   // the uniform sampler's Z is N - k
     const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.tcap;
     // one wave of loads: the tiles' candidate counts and shares of Z (two
     // tiles per thread: at most kMaxTiles tiles) and the candidates' level-2
@@ -391,7 +391,7 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
         sh.r_theta = theta;
         sh.r_cut = (int32_t)idx_cut;
         sh.r_m = m;
-        sh.r_Z = __fadd_rn(hh, ll);
+        sh.r_Z = (p.strata == 1) ? p.z_uniform : __fadd_rn(hh, ll);
     }
 }
 
@@ -424,6 +424,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
     const uint16_t* ub = ws_ubuf(p) + (size_t)u * pl.np + base;
     const float B = p.budget;
     const bool sampling = B > 0.0f;
+    const bool uniform = p.strata == 1;   // every remainder token has the same p: e = 1, Z = N - k
     // Each warp stages its slice kSlice tokens at a time (scores and Philox
     // prefixes, cp.async) into two buffers: the next chunk's copies are in
     // flight while the current one is walked.  The first chunk's copies go
@@ -511,6 +512,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
         for (int w = 0; w < kSelWarps; ++w) zlb += sh.zlb[w];
         zlb *= 0.999f;
     }
+    if (uniform) zlb = p.z_uniform;   // the exact normaliser
     // u >= prefix * 2^-16 >= B e / Z_lb >= p (any Z >= Z_lb): the token cannot be drawn
     const float bound_scale = (zlb > 0.0f) ? __fdiv_ru(B, zlb) : INFINITY;
     SSA_MARK(17);
@@ -575,8 +577,8 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
                 bool keep = above || is_cand;
                 val[q] = above ? INFINITY : sv[q];
                 if (sampling && valid && b1 < f1.bin) {
-                    const float e = expf(__fsub_rn(sv[q], m));
-                    zacc(zh4[q], zl4[q], e);
+                    const float e = uniform ? 1.0f : expf(__fsub_rn(sv[q], m));
+                    if (!uniform) zacc(zh4[q], zl4[q], e);
                     keep = __fmul_ru(e, bound16) > __uint2float_rn(pr[q]);
                     val[q] = e;
                 }

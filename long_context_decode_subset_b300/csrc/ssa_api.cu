@@ -144,6 +144,18 @@ ssa_status check_ws(void* ws, size_t ws_bytes, const ssa::Plan& pl)
 }
 
 bool bad_scalars(int64_t top_k, float budget) { return top_k < 0 || !(budget >= 0.0f); }
+bool bad_strata(int strata, float top_p)
+{
+    return strata < SSA_STRATA_SSA || strata > SSA_STRATA_TOP_P || !(top_p >= 0.0f) || std::isnan(top_p);
+}
+
+// The remainder's sampler: strata 1 keeps every remainder token with
+// p = min(1, B / (N - min(k, N))), i.e. e = 1 and Z = N - min(k, N).
+void set_strata(ssa::Params& p, int strata, int64_t top_k, int64_t N)
+{
+    p.strata = strata == SSA_STRATA_UNIFORM ? 1 : 0;
+    p.z_uniform = (float)(N - std::min<int64_t>(top_k, N));
+}
 bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -511,10 +523,19 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
                       int32_t* count, int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
                       cudaStream_t stream)
 {
+    return ssa_select_strata(s_hat, SSA_STRATA_SSA, top_k, 0.0f, budget, seed, idx, p, count, list_cap, ws, ws_bytes,
+                             shape, stream);
+}
+
+ssa_status ssa_select_strata(const float* s_hat, int strata, int64_t top_k, float top_p, float budget, uint64_t seed,
+                             int32_t* idx, float* p, int32_t* count, int64_t list_cap, void* ws, size_t ws_bytes,
+                             const ssa_shape* shape, cudaStream_t stream)
+{
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!s_hat || !idx || !p || !count) return SSA_ERR_INVALID_ARG;
-    if (bad_scalars(top_k, budget)) return SSA_ERR_INVALID_ARG;
+    if (bad_scalars(top_k, budget) || bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
+    if (strata == SSA_STRATA_TOP_P) return SSA_ERR_UNSUPPORTED;
     const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
@@ -523,6 +544,7 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
     prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
+    set_strata(prm, strata, top_k, shape->ctx_len);
     prm.idx_out = idx;
     prm.p_out = p;
     prm.count_out = count;
@@ -592,7 +614,7 @@ void set_append(ssa::Params& p, const AppendArgs& a, int64_t pos, const ssa_shap
     p.ks_sh = s.ks_stride_h;
 }
 
-ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+ssa_status decode_impl(const AppendArgs* app, int strata, const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                        const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed,
                        float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
                        int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
@@ -619,6 +641,7 @@ ssa_status decode_impl(const AppendArgs* app, const ssa_bf16* q, const ssa_bf16*
     prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
+    set_strata(prm, strata, top_k, shape->ctx_len);
     float* scores = s_hat_opt ? s_hat_opt : reinterpret_cast<float*>(w + pl.o_scores);
     prm.s_dst = scores;
     prm.s_src = scores;
@@ -658,8 +681,20 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
                       float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
 {
-    return decode_impl(nullptr, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt, idx_opt, p_opt,
-                       count_opt, list_cap, ws, ws_bytes, shape, stream);
+    return decode_impl(nullptr, SSA_STRATA_SSA, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt,
+                       idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+}
+
+ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
+                             const int32_t* sel_ch, int strata, int64_t top_k, float top_p, float budget,
+                             uint64_t seed, float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt,
+                             float* p_opt, int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes,
+                             const ssa_shape* shape, cudaStream_t stream)
+{
+    if (bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
+    if (strata == SSA_STRATA_TOP_P) return SSA_ERR_UNSUPPORTED;
+    return decode_impl(nullptr, strata, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt, idx_opt,
+                       p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K,
@@ -672,8 +707,8 @@ ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa
     if (shape->ctx_len < 1 || !k_new || !v_new || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SSA_ERR_INVALID_ARG;
     const AppendArgs app{k_new, v_new, K, V, Ks};
-    return decode_impl(&app, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, nullptr, nullptr, nullptr,
-                       nullptr, 0, ws, ws_bytes, shape, stream);
+    return decode_impl(&app, SSA_STRATA_SSA, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, nullptr,
+                       nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_t* sel_ch, int64_t pos,

@@ -29,7 +29,9 @@ EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
     "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append", "ssa_select_capacity",
+    "ssa_select_strata", "ssa_decode_strata",
 ]
+STRATA_SSA, STRATA_UNIFORM, STRATA_TOP_P = 0, 1, 2
 
 
 class SsaError(RuntimeError):
@@ -72,6 +74,9 @@ def load_library():
         "ssa_decode_append": ([P, P, P, P, P, P, P, i64, f32, u64, f32, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_score": ([P, P, P, f32, P, P, sz, SP, P], ctypes.c_int),
         "ssa_select": ([P, i64, f32, u64, P, P, P, i64, P, sz, SP, P], ctypes.c_int),
+        "ssa_select_strata": ([P, ctypes.c_int, i64, f32, f32, u64, P, P, P, i64, P, sz, SP, P], ctypes.c_int),
+        "ssa_decode_strata": ([P, P, P, P, P, ctypes.c_int, i64, f32, f32, u64, f32, P, P, P, P, P, P, i64, P, sz, SP, P],
+                              ctypes.c_int),
         "ssa_attend": ([P, P, P, P, P, P, i64, f32, P, P, P, sz, SP, P], ctypes.c_int),
         "ssa_decode": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, P, P, P, i64, P, sz, SP, P], ctypes.c_int),
         "ssa_decode_host": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, sz, SP, P], ctypes.c_int),
@@ -208,6 +213,27 @@ def ssa_select(s_hat: torch.Tensor, top_k: int, budget: float, seed: int, idx=No
     return idx, p, count
 
 
+def ssa_select_strata(s_hat: torch.Tensor, strata: int, top_k: int, top_p: float, budget: float, seed: int,
+                      idx=None, p=None, count=None, list_cap: int = 0, ws=None, stream=None):
+    """ssa_select with a choice of strata (STRATA_SSA, STRATA_UNIFORM, STRATA_TOP_P)."""
+    Bt, Hkv, N = s_hat.shape
+    shape = _scores_shape(s_hat)
+    cap = list_cap if list_cap > 0 else max(N, 1)
+    if idx is None:
+        idx = torch.empty((Bt, Hkv, cap), dtype=torch.int32, device=s_hat.device)
+    if p is None:
+        p = torch.empty((Bt, Hkv, cap), dtype=torch.float32, device=s_hat.device)
+    if count is None:
+        count = torch.empty((Bt, Hkv), dtype=torch.int32, device=s_hat.device)
+    if ws is None:
+        ws = workspace(shape, cap, s_hat.device)
+    _check(load_library().ssa_select_strata(_ptr(s_hat), int(strata), int(top_k), float(top_p), float(budget),
+                                            int(seed) & (2**64 - 1), _ptr(idx), _ptr(p), _ptr(count), int(cap),
+                                            _ptr(ws), ws.numel(), ctypes.byref(shape), _stream(stream)),
+           "ssa_select_strata")
+    return idx, p, count
+
+
 def ssa_attend(q, K, V, idx, p, count, scale: float, out=None, lse=None, ws=None, stream=None):
     """Returns (out [Bt][Hq][d] fp32, lse [Bt][Hq] fp32)."""
     shape = shape_of(q, K, d_sel=16)
@@ -241,6 +267,27 @@ def ssa_decode(q, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale:
                                      float(budget), int(seed) & (2**64 - 1), float(scale), _ptr(out),
                                      _ptr(lse), _ptr(s_hat), _ptr(idx), _ptr(p), _ptr(count), int(cap),
                                      _ptr(ws), ws.numel(), ctypes.byref(shape), _stream(stream)), "ssa_decode")
+    return out, lse
+
+
+def ssa_decode_strata(q, K, V, Ks, sel_ch, strata: int, top_k: int, top_p: float, budget: float, seed: int,
+                      scale: float, out=None, lse=None, s_hat=None, idx=None, p=None, count=None, list_cap: int = 0,
+                      ws=None, stream=None):
+    """ssa_decode with a choice of strata; returns (out, lse)."""
+    shape = shape_of(q, K, Ks)
+    Bt, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((Bt, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Bt, Hq), dtype=torch.float32, device=q.device)
+    cap = list_cap if list_cap > 0 else (idx.shape[-1] if idx is not None else 0)
+    if ws is None:
+        ws = workspace(shape, cap, q.device)
+    _check(load_library().ssa_decode_strata(_ptr(q), _ptr(K), _ptr(V), _ptr(Ks), _ptr(sel_ch), int(strata),
+                                            int(top_k), float(top_p), float(budget), int(seed) & (2**64 - 1),
+                                            float(scale), _ptr(out), _ptr(lse), _ptr(s_hat), _ptr(idx), _ptr(p),
+                                            _ptr(count), int(cap), _ptr(ws), ws.numel(), ctypes.byref(shape),
+                                            _stream(stream)), "ssa_decode_strata")
     return out, lse
 
 

@@ -8,9 +8,9 @@ strata": the two baselines it contrasts).
 
 Dense attention is the library's own dense limit (B = +inf), which the
 parity tests pin against the oracle.  The uniform hybrid keeps the same
-top-k stratum and draws every other token with p = B / (N - k) (host
-draws, seeded), attended through ssa_attend.  The numbers are printed as
-one JSON line; the assertions are only sanity bounds.
+top-k stratum and draws every other token with p = B / (N - k), with the
+same Philox uniforms (the library's SSA_STRATA_UNIFORM).  The numbers are
+printed as one JSON line; the assertions are only sanity bounds.
 """
 import json
 import math
@@ -50,26 +50,8 @@ def test_error_vs_dense_statistic():
         s_hat = torch.empty((Bt, Hkv, N), dtype=torch.float32, device=DEV)
         out_ssa, _ = ssa.ssa_decode(q, K, V, Ks, sel, k, B, seed, cfg.scale, s_hat=s_hat)
         out_topk, _ = ssa.ssa_decode(q, K, V, Ks, sel, k + int(B), 0.0, seed, cfg.scale)
-        # top-k stratum of the same scores (score desc, index asc) + uniform draws
-        rng = np.random.default_rng(1_000_003 * seed + 17)
-        s_np = s_hat.cpu().numpy()
-        pu = float(B) / float(N - k)
-        idx = np.zeros((Bt, Hkv, N), np.int32)
-        p = np.zeros((Bt, Hkv, N), np.float32)
-        count = np.zeros((Bt, Hkv), np.int32)
-        ar = np.arange(N)
-        for b in range(Bt):
-            for h in range(Hkv):
-                order = np.lexsort((ar, -s_np[b, h].astype(np.float64)))
-                in_t = np.zeros(N, bool)
-                in_t[order[:k]] = True
-                keep = in_t | (rng.random(N) < pu)
-                rows = np.nonzero(keep)[0]
-                idx[b, h, :rows.size] = rows
-                p[b, h, :rows.size] = np.where(in_t[rows], 1.0, pu)
-                count[b, h] = rows.size
-        idx, p, count = (torch.from_numpy(x).to(DEV) for x in (idx, p, count))
-        out_uh, _ = ssa.ssa_attend(q, K, V, idx, p, count, cfg.scale)
+        # the top-k + uniform hybrid at the same budget, drawn by the library (SSA_STRATA_UNIFORM)
+        out_uh, _ = ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.ssa.STRATA_UNIFORM, k, 0.0, B, seed, cfg.scale)
         torch.cuda.synchronize()
         errs["ssa"].append(_rel_err(out_ssa, dense))
         errs["topk"].append(_rel_err(out_topk, dense))

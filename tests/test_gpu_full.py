@@ -149,3 +149,20 @@ def test_full_size_attend_given_oracle_lists(oracle_mod, name):
         assert np.allclose(lg, lse_o, atol=2e-3, rtol=2e-3), (b, h, np.abs(lg - lse_o).max())
         worst = max(worst, float(np.abs(og - out_o).max()))
     print(f"{name}: every unit within 2e-3, max |out - oracle| = {worst:.2e}")
+
+
+def test_full_size_uniform_hybrid_given_oracle_scores(oracle_mod):
+    """The top-k + uniform hybrid at the 128K workload in the automatic plan: identical lists, p bit for bit."""
+    cfg = workloads.CONFIGS["ministral8b_128k"]
+    seed = 6
+    w = workloads.generate(cfg, 0, "cuda")
+    s_np = _oracle_scores(oracle_mod, w, cfg)
+    del w
+    idx, p, count = ssa.ssa_select_strata(torch.from_numpy(s_np).cuda(), ssa.ssa.STRATA_UNIFORM, cfg.top_k, 0.0,
+                                          cfg.budget, seed)
+    idx, p, count = idx.cpu().numpy(), p.cpu().numpy(), count.cpu().numpy()
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            o_idx, o_p = oracle_mod.select_unit_uniform(s_np[b, h], cfg.top_k, cfg.budget, seed, b, h)
+            n = int(count[b, h])
+            assert np.array_equal(idx[b, h, :n], o_idx) and np.array_equal(p[b, h, :n], o_p), (b, h)

@@ -228,3 +228,86 @@ def test_select_flags_nonfinite_scores(bad):
         n = int(c[0, h])
         ids = idx[0, h, :n].cpu()
         assert torch.all((ids >= 0) & (ids < 1000))
+
+
+def _uniform_p_all(oracle_mod, s_unit, k, B):
+    """The uniform hybrid's inclusion probability of every token, from the oracle's own top-k stratum
+    (1 on T, min(1, fl32(B / fl32(N - |T|))) on the remainder)."""
+    N = s_unit.size
+    t_idx = oracle_mod.select_unit(s_unit, k, 0.0, 0, 0, 0)[0]
+    p_all = np.empty(N, np.float32)
+    n_r = N - t_idx.size
+    p_all[:] = 1.0 if (n_r == 0 or math.isinf(B)) else min(np.float32(1.0), np.float32(np.float32(B) / np.float32(n_r)))
+    p_all[t_idx] = 1.0
+    return p_all
+
+
+def _select_uniform_and_compare(oracle_mod, s_np, k, B, seed, tile=None, split=None):
+    s = torch.from_numpy(s_np).to(DEV)
+    Bt, Hkv, N = s_np.shape
+    with plan_env(tile, split):
+        idx, p, count = ssa.ssa_select_strata(s, ssa.ssa.STRATA_UNIFORM, k, 0.0, B, seed)
+    torch.cuda.synchronize()
+    idx, p, count = idx.cpu().numpy(), p.cpu().numpy(), count.cpu().numpy()
+    for b in range(Bt):
+        for h in range(Hkv):
+            o_idx, o_p = oracle_mod.select_unit_uniform(s_np[b, h], k, B, seed, b, h)
+            n = int(count[b, h])
+            # the same Philox uniforms against the same fp32 p: identical lists, p bit for bit
+            assert np.array_equal(idx[b, h, :n], o_idx), (b, h, n, o_idx.size)
+            assert np.array_equal(p[b, h, :n], o_p), (b, h)
+
+
+@pytest.mark.parametrize("tile,split", [(None, None), (512, 1), (1024, 3), (4096, 2)])
+def test_select_uniform_hybrid_parity(oracle_mod, tile, split):
+    """The top-k + uniform hybrid (SSA_STRATA_UNIFORM) against the oracle's select_unit_uniform, given the
+    oracle's scores, over several tilings."""
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
+    _select_uniform_and_compare(oracle_mod, s_np, cfg.top_k, cfg.budget, 7, tile, split)
+
+
+def test_select_uniform_hybrid_edge_cases(oracle_mod):
+    rng = np.random.default_rng(21)
+    for N, k, B, kind in [(3000, 40, 40.0, "ties"), (3000, 40, 40.0, "constant"), (2500, 0, 30.0, "normal"),
+                          (2500, 25, 0.0, "normal"), (700, 699, 10.0, "normal"), (4097, 60, 1e6, "normal"),
+                          (513, 5, 5.0, "signed_zero")]:
+        if kind == "ties":
+            s = np.round(rng.standard_normal((1, 2, N)) * 2) / 4
+        elif kind == "constant":
+            s = np.full((1, 2, N), 0.375)
+        elif kind == "signed_zero":
+            s = np.where(rng.random((1, 2, N)) < 0.5, 0.0, -0.0) * np.ones((1, 2, N))
+        else:
+            s = rng.standard_normal((1, 2, N)) * 1.5
+        _select_uniform_and_compare(oracle_mod, s.astype(np.float32), k, B, 4)
+
+
+def test_decode_uniform_hybrid_parity(oracle_mod):
+    """The whole step with the uniform hybrid: the selection against the oracle's hybrid on the oracle's
+    scores (boundary cases at the top-k edge excepted), the output against the oracle's attention over the
+    oracle's lists."""
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    Bt, Hkv, N = cfg.batch, cfg.n_kv_heads, cfg.ctx_len
+    G = cfg.group
+    idx = torch.empty((Bt, Hkv, N), dtype=torch.int32, device=DEV)
+    p = torch.empty((Bt, Hkv, N), dtype=torch.float32, device=DEV)
+    count = torch.empty((Bt, Hkv), dtype=torch.int32, device=DEV)
+    out, lse = ssa.ssa_decode_strata(w["q"], w["K"], w["V"], w["Ks"], w["sel_ch"], ssa.ssa.STRATA_UNIFORM,
+                                     cfg.top_k, 0.0, cfg.budget, 9, cfg.scale, idx=idx, p=p, count=count)
+    s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
+    for b in range(Bt):
+        for h in range(Hkv):
+            o_idx, o_p = oracle_mod.select_unit_uniform(s_np[b, h], cfg.top_k, cfg.budget, 9, b, h)
+            n = int(count[b, h])
+            g_idx = idx[b, h, :n].cpu().numpy()
+            assert len(set(g_idx.tolist()) ^ set(o_idx.tolist())) <= 2
+            out_o, lse_o = oracle_mod.attend_unit(q[b, h * G:(h + 1) * G], K[b, h], V[b, h], g_idx,
+                                                  _uniform_p_all(oracle_mod, s_np[b, h], cfg.top_k, cfg.budget)[g_idx],
+                                                  cfg.scale)
+            assert np.allclose(out[b, h * G:(h + 1) * G].cpu().numpy(), out_o, atol=2e-3, rtol=2e-3)
+            assert np.allclose(lse[b, h * G:(h + 1) * G].cpu().numpy(), lse_o, atol=2e-3, rtol=2e-3)
