@@ -12,8 +12,11 @@ Prints one JSON line (rank 0): value (us per step), roofline (the score
 pass alone against the measured copy bandwidth, with the DRAM traffic
 recorded for these kernel sources), e2e (through ssa_decode_host, host
 memory in and out), append_step (ssa_decode_append, the serving form),
-secondary (the 1M-context workload), cpu_baseline (the oracle on the host
-cores) and cpu_dense (dense attention on the same cores).  --impl reference
+secondary (the 1M-context workload), configs (the 32K workload and the 27B
+sweep points: us per step, achieved GB/s and roofline fraction each),
+host_tier (the 32K step with K/V in pinned host memory), cpu_baseline (the
+oracle on the host cores) and cpu_dense (dense attention on the same
+cores).  --impl reference
 times the CPU oracle instead (the reference arm for this method has no
 runnable upstream code).
 """
@@ -49,6 +52,10 @@ def parse_args():
     ap.add_argument("--secondary", default="ministral8b_1m", help="second workload reported beside ('' = none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default="ministral8b_32k,27b_128k_10x,27b_128k_20x,27b_128k_50x,27b_128k_100x,"
+                    "27b_128k_dense", help="further workloads timed for the per-config records ('' = none)")
+    ap.add_argument("--host-tier", default="ministral8b_32k",
+                    help="workload timed with K/V in pinned host memory ('' = none)")
     return ap.parse_args()
 
 
@@ -365,6 +372,58 @@ def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
     return res
 
 
+def time_steps(cfg, steps: int, warmup: int, dev, host_kv: bool = False):
+    """Mean us per ssa_decode step of workload `cfg` (L2 flushed before every step, seed = step index) and
+    the mean rows selected; with host_kv the K and V rows sit in pinned host memory."""
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    w = workloads.generate(cfg, 0, dev)
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    q, K, V, sel = w["q"], w["K"], w["V"], w["sel_ch"]
+    if host_kv:
+        K, V = K.cpu().pin_memory(), V.cpu().pin_memory()
+        del w["K"], w["V"]
+    shape = ssa.shape_of(q, K, Ks)
+    ws = ssa.workspace(shape, 0, dev)
+    out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((cfg.batch, cfg.n_q_heads), dtype=torch.float32, device=dev)
+    counts = torch.zeros((steps, cfg.units), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        flush.fill_(i & 0xff)
+        ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, 1_000_000 + i, cfg.scale, out=out, lse=lse, ws=ws,
+                       stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(20_000_000)
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, out=out, lse=lse, count=counts[i],
+                           ws=ws, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    rows = counts.sum(dim=1).double().mean().item()
+    return us, rows, clk.summary()
+
+
+def config_record(cfg, us, rows, peak, clocks):
+    ab = algorithmic_bytes(cfg, rows)
+    gbs = ab / (us * 1e-6) / 1e9
+    return {"workload": cfg.name, "value": round(us, 3), "unit": UNIT, "rows_selected_per_step": round(rows, 1),
+            "algorithmic_bytes_per_step": int(ab), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "frac_of_8000": round(gbs / 8000.0, 4), "clocks": clocks}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -438,7 +497,8 @@ def run_ours(args):
         "aggregate_steps_per_s": round(rep["aggregate_steps_per_s"], 1),
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": m["h2d"],
                 "aggregate_steps_per_s": round(rep["aggregate_e2e_steps_per_s"], 1),
-                "d2h_bytes_per_step": m["d2h"], "api": "ssa_decode_host (pinned host q in, out/lse back)"},
+                "d2h_bytes_per_step": m["d2h"],
+                "api": "ssa_decode_host: the kernels read q from pinned host memory and write out/lse into it"},
         "append_step": {"value": round(statistics.fmean(m["append_us"]), 3), "unit": UNIT,
                         "api": "ssa_decode_append (the new token's K/V and summary rows written by the chain's "
                                "first kernel, then the step over all tokens)"},
@@ -464,6 +524,29 @@ def run_ours(args):
         del m2
         torch.cuda.empty_cache()
         m = None
+    if rank == 0 and args.sweep:
+        # the other workloads' steps (the per-config records of the measurement plan)
+        line["configs"] = []
+        for name in [x for x in args.sweep.split(",") if x]:
+            cfgx = workloads.CONFIGS[name]
+            steps_x = max(20, min(args.steps, 200))
+            us, rows, clk = time_steps(cfgx, steps_x, max(3, min(args.warmup, 10)), dev)
+            rec = config_record(cfgx, us, rows, peak, clk)
+            rec["steps"] = steps_x
+            line["configs"].append(rec)
+            torch.cuda.empty_cache()
+    if rank == 0 and args.host_tier:
+        # the host-resident tier: K and V in pinned host memory, the summary in HBM; the selected rows cross
+        # the host link
+        cfgh = workloads.CONFIGS[args.host_tier]
+        steps_h = max(20, min(args.steps, 100))
+        us, rows, clk = time_steps(cfgh, steps_h, 3, dev, host_kv=True)
+        rec = config_record(cfgh, us, rows, peak, clk)
+        rec.update(steps=steps_h, kv="pinned host memory (mapped), summary in HBM",
+                   row_bytes_per_step=int(rows * cfgh.head_dim * 2 * 2),
+                   host_link_gbs=round(rows * cfgh.head_dim * 4 / (us * 1e-6) / 1e9, 1))
+        line["host_tier"] = rec
+        torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle as it stands, on this host's cores, on a bounded sample of the same workload
         w = workloads.generate(cfg, 0, dev)

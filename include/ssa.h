@@ -61,6 +61,17 @@
  *
  * K, V and Ks may be NULL when ctx_len == 0 (nothing is read).
  *
+ * Memory tiers ("FASA: Frequency-Aware Sparse Attention", section 3,
+ * Variants, FASA-M: the dominant-channel summary stays in GPU memory while
+ * the full K and V rows are offloaded to host memory and fetched for the
+ * selected tokens only): K and V may be pinned host memory mapped into the
+ * device's address space at the same address (cudaHostAlloc /
+ * cudaHostRegister on a device with unified addressing); the step then
+ * gathers the selected rows over the host link and streams the summary from
+ * HBM as usual.  q, Ks, the workspace and the outputs must be device memory.
+ * Pageable host memory (and any pointer the device cannot read) is refused
+ * with SSA_ERR_INVALID_ARG before anything is launched.
+ *
  * Memory and ownership: every buffer, the workspace included, is allocated
  * and owned by the caller.  Device pointers unless stated otherwise.  The
  * library allocates no device memory (ssa_decode_static's built-in array,
@@ -262,10 +273,13 @@ ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa
                              const ssa_shape* shape, cudaStream_t stream);
 
 /* ssa_decode with the step's query read from, and its result written to,
- * HOST memory (pinned for asynchrony): copies q_host to a device staging
- * area inside the workspace, runs the step, and copies out / lse back to
- * out_host / lse_host, all enqueued on `stream`.  The caller synchronises.
- * The KV cache (K, V, Ks, sel_ch) stays resident on the device. */
+ * HOST memory, all on `stream`; the caller synchronises.  When q_host,
+ * out_host and lse_host are pinned and mapped into the device's address
+ * space (cudaHostAlloc / cudaHostRegister with unified addressing), the
+ * kernels read q and write out / lse there directly and no copy is enqueued;
+ * otherwise (pageable buffers) q is copied to a staging area inside the
+ * workspace, the step runs, and out / lse are copied back.  The KV cache
+ * (K, V, Ks, sel_ch) stays where it is (see the memory tiers above). */
 ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_bf16* V,
                            const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
                            uint64_t seed, float scale, float* out_host, float* lse_host,

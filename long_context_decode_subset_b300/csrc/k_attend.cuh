@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     if (warp == 4 && p.attend) tmem_alloc(&misc[0], CF::TCOLS);
     // the query operand: head slot n < G = q_n (the scale is applied to S),
-    // slots G..15 zero; K-major, 128-byte swizzle, two 64-dim planes
+    // slots G..15 zero; K-major, 128-byte swizzle, two 64-dim planes (a query
+    // the chain's first kernel stages is read after the wait for it)
+    if (p.q_staged) grid_dep_wait();
     if (tid < 256) {
         const int n = tid >> 4, pc = tid & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);

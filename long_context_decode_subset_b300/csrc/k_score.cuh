@@ -47,6 +47,8 @@ struct Params {
     int32_t attend;            // K2 computes attention (else it only writes the compact list)
     int32_t src_mode;          // K2 rows: 0 the selection, 1 all tokens, 2 the caller's compact list
     int32_t strata;            // the remainder's sampler: 0 p proportional to exp(s), 1 uniform
+    int32_t q_staged;          // q is copied from q_host into the workspace by K0: read it after the wait
+    const uint16_t* q_host;    // the step's query in pinned host memory (q_staged), [Bt][Hq][d]
     float z_uniform;           // strata 1: the remainder's size N - min(k, N) as fp32
     const uint16_t* q;         // [Bt][Hq][d]
     const uint16_t* K;         // [Bt][Hkv][N][d] with the strides below
@@ -138,6 +140,14 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
     const int u = blockIdx.x;
     const int tid = threadIdx.x;
     if (p.k_new != nullptr) append_unit(p, u, tid, 256);   // read by K1 only after its wait for this grid
+    if (p.q_staged) {
+        // the unit's G query rows from pinned host memory into the workspace
+        // copy every later kernel reads (after its wait for this grid)
+        const int G = p.Hq / p.Hkv, b = u / p.Hkv, h = u % p.Hkv;
+        const int64_t off = ((int64_t)b * p.Hq + (int64_t)h * G) * p.d;
+        for (int i = tid; i < G * p.d / 8; i += 256)
+            reinterpret_cast<uint4*>(const_cast<uint16_t*>(p.q) + off)[i] = reinterpret_cast<const uint4*>(p.q_host + off)[i];
+    }
     uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
     if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
     uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);
@@ -352,6 +362,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
         const int64_t g0 = st * blockIdx.x / gridDim.x;
         if (g0 < st * (blockIdx.x + 1) / gridDim.x) {
             first_u = (int)(g0 / pl.sf);
+            if (p.q_staged) grid_dep_wait();   // K0 copies the query into the workspace
             fetch_q(first_u);
         }
     }

@@ -143,6 +143,23 @@ ssa_status check_ws(void* ws, size_t ws_bytes, const ssa::Plan& pl)
     return SSA_OK;
 }
 
+// Whether the device can read `ptr` directly: device (or managed) memory, or
+// pinned host memory mapped into the device's address space at the same
+// address (the K/V rows of the host-resident memory tier).  Pageable host
+// memory is refused: a kernel reading it would fault.  `host_ok` false
+// refuses host memory as well.
+bool device_readable(const void* ptr, bool host_ok)
+{
+    if (!ptr) return true;   // null pointers are checked where they matter
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return host_ok && a.type == cudaMemoryTypeHost && a.devicePointer == ptr;
+}
+
 bool bad_scalars(int64_t top_k, float budget) { return top_k < 0 || !(budget >= 0.0f); }
 bool bad_strata(int strata, float top_p)
 {
@@ -572,6 +589,7 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     if (bad_scale(scale)) return SSA_ERR_INVALID_ARG;
     const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (!device_readable(K, true) || !device_readable(V, true) || !device_readable(q, false)) return SSA_ERR_INVALID_ARG;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
     prm.q = q;
@@ -614,7 +632,8 @@ void set_append(ssa::Params& p, const AppendArgs& a, int64_t pos, const ssa_shap
     p.ks_sh = s.ks_stride_h;
 }
 
-ssa_status decode_impl(const AppendArgs* app, int strata, const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+ssa_status decode_impl(const AppendArgs* app, int strata, bool host_io, const ssa_bf16* q, const ssa_bf16* K,
+                       const ssa_bf16* V,
                        const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed,
                        float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
                        int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
@@ -629,11 +648,21 @@ ssa_status decode_impl(const AppendArgs* app, int strata, const ssa_bf16* q, con
     if ((idx_opt == nullptr) != (p_opt == nullptr)) return SSA_ERR_INVALID_ARG;
     const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    // K and V may sit in pinned host memory (the host-resident tier); the
+    // summary the score kernel streams, and the query, live on the device
+    if (!device_readable(K, true) || !device_readable(V, true) || !device_readable(Ks, false) ||
+        !device_readable(q, host_io) || !device_readable(out, host_io) || !device_readable(lse, host_io))
+        return SSA_ERR_INVALID_ARG;
     if (pl.U == 0) return SSA_OK;
     char* w = static_cast<char*>(ws);
     ssa::Params prm = base_params(*shape, pl, ws);
     if (!empty && (st = encode_summary_map(&prm.ks_map, Ks, *shape)) != SSA_OK) return st;
     prm.q = q;
+    if (host_io) {   // the first kernel stages the query from host memory into the workspace
+        prm.q = reinterpret_cast<const ssa_bf16*>(w + pl.o_hq);
+        prm.q_host = q;
+        prm.q_staged = 1;
+    }
     prm.K = K;
     prm.V = V;
     prm.sel_ch = sel_ch;
@@ -666,7 +695,7 @@ ssa_status decode_impl(const AppendArgs* app, int strata, const ssa_bf16* q, con
     // appended token); a step that keeps every token and wants no scores
     // runs the unit kernel alone
     const bool score = !empty && (!prm.dense || s_hat_opt);
-    const bool init = score || app;
+    const bool init = score || app || host_io;
     if (init && (st = launch_init(prm, stream)) != SSA_OK) return st;
     if (score && (st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
     return launch_unit(prm, *shape, stream, init);
@@ -681,8 +710,8 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
                       float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
 {
-    return decode_impl(nullptr, SSA_STRATA_SSA, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt,
-                       idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+    return decode_impl(nullptr, SSA_STRATA_SSA, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+                       s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
@@ -693,8 +722,8 @@ ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
 {
     if (bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
     if (strata == SSA_STRATA_TOP_P) return SSA_ERR_UNSUPPORTED;
-    return decode_impl(nullptr, strata, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt, idx_opt,
-                       p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+    return decode_impl(nullptr, strata, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt,
+                       idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K,
@@ -707,8 +736,8 @@ ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa
     if (shape->ctx_len < 1 || !k_new || !v_new || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SSA_ERR_INVALID_ARG;
     const AppendArgs app{k_new, v_new, K, V, Ks};
-    return decode_impl(&app, SSA_STRATA_SSA, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, nullptr,
-                       nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
+    return decode_impl(&app, SSA_STRATA_SSA, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+                       nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_t* sel_ch, int64_t pos,
@@ -737,6 +766,12 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     ssa_status st = check_shape(shape);
     if (st != SSA_OK) return st;
     if (!q_host || !out_host || !lse_host) return SSA_ERR_INVALID_ARG;
+    // pinned, mapped buffers: the kernels read q from host memory and write
+    // out / lse into it (no copy is enqueued)
+    if (device_readable(q_host, true) && device_readable(out_host, true) && device_readable(lse_host, true))
+        return decode_impl(nullptr, SSA_STRATA_SSA, true, q_host, K, V, Ks, sel_ch, top_k, budget, seed, scale,
+                           out_host, lse_host, nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
+    // otherwise one staged copy in, the step, two staged copies out
     const ssa::Plan pl = make_plan(*shape, 0);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     char* w = static_cast<char*>(ws);

@@ -126,6 +126,15 @@ def test_decode_host_matches_device_path():
                         out_h, lse_h, ws)
     torch.cuda.synchronize()
     assert torch.equal(out_h, g["out"].cpu()) and torch.equal(lse_h, g["lse"].cpu())
+    # pageable host buffers take the staged-copy path: the same results
+    q_p = w["q"].cpu()
+    out_p = torch.full(g["out"].shape, float("nan"))
+    lse_p = torch.full(g["lse"].shape, float("nan"))
+    assert not q_p.is_pinned()
+    ssa.ssa_decode_host(q_p, w["K"], w["V"], w["Ks"], w["sel_ch"], cfg.top_k, cfg.budget, 9, cfg.scale,
+                        out_p, lse_p, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, g["out"].cpu()) and torch.equal(lse_p, g["lse"].cpu())
 
 
 def test_strided_cache_layout(oracle_mod):
