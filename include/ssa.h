@@ -127,8 +127,12 @@ typedef enum {
                                 p = min(1, fl32(B / fl32(N - min(k, N)))) (1 for B = +inf):
                                 the top-k + uniform-sampling hybrid */
     SSA_STRATA_TOP_P = 2     /* top-p stratum: the fewest tokens, in the top-k order, whose share
-                                of the softmax of s over all N tokens reaches top_p; the
-                                remainder drawn as in SSA_STRATA_SSA */
+                                of the softmax of s over all N tokens reaches top_p (none for
+                                top_p <= 0, all for top_p >= 1); the remainder drawn as in
+                                SSA_STRATA_SSA with k = that size.  The shares are summed from
+                                fp32 expf terms in exact fixed point (63 fractional bits), so a
+                                size can differ by one from an exact computation only where the
+                                top_p falls within a few fp32 roundings of a token's boundary */
 } ssa_strata;
 
 /* Device status bits (ssa_get_device_status). */
@@ -215,8 +219,7 @@ ssa_status ssa_select(const float* s_hat, int64_t top_k, float budget, uint64_t 
 
 /* ssa_select with a choice of strata (ssa_strata; top_p is read for
  * SSA_STRATA_TOP_P only, top_k for the others).  The same Philox uniforms
- * decide every draw.  SSA_STRATA_TOP_P is declared but not built: it returns
- * SSA_ERR_UNSUPPORTED.  An unknown strata or a negative or NaN top_p is
+ * decide every draw.  An unknown strata or a negative or NaN top_p is
  * SSA_ERR_INVALID_ARG. */
 ssa_status ssa_select_strata(const float* s_hat, int strata, int64_t top_k, float top_p, float budget,
                              uint64_t seed, int32_t* idx, float* p, int32_t* count, int64_t list_cap,

@@ -61,6 +61,11 @@ constexpr int kSelThreads = 512;       // K2 block size; in the selection each w
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kInThreads = 256;        // score_input_kernel block size
 constexpr int kQselBytes = 1024;       // B operand: 16 rows x d_sel bf16, swizzled
+// top-p stratum: per unit, mass and count histograms of three radix levels
+// (12, 12 and 8 key bits), each bin three 64-bit words (mass high part, mass
+// low part, count)
+constexpr int kTopPBins = 4096 + 4096 + 256;
+constexpr size_t kTopPUnitBytes = (size_t)kTopPBins * 3 * 8;
 
 // Per-unit control block (zeroed by K0).
 struct UnitCtrl {
@@ -68,7 +73,8 @@ struct UnitCtrl {
     uint32_t k1_next;    // unit 0 only: K1's shared stage queue (stages taken)
     uint32_t karrive;    // K2 CTAs whose kept count is written
     uint32_t done;       // K2 CTAs whose attention partial is written
-    uint32_t pad[12];
+    uint32_t tp_arrive[3];   // top-p stratum: K2 tiles whose mass counts of level 0 / 1 / 2 are added
+    uint32_t pad[9];
 };
 static_assert(sizeof(UnitCtrl) == 64, "control block is 64 bytes");
 
@@ -88,7 +94,7 @@ struct Plan {
     // workspace byte offsets
     int32_t tcap;        // tiles the per-tile arrays hold per unit (>= ntile)
     size_t o_status, o_ctrl, o_hist1, o_zpart, o_kcnt, o_part, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
-        o_hout, o_hlse, total;
+        o_hout, o_hlse, o_topp, total;
 };
 
 // ---------------------------------------------------------------------------

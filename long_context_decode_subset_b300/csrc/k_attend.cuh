@@ -278,7 +278,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     int64_t lo = 0, hi = 0;
     if (p.src_mode == 0) {
         SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
-        const TileSel ts = tile_pass(p, u, r, sh, smem);
+        // the stratum's size: k, or (top-p) found from the unit's score masses
+        const uint32_t k_unit = (p.strata == 2) ? topp_size(p, u, r, sh, smem)
+                                                : (uint32_t)min(p.top_k, (int64_t)0xffffffff);
+        const TileSel ts = tile_pass(p, u, r, k_unit, sh, smem);
         if (tid == 0) {
             uint32_t run = 0;
             for (int w = 0; w < kSelWarps; ++w) {

@@ -46,7 +46,8 @@ struct Params {
     int32_t dense;             // every token selected with p = 1 (top_k >= N or budget = +inf)
     int32_t attend;            // K2 computes attention (else it only writes the compact list)
     int32_t src_mode;          // K2 rows: 0 the selection, 1 all tokens, 2 the caller's compact list
-    int32_t strata;            // the remainder's sampler: 0 p proportional to exp(s), 1 uniform
+    int32_t strata;            // 0 top-k + p proportional to exp(s), 1 top-k + uniform, 2 top-p + p proportional to exp(s)
+    float top_p;               // strata 2: the stratum's share of the softmax of the scores
     int32_t q_staged;          // q is copied from q_host into the workspace by K0: read it after the wait
     const uint16_t* q_host;    // the step's query in pinned host memory (q_staged), [Bt][Hq][d]
     float z_uniform;           // strata 1: the remainder's size N - min(k, N) as fp32
@@ -90,6 +91,7 @@ __device__ __forceinline__ uint32_t* ws_hist2(const Params& p) { return ws_hist1
 __device__ __forceinline__ float2* ws_zpart(const Params& p) { return reinterpret_cast<float2*>(p.ws + p.pl.o_zpart); }
 __device__ __forceinline__ uint32_t* ws_kcnt(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_kcnt); }
 __device__ __forceinline__ float* ws_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_part); }
+__device__ __forceinline__ unsigned long long* ws_topp(const Params& p) { return reinterpret_cast<unsigned long long*>(p.ws + p.pl.o_topp); }
 __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_cand); }
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
@@ -155,6 +157,10 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
     for (int i = tid; i < kBins / 4; i += 256) {
         h1[i] = make_uint4(0, 0, 0, 0);
         h2[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (p.strata == 2) {   // the top-p stratum's mass histograms
+        uint4* t = reinterpret_cast<uint4*>(ws_topp(p) + (size_t)u * kTopPBins * 3);
+        for (int i = tid; i < (int)(kTopPUnitBytes / 16); i += 256) t[i] = make_uint4(0, 0, 0, 0);
     }
 }
 

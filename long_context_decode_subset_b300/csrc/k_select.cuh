@@ -55,6 +55,9 @@ struct SelShared {
     unsigned long long zi[kSelWarps][2];
     uint32_t coff[kMaxTiles + 1];   // per-tile candidate offsets
     uint32_t wcnt[kSelWarps];       // the tile pass: list length of each warp slice
+    double dscan[kSelWarps];        // the top-p select: the warps' mass sums
+    double pick_m[2];               // ... the crossing bin's mass above and its own
+    uint32_t pick_u[3];             // ... the crossing bin, the tokens above, its own
     // the resolve's results: order key of the k-th score, the tie cut, m and Z
     uint32_t r_theta;
     int32_t r_cut;
@@ -197,7 +200,7 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
-    const bool want_z = p.budget > 0.0f && p.strata == 0;   // the uniform sampler's Z is N - k
+    const bool want_z = p.budget > 0.0f && p.strata != 1;   // the uniform sampler's Z is N - k
     const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.tcap;
     // one wave of loads: the tiles' candidate counts and shares of Z (two
     // tiles per thread: at most kMaxTiles tiles) and the candidates' level-2
@@ -396,6 +399,263 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
 }
 
 // ---------------------------------------------------------------------------
+// The top-p stratum's size
+// ---------------------------------------------------------------------------
+// ("Stratified Sparse Attention speeds up decoding 2.96x on a 1M context",
+// section "How SSA splits the cache into strata": top-p is a special case of
+// the deterministic stratum.)  The stratum is the fewest tokens, taken in the
+// top-k order (order key desc, index asc), whose share of sum_j exp(s_j) over
+// all N tokens reaches top_p.  Its size is found by a mass-weighted radix
+// select across the unit's tiles: every tile adds, per bin of the current
+// radix level, its tokens' count and their terms w = expf(s - M) (M above
+// every score, so w <= 1) as exact fixed point -- w * 2^63 truncated to an
+// integer, split into two 32-bit halves summed in 64-bit words, so the sums
+// are exact and independent of order -- to the unit's histogram; once every
+// tile has arrived, each CTA finds the first bin from the top whose
+// cumulative mass reaches the remaining target.  Three levels (12, 12 and 8
+// key bits) leave the key of the crossing token; its ties have equal terms,
+// so the number of them the stratum needs is a division.
+
+struct MassPick {
+    uint32_t bin;          // the crossing bin
+    uint32_t count_above;  // tokens in higher bins
+    uint32_t count_bin;    // tokens in the crossing bin
+    double mass_above;     // mass of the higher bins
+    double mass_bin;       // mass of the crossing bin
+    double total;          // mass of every bin
+};
+
+// The bin, from the top of the unit's NB-bin mass histogram h ([3][NB]
+// words: high part, low part, count), whose cumulative mass first reaches
+// the target: `target` times the histogram's total when `frac` is set, else
+// `target` itself (if rounding leaves it unreached, the lowest non-empty
+// bin).  Block-wide (kSelThreads); every thread returns it.
+template <int NB>
+__device__ MassPick mass_pick(const unsigned long long* h, double target, bool frac, SelShared& sh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int CH = NB >= kSelThreads ? NB / kSelThreads : 1;
+    constexpr double kHiUnit = 1.0 / 2147483648.0;            // 2^-31: one unit of the high part
+    constexpr double kLoUnit = kHiUnit / 4294967296.0;       // 2^-63
+    double wm[CH];
+    uint32_t wc[CH];
+    double lm = 0.0;
+    uint32_t lc = 0, deepest = 0;   // deepest: 1 + the lowest non-empty position of this thread (0: none)
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+        const int pos = tid * CH + j;   // pos-th bin from the top
+        wm[j] = 0.0;
+        wc[j] = 0u;
+        if (pos < NB) {
+            const int bin = NB - 1 - pos;
+            wm[j] = (double)__ldcg(h + bin) * kHiUnit + (double)__ldcg(h + NB + bin) * kLoUnit;
+            wc[j] = (uint32_t)__ldcg(h + 2 * NB + bin);
+            if (wc[j]) deepest = (uint32_t)pos + 1u;
+        }
+        lm += wm[j];
+        lc += wc[j];
+    }
+    double xm = lm;
+    uint32_t xc = lc, dmax = deepest;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double ym = __shfl_up_sync(0xffffffffu, xm, o);
+        const uint32_t yc = __shfl_up_sync(0xffffffffu, xc, o);
+        if (lane >= o) {
+            xm += ym;
+            xc += yc;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dmax = max(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+    if (lane == 31) {
+        sh.dscan[warp] = xm;
+        sh.scan[warp] = xc;
+    }
+    if (lane == 0) sh.wcnt[warp] = dmax;
+    if (tid == 0) sh.pick_u[0] = 0xffffffffu;
+    __syncthreads();
+    double em = 0.0, total = 0.0;
+    uint32_t ec = 0;
+    dmax = 0;
+    for (int w = 0; w < kSelWarps; ++w) {
+        if (w < warp) {
+            em += sh.dscan[w];
+            ec += sh.scan[w];
+        }
+        total += sh.dscan[w];
+        dmax = max(dmax, sh.wcnt[w]);
+    }
+    em += xm - lm;   // exclusive prefix of this thread's bins
+    ec += xc - lc;
+    const double tgt = frac ? target * total : target;
+    if (lc > 0 && em < tgt && tgt <= em + lm) {
+        double cum = em;
+        uint32_t cc = ec;
+        bool done = false;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (!done && wc[j] > 0 && cum + wm[j] >= tgt) {
+                sh.pick_u[0] = (uint32_t)(NB - 1 - (tid * CH + j));
+                sh.pick_u[1] = cc;
+                sh.pick_u[2] = wc[j];
+                sh.pick_m[0] = cum;
+                sh.pick_m[1] = wm[j];
+                done = true;
+            }
+            cum += wm[j];
+            cc += wc[j];
+        }
+    }
+    __syncthreads();
+    if (sh.pick_u[0] == 0xffffffffu && dmax > 0 && (int)(dmax - 1) / CH == tid) {
+        // unreached: the lowest non-empty bin (this thread holds it)
+        const int pos = (int)dmax - 1, jl = pos % CH;
+        double cum = em;
+        uint32_t cc = ec;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (j == jl) {
+                sh.pick_u[0] = (uint32_t)(NB - 1 - pos);
+                sh.pick_u[1] = cc;
+                sh.pick_u[2] = wc[j];
+                sh.pick_m[0] = cum;
+                sh.pick_m[1] = wm[j];
+            }
+            cum += wm[j];
+            cc += wc[j];
+        }
+    }
+    __syncthreads();
+    MassPick r{sh.pick_u[0], sh.pick_u[1], sh.pick_u[2], sh.pick_m[0], sh.pick_m[1], total};
+    if (r.bin == 0xffffffffu) r = MassPick{0u, 0u, 0u, 0.0, 0.0, total};   // no token at all
+    __syncthreads();
+    return r;
+}
+
+// One radix level of the top-p select over this tile: every token whose
+// order key matches `prefix` in its bits from `hi_shift` up (every token when
+// hi_shift is 32) adds its count and term to bin (key >> lo_shift) & (NB - 1)
+// of the CTA's histogram in shared memory, which is then added to the unit's
+// histogram h.  Shared memory: NB * 20 bytes of histogram, then 16 warps'
+// 256-score staging (16 KB).
+template <int NB>
+__device__ void mass_level(const Params& p, int u, int tile, float M, uint32_t prefix, int hi_shift, int lo_shift,
+                           unsigned long long* h, unsigned char* smem)
+{
+    const Plan& pl = p.pl;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long* sA = reinterpret_cast<unsigned long long*>(smem);
+    unsigned long long* sB = sA + NB;
+    uint32_t* sC = reinterpret_cast<uint32_t*>(sB + NB);
+    float* stg = reinterpret_cast<float*>(smem + 80 * 1024) + warp * 256;
+    for (int i = tid; i < NB; i += kSelThreads) {
+        sA[i] = 0ull;
+        sB[i] = 0ull;
+        sC[i] = 0u;
+    }
+    __syncthreads();
+    const int W2 = pl.tt / kSelWarps;
+    const int64_t base = (int64_t)tile * pl.tt + (int64_t)warp * W2;
+    const float* S = p.s_src + (int64_t)u * pl.N;
+#pragma unroll 1
+    for (int c0 = 0; c0 < W2; c0 += 256) {
+        const int n = min(256, W2 - c0);
+        __syncwarp();
+#pragma unroll 1
+        for (int i = lane; i < n; i += 32) cp_async_4(stg + i, S + min(base + c0 + i, pl.N - 1));
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+#pragma unroll 1
+        for (int i = lane; i < n; i += 32) {
+            if (base + c0 + i >= pl.N) continue;
+            const float sv = stg[i];
+            const uint32_t k = okey(sv);
+            if (hi_shift < 32 && (k >> hi_shift) != prefix) continue;
+            const uint32_t bin = (k >> lo_shift) & (uint32_t)(NB - 1);
+            const float w = expf(__fsub_rn(sv, M));
+            const unsigned long long v = __float2ull_rz(w * 9223372036854775808.0f);   // w * 2^63, w <= 1
+            atomicAdd(&sA[bin], v >> 32);
+            atomicAdd(&sB[bin], v & 0xffffffffull);
+            atomicAdd(&sC[bin], 1u);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < NB; i += kSelThreads) {
+        if (sC[i]) {
+            atomicAdd(h + i, sA[i]);
+            atomicAdd(h + NB + i, sB[i]);
+            atomicAdd(h + 2 * NB + i, (unsigned long long)sC[i]);
+        }
+    }
+}
+
+// All tiles of unit u have added their level to the unit's histogram.
+__device__ __forceinline__ void mass_level_arrive(const Params& p, int u, int level)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        UnitCtrl* ctrl = ws_ctrl(p) + u;
+        __threadfence();
+        atomicAdd(&ctrl->tp_arrive[level], 1u);
+        if (!wait_geq_bounded(&ctrl->tp_arrive[level], (uint32_t)p.pl.ntile)) flag(ws_status(p), DEV_TIMEOUT);
+    }
+    __syncthreads();
+}
+
+// The size of unit u's top-p stratum (every CTA of the unit returns the same
+// value, at least 1).  Block-wide; uses the first 96 KB of `smem`.
+__device__ __noinline__ uint32_t topp_size(const Params& p, int u, int tile, SelShared& sh, unsigned char* smem)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long* h0 = ws_topp(p) + (size_t)u * kTopPBins * 3;
+    unsigned long long* h1 = h0 + (size_t)4096 * 3;
+    unsigned long long* h2 = h1 + (size_t)4096 * 3;
+    // M: the lower edge of the bucket above the highest non-empty bucket of
+    // the unit's count histogram (above every score, so every term is <= 1)
+    const uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
+    uint32_t top = 0;
+    for (int i = tid; i < kBins; i += kSelThreads)
+        if (__ldcg(hist1 + i)) top = max(top, (uint32_t)i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
+    if (lane == 0) sh.scan[warp] = top;
+    __syncthreads();
+    for (int w = 0; w < kSelWarps; ++w) top = max(top, sh.scan[w]);
+    __syncthreads();
+    float M = okey_value(min(top + 1u, (uint32_t)(kBins - 1)) << 20);
+    if (!isfinite(M)) {   // scores at the top of the binary32 range: no margin above them
+        if (tid == 0) flag(ws_status(p), DEV_NONFINITE);
+        M = 3.4028234663852886e38f;
+    }
+    // level 0: the 12-bit order-key buckets
+    mass_level<4096>(p, u, tile, M, 0u, 32, 20, h0, smem);
+    mass_level_arrive(p, u, 0);
+    const MassPick a = mass_pick<4096>(h0, (double)p.top_p, true, sh);
+    const double t1 = (double)p.top_p * a.total - a.mass_above;   // the target left inside bucket a
+    // level 1: the next 12 bits of bucket a's members
+    mass_level<4096>(p, u, tile, M, a.bin, 20, 8, h1, smem);
+    mass_level_arrive(p, u, 1);
+    const MassPick b = mass_pick<4096>(h1, t1, false, sh);
+    const double t2 = t1 - b.mass_above;
+    // level 2: the last 8 bits of the members sharing those 24 bits
+    mass_level<256>(p, u, tile, M, (a.bin << 12) | b.bin, 8, 0, h2, smem);
+    mass_level_arrive(p, u, 2);
+    const MassPick c = mass_pick<256>(h2, t2, false, sh);
+    // the crossing key's ties have equal terms: the stratum takes the fewest
+    // of them (in index order) whose mass reaches what is left
+    uint32_t r = 1;
+    if (c.count_bin > 0 && c.mass_bin > 0.0) {
+        const double w = c.mass_bin / (double)c.count_bin, rem = t2 - c.mass_above;
+        double need = floor(rem / w);
+        if (need * w < rem) need += 1.0;   // the fewest ties whose mass reaches what is left
+        r = (uint32_t)fmin(fmax(need, 1.0), (double)c.count_bin);
+    }
+    return a.count_above + b.count_above + c.count_above + r;
+}
+
+// ---------------------------------------------------------------------------
 // The selection pass of one (unit, tile): block-wide, kSelThreads threads.
 // ---------------------------------------------------------------------------
 
@@ -411,7 +671,8 @@ struct TileSel {
 // Philox prefixes); the resolve stages candidates in the same bytes.
 constexpr uint32_t kSelStageBytes = (uint32_t)kSelWarps * kSlice * 2u * 6u;
 
-__device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelShared& sh, unsigned char* k2dyn)
+__device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint32_t k_unit, SelShared& sh,
+                                          unsigned char* k2dyn)
 {
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -455,7 +716,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, SelS
 
     // bucket f1 of the k-th score (the largest when k = 0): each thread reads
     // 8 bins of the unit's histogram, top bin first
-    const uint32_t target = (uint32_t)(p.top_k > 0 ? p.top_k : 1);
+    const uint32_t target = k_unit > 0 ? k_unit : 1u;
     const uint32_t* hist1 = ws_hist1(p) + (size_t)u * kBins;
     constexpr int CH = kBins / kSelThreads;
     uint32_t c[CH];

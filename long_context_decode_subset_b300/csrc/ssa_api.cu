@@ -112,6 +112,7 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     pl.o_hq = take((size_t)heads * D * 2);
     pl.o_hout = take((size_t)heads * D * 4);
     pl.o_hlse = take((size_t)heads * 4);
+    pl.o_topp = take((size_t)U * kTopPUnitBytes);
     pl.total = o;
     return pl;
 }
@@ -166,12 +167,29 @@ bool bad_strata(int strata, float top_p)
     return strata < SSA_STRATA_SSA || strata > SSA_STRATA_TOP_P || !(top_p >= 0.0f) || std::isnan(top_p);
 }
 
-// The remainder's sampler: strata 1 keeps every remainder token with
-// p = min(1, B / (N - min(k, N))), i.e. e = 1 and Z = N - min(k, N).
-void set_strata(ssa::Params& p, int strata, int64_t top_k, int64_t N)
+// The strata of a step.  Strata 1 keeps every remainder token with
+// p = min(1, B / (N - min(k, N))), i.e. e = 1 and Z = N - min(k, N).  Top-p
+// with top_p <= 0 is the SSA step with k = 0, with top_p >= 1 the step that
+// keeps every token; otherwise the unit kernel finds each unit's stratum size
+// (p.top_k is then only a nonzero placeholder).  Returns the k the host's
+// dense test uses.
+int64_t set_strata(ssa::Params& p, int strata, int64_t top_k, float top_p, int64_t N)
 {
-    p.strata = strata == SSA_STRATA_UNIFORM ? 1 : 0;
+    p.strata = 0;
+    if (strata == SSA_STRATA_UNIFORM) {
+        p.strata = 1;
+    } else if (strata == SSA_STRATA_TOP_P) {
+        if (!(top_p > 0.0f)) top_k = 0;
+        else if (top_p >= 1.0f) top_k = std::max<int64_t>(N, 1);
+        else {
+            p.strata = 2;
+            p.top_p = top_p;
+            top_k = 1;
+        }
+    }
+    p.top_k = top_k;
     p.z_uniform = (float)(N - std::min<int64_t>(top_k, N));
+    return top_k;
 }
 bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
 
@@ -552,16 +570,14 @@ ssa_status ssa_select_strata(const float* s_hat, int strata, int64_t top_k, floa
     if (st != SSA_OK) return st;
     if (!s_hat || !idx || !p || !count) return SSA_ERR_INVALID_ARG;
     if (bad_scalars(top_k, budget) || bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
-    if (strata == SSA_STRATA_TOP_P) return SSA_ERR_UNSUPPORTED;
     const ssa::Plan pl = unit_plan(*shape);
     if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
     if (pl.U == 0) return SSA_OK;
     ssa::Params prm = base_params(*shape, pl, ws);
     prm.s_src = s_hat;
-    prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
-    set_strata(prm, strata, top_k, shape->ctx_len);
+    top_k = set_strata(prm, strata, top_k, top_p, shape->ctx_len);
     prm.idx_out = idx;
     prm.p_out = p;
     prm.count_out = count;
@@ -632,7 +648,7 @@ void set_append(ssa::Params& p, const AppendArgs& a, int64_t pos, const ssa_shap
     p.ks_sh = s.ks_stride_h;
 }
 
-ssa_status decode_impl(const AppendArgs* app, int strata, bool host_io, const ssa_bf16* q, const ssa_bf16* K,
+ssa_status decode_impl(const AppendArgs* app, int strata, float top_p, bool host_io, const ssa_bf16* q, const ssa_bf16* K,
                        const ssa_bf16* V,
                        const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed,
                        float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
@@ -667,10 +683,9 @@ ssa_status decode_impl(const AppendArgs* app, int strata, bool host_io, const ss
     prm.V = V;
     prm.sel_ch = sel_ch;
     prm.scale = scale;
-    prm.top_k = top_k;
     prm.budget = budget;
     prm.seed = seed;
-    set_strata(prm, strata, top_k, shape->ctx_len);
+    top_k = set_strata(prm, strata, top_k, top_p, shape->ctx_len);
     float* scores = s_hat_opt ? s_hat_opt : reinterpret_cast<float*>(w + pl.o_scores);
     prm.s_dst = scores;
     prm.s_src = scores;
@@ -710,8 +725,8 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
                       float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
 {
-    return decode_impl(nullptr, SSA_STRATA_SSA, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
-                       s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+    return decode_impl(nullptr, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out,
+                       lse, s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
@@ -721,9 +736,8 @@ ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
                              const ssa_shape* shape, cudaStream_t stream)
 {
     if (bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
-    if (strata == SSA_STRATA_TOP_P) return SSA_ERR_UNSUPPORTED;
-    return decode_impl(nullptr, strata, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt,
-                       idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+    return decode_impl(nullptr, strata, top_p, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+                       s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K,
@@ -736,7 +750,7 @@ ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa
     if (shape->ctx_len < 1 || !k_new || !v_new || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SSA_ERR_INVALID_ARG;
     const AppendArgs app{k_new, v_new, K, V, Ks};
-    return decode_impl(&app, SSA_STRATA_SSA, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+    return decode_impl(&app, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
                        nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
 }
 
@@ -769,7 +783,7 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     // pinned, mapped buffers: the kernels read q from host memory and write
     // out / lse into it (no copy is enqueued)
     if (device_readable(q_host, true) && device_readable(out_host, true) && device_readable(lse_host, true))
-        return decode_impl(nullptr, SSA_STRATA_SSA, true, q_host, K, V, Ks, sel_ch, top_k, budget, seed, scale,
+        return decode_impl(nullptr, SSA_STRATA_SSA, 0.0f, true, q_host, K, V, Ks, sel_ch, top_k, budget, seed, scale,
                            out_host, lse_host, nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
     // otherwise one staged copy in, the step, two staged copies out
     const ssa::Plan pl = make_plan(*shape, 0);

@@ -247,6 +247,22 @@ def top_p_count(s: np.ndarray, top_p: float) -> int:
     return int(min(N, np.searchsorted(mass, top_p, side="left") + 1))
 
 
+def top_p_shares(s: np.ndarray, top_p: float):
+    """(k, share of the first k - 1 tokens, share of the first k tokens) for k = top_p_count(s, top_p),
+    the shares computed as top_p_count computes them: how close top_p falls to the stratum's edges."""
+    s = _c(s, np.float32)
+    N = s.size
+    k = top_p_count(s, top_p)
+    if N == 0 or k == 0:
+        return k, 0.0, 0.0
+    bits = s.view(np.uint32).astype(np.uint64)
+    key = np.where(bits >> 31, (~bits) & 0xFFFFFFFF, bits | 0x80000000)
+    order = np.lexsort((np.arange(N), -key.astype(np.int64)))
+    w = np.exp(s.astype(np.float64) - float(np.max(s)))
+    mass = np.cumsum(w[order]) / np.sum(w)
+    return k, (float(mass[k - 2]) if k >= 2 else 0.0), float(mass[k - 1])
+
+
 def select_unit_top_p(s: np.ndarray, top_p: float, budget: float, seed: int, b: int, h_kv: int):
     """The top-p stratum with the SSA sampler on the rest: T is the top-p set
     (top_p_count tokens in the top-k order, i.e. the top-k stratum with

@@ -118,15 +118,16 @@ def test_other_entry_points_validate():
     assert lib.ssa_query_plan(None, None, None, None) == 1
     assert lib.ssa_select_capacity(ctypes.byref(s)) == s.ctx_len
     assert lib.ssa_select_capacity(None) == 0
-    # strata: an unknown kind or a negative / NaN top_p is invalid; top-p is declared but not built
+    # strata: an unknown kind or a negative / NaN top_p is invalid
     assert lib.ssa_select_strata(f, 3, 5, 0.0, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
     assert lib.ssa_select_strata(f, -1, 5, 0.0, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
     assert lib.ssa_select_strata(f, 1, 5, float("nan"), 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
-    assert lib.ssa_select_strata(f, 2, 5, 0.9, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 2
+    assert lib.ssa_select_strata(f, 2, 5, -0.5, 1.0, 0, f, f, f, cap, f, 1 << 40, ctypes.byref(s), None) == 1
+    assert lib.ssa_select_strata(f, 2, 5, 0.9, 1.0, 0, f, f, f, cap, f, 16, ctypes.byref(s), None) == 3
     assert lib.ssa_decode_strata(f, f, f, f, f, 7, 5, 0.0, 1.0, 0, 0.1, f, f, None, None, None, None, cap, f, 1 << 40,
                                  ctypes.byref(s), None) == 1
-    assert lib.ssa_decode_strata(f, f, f, f, f, 2, 5, 0.5, 1.0, 0, 0.1, f, f, None, None, None, None, cap, f, 1 << 40,
-                                 ctypes.byref(s), None) == 2
+    assert lib.ssa_decode_strata(f, f, f, f, f, 2, 5, float("nan"), 1.0, 0, 0.1, f, f, None, None, None, None, cap, f,
+                                 1 << 40, ctypes.byref(s), None) == 1
 
 
 def test_binding_requires_the_library(monkeypatch, tmp_path):

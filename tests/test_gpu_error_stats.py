@@ -9,7 +9,9 @@ strata": the two baselines it contrasts).
 Dense attention is the library's own dense limit (B = +inf), which the
 parity tests pin against the oracle.  The uniform hybrid keeps the same
 top-k stratum and draws every other token with p = B / (N - k), with the
-same Philox uniforms (the library's SSA_STRATA_UNIFORM).  The numbers are
+same Philox uniforms (the library's SSA_STRATA_UNIFORM); the top-p stratum
+(SSA_STRATA_TOP_P, top_p = 0.9) keeps the tokens holding 90 % of the
+estimated softmax and samples the rest as SSA does.  The numbers are
 printed as one JSON line; the assertions are only sanity bounds.
 """
 import json
@@ -40,7 +42,7 @@ def _stats(x):
 def test_error_vs_dense_statistic():
     cfg = workloads.CONFIGS["ministral8b_32k"]
     k, B = cfg.top_k, cfg.budget
-    errs = {"ssa": [], "topk": [], "uniform_hybrid": []}
+    errs = {"ssa": [], "topk": [], "uniform_hybrid": [], "top_p_0.9": []}
     for seed in range(3):
         w = workloads.generate(cfg, seed, DEV)
         Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
@@ -52,12 +54,15 @@ def test_error_vs_dense_statistic():
         out_topk, _ = ssa.ssa_decode(q, K, V, Ks, sel, k + int(B), 0.0, seed, cfg.scale)
         # the top-k + uniform hybrid at the same budget, drawn by the library (SSA_STRATA_UNIFORM)
         out_uh, _ = ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.ssa.STRATA_UNIFORM, k, 0.0, B, seed, cfg.scale)
+        # the top-p stratum (the tokens holding 90 % of the estimated softmax) with the SSA sampler on the rest
+        out_tp, _ = ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.ssa.STRATA_TOP_P, 0, 0.9, B, seed, cfg.scale)
         torch.cuda.synchronize()
         errs["ssa"].append(_rel_err(out_ssa, dense))
         errs["topk"].append(_rel_err(out_topk, dense))
         errs["uniform_hybrid"].append(_rel_err(out_uh, dense))
+        errs["top_p_0.9"].append(_rel_err(out_tp, dense))
     report = {m: _stats(v) for m, v in errs.items()}
     report["config"] = {"workload": cfg.name, "top_k": k, "budget": B, "seeds": 3, "heads": int(errs["ssa"][0].size)}
     print("error_vs_dense", json.dumps(report))
-    for m in ("ssa", "topk", "uniform_hybrid"):   # sanity only: heads with a small dense output dominate the tail
+    for m in ("ssa", "topk", "uniform_hybrid", "top_p_0.9"):   # sanity only: heads with a small dense output dominate the tail
         assert math.isfinite(report[m]["mean"]) and report[m]["p50"] < 1.0, (m, report[m])

@@ -166,3 +166,29 @@ def test_full_size_uniform_hybrid_given_oracle_scores(oracle_mod):
             o_idx, o_p = oracle_mod.select_unit_uniform(s_np[b, h], cfg.top_k, cfg.budget, seed, b, h)
             n = int(count[b, h])
             assert np.array_equal(idx[b, h, :n], o_idx) and np.array_equal(p[b, h, :n], o_p), (b, h)
+
+
+def test_full_size_top_p_given_oracle_scores(oracle_mod):
+    """The top-p stratum at the 128K workload in the automatic plan: the stratum's size and set against the
+    oracle's (a size one off only where top_p falls within 2e-6 of the stratum's edge), the sampled lists as
+    the oracle's SSA sampler draws them for that size."""
+    cfg = workloads.CONFIGS["ministral8b_128k"]
+    w = workloads.generate(cfg, 0, "cuda")
+    s_np = _oracle_scores(oracle_mod, w, cfg)
+    del w
+    s = torch.from_numpy(s_np).cuda()
+    top_p, seed = 0.9, 8
+    i0, _, c0 = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, top_p, 0.0, seed)
+    idx, p, count = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, top_p, cfg.budget, seed)
+    i0, c0 = i0.cpu().numpy(), c0.cpu().numpy()
+    idx, p, count = idx.cpu().numpy(), p.cpu().numpy(), count.cpu().numpy()
+    for b in range(cfg.batch):
+        for h in range(cfg.n_kv_heads):
+            k_o, before, at = oracle_mod.top_p_shares(s_np[b, h], top_p)
+            k = int(c0[b, h])
+            assert k == k_o or (k == k_o - 1 and top_p - before <= 2e-6) or (k == k_o + 1 and at - top_p <= 2e-6)
+            assert np.array_equal(i0[b, h, :k], oracle_mod.select_unit(s_np[b, h], k, 0.0, seed, b, h)[0])
+            o_idx, o_p, m, Z, p_all = oracle_mod.select_unit(s_np[b, h], k, cfg.budget, seed, b, h, want_p_all=True)
+            n = int(count[b, h])
+            compare_unit_lists(idx[b, h, :n], p[b, h, :n], o_idx, o_p, p_all,
+                               lambda j: oracle_mod.uniform(seed, j, h, b))

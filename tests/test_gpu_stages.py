@@ -311,3 +311,118 @@ def test_decode_uniform_hybrid_parity(oracle_mod):
                                                   cfg.scale)
             assert np.allclose(out[b, h * G:(h + 1) * G].cpu().numpy(), out_o, atol=2e-3, rtol=2e-3)
             assert np.allclose(lse[b, h * G:(h + 1) * G].cpu().numpy(), lse_o, atol=2e-3, rtol=2e-3)
+
+
+def _top_p_sizes(oracle_mod, s_unit, top_p, tol=2e-6):
+    """The oracle's top-p stratum size and, where top_p falls within `tol` of a stratum edge (the GPU sums
+    fp32 expf terms, the oracle double exp terms), the neighbouring size the GPU may find instead."""
+    k, before, at = oracle_mod.top_p_shares(s_unit, top_p)
+    sizes = [k]
+    if k >= 1 and top_p - before <= tol * top_p:
+        sizes.append(k - 1)
+    if at - top_p <= tol * top_p and k < s_unit.size:
+        sizes.append(k + 1)
+    return sizes
+
+
+def _select_top_p_and_compare(oracle_mod, s_np, top_p, B, seed, tile=None, split=None):
+    s = torch.from_numpy(s_np).to(DEV)
+    Bt, Hkv, N = s_np.shape
+    with plan_env(tile, split):
+        i0, p0, c0 = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, top_p, 0.0, seed)   # the stratum alone
+        idx, p, count = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, top_p, B, seed)
+    torch.cuda.synchronize()
+    i0, c0 = i0.cpu().numpy(), c0.cpu().numpy()
+    idx, p, count = idx.cpu().numpy(), p.cpu().numpy(), count.cpu().numpy()
+    edges = 0
+    for b in range(Bt):
+        for h in range(Hkv):
+            sizes = _top_p_sizes(oracle_mod, s_np[b, h], top_p)
+            k = int(c0[b, h])
+            assert k in sizes, (b, h, k, sizes)
+            edges += k != sizes[0]
+            t_idx = oracle_mod.select_unit(s_np[b, h], k, 0.0, seed, b, h)[0]
+            assert np.array_equal(i0[b, h, :k], t_idx)
+            o_idx, o_p, m, Z, p_all = oracle_mod.select_unit(s_np[b, h], k, B, seed, b, h, want_p_all=True)
+            n = int(count[b, h])
+            compare_unit_lists(idx[b, h, :n], p[b, h, :n], o_idx, o_p, p_all,
+                               lambda j: oracle_mod.uniform(seed, j, h, b))
+    return edges
+
+
+@pytest.mark.parametrize("tile,split", [(None, None), (512, 1), (1024, 3), (4096, 2)])
+def test_select_top_p_parity(oracle_mod, tile, split):
+    """The top-p stratum (SSA_STRATA_TOP_P) against the oracle's top_p_count / select_unit_top_p, given the
+    oracle's scores, over several tilings and stratum sizes."""
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
+    for top_p in (0.01, 0.3, 0.9, 0.999):
+        assert _select_top_p_and_compare(oracle_mod, s_np, top_p, cfg.budget, 7, tile, split) <= 1
+
+
+def test_select_top_p_edge_cases(oracle_mod):
+    rng = np.random.default_rng(31)
+    for N, top_p, B, kind in [(3000, 0.5, 40.0, "constant"), (3000, 0.37, 40.0, "ties"), (2500, 0.8, 30.0, "wide"),
+                              (513, 0.6, 5.0, "signed_zero"), (4097, 0.95, 1e6, "normal"), (1, 0.5, 5.0, "normal"),
+                              (2000, 0.2, 0.0, "needles")]:
+        if kind == "constant":
+            s = np.full((1, 2, N), 0.375)
+        elif kind == "ties":
+            s = np.round(rng.standard_normal((1, 2, N)) * 2) / 4
+        elif kind == "wide":
+            s = rng.standard_normal((1, 2, N)) * np.exp2(rng.integers(-10, 4, (1, 2, N)))
+        elif kind == "signed_zero":
+            s = np.where(rng.random((1, 2, N)) < 0.5, 0.0, -0.0) * np.ones((1, 2, N))
+            s[..., ::7] = rng.standard_normal(s[..., ::7].shape)
+        elif kind == "needles":
+            s = rng.standard_normal((1, 2, N)) * 1.5
+            s[..., rng.choice(N, 12, replace=False)] += 9.0
+        else:
+            s = rng.standard_normal((1, 2, N)) * 1.5
+        _select_top_p_and_compare(oracle_mod, s.astype(np.float32), top_p, B, 4)
+
+
+def test_select_top_p_limits(oracle_mod):
+    """top_p <= 0: no stratum (the SSA sampler with k = 0); top_p >= 1: every token."""
+    s_np = (np.random.default_rng(2).standard_normal((1, 2, 3000)) * 1.5).astype(np.float32)
+    s = torch.from_numpy(s_np).to(DEV)
+    idx, p, count = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, 0.0, 30.0, 3)
+    for h in range(2):
+        o_idx, o_p, m, Z, p_all = oracle_mod.select_unit(s_np[0, h], 0, 30.0, 3, 0, h, want_p_all=True)
+        n = int(count[0, h])
+        compare_unit_lists(idx[0, h, :n].cpu().numpy(), p[0, h, :n].cpu().numpy(), o_idx, o_p, p_all,
+                           lambda j: oracle_mod.uniform(3, j, h, 0))
+    idx, p, count = ssa.ssa_select_strata(s, ssa.STRATA_TOP_P, 0, 1.0, 30.0, 3)
+    assert torch.all(count == 3000)
+
+
+def test_decode_top_p_parity(oracle_mod):
+    """The whole step with the top-p stratum: the lists against the oracle's on the oracle's scores (stratum
+    and sampling boundaries excepted), the output against the oracle's attention over the GPU's index set with
+    the oracle's inclusion probabilities."""
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = oracle_inputs(w)
+    Bt, Hkv, N = cfg.batch, cfg.n_kv_heads, cfg.ctx_len
+    G = cfg.group
+    top_p = 0.9
+    idx = torch.empty((Bt, Hkv, N), dtype=torch.int32, device=DEV)
+    p = torch.empty((Bt, Hkv, N), dtype=torch.float32, device=DEV)
+    count = torch.empty((Bt, Hkv), dtype=torch.int32, device=DEV)
+    out, lse = ssa.ssa_decode_strata(w["q"], w["K"], w["V"], w["Ks"], w["sel_ch"], ssa.STRATA_TOP_P, 0, top_p,
+                                     cfg.budget, 9, cfg.scale, idx=idx, p=p, count=count)
+    s_np = oracle_mod.score(q, Ks, sel, cfg.scale)
+    for b in range(Bt):
+        for h in range(Hkv):
+            o_idx, o_p, m, Z = oracle_mod.select_unit_top_p(s_np[b, h], top_p, cfg.budget, 9, b, h)
+            _, _, _, _, p_all = oracle_mod.select_unit(s_np[b, h], oracle_mod.top_p_count(s_np[b, h], top_p),
+                                                       cfg.budget, 9, b, h, want_p_all=True)
+            n = int(count[b, h])
+            g_idx = idx[b, h, :n].cpu().numpy()
+            assert len(set(g_idx.tolist()) ^ set(o_idx.tolist())) <= 3
+            out_o, lse_o = oracle_mod.attend_unit(q[b, h * G:(h + 1) * G], K[b, h], V[b, h], g_idx, p_all[g_idx],
+                                                  cfg.scale)
+            assert np.allclose(out[b, h * G:(h + 1) * G].cpu().numpy(), out_o, atol=2e-3, rtol=2e-3)
+            assert np.allclose(lse[b, h * G:(h + 1) * G].cpu().numpy(), lse_o, atol=2e-3, rtol=2e-3)

@@ -138,3 +138,15 @@ def test_uniform_hybrid_is_unbiased_by_enumeration(oracle_mod):
     want_num, want_den = _dense_sums(qh, K, V, scale)
     assert np.allclose(den, want_den, rtol=2e-6)
     assert np.allclose(num, want_num, rtol=2e-5, atol=2e-5 * np.abs(want_num).max())
+
+
+def test_top_p_shares_bracket_top_p(oracle_mod):
+    """The stratum's edge: the share of one token fewer stays below top_p, the stratum's own reaches it."""
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        N = int(rng.integers(2, 300))
+        s = (rng.standard_normal(N) * 2).astype(np.float32)
+        top_p = float(rng.uniform(0.05, 0.95))
+        k, before, at = oracle_mod.top_p_shares(s, top_p)
+        assert k == oracle_mod.top_p_count(s, top_p)
+        assert before < top_p <= at
