@@ -165,8 +165,9 @@ int ssa_version(void);
  * (about 22 bytes per cached token plus 32 KB per unit: scores, candidate
  * and selection lists sized for the worst case, 16-bit Philox prefixes,
  * histograms).
- * Independent of the stream, the device and list_cap (kept for symmetry with
- * the calls that take a list capacity); 0 on invalid input. */
+ * Independent of the stream, the device, the strides and list_cap (kept for
+ * symmetry with the calls that take a list capacity); the four stride fields
+ * may all be 0 (the paged cache's shape).  0 on invalid input. */
 size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap);
 
 /* Append-time key summary (step a0): Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]]
@@ -192,7 +193,7 @@ ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_
 
 /* Worst-case list length per unit: ctx_len (every cached token selected, as
  * when top_k >= ctx_len or budget = +inf).  A list_cap of at least this
- * never overflows.  0 on invalid input. */
+ * never overflows.  Strides as in ssa_workspace_bytes.  0 on invalid input. */
 size_t ssa_select_capacity(const ssa_shape* shape);
 
 /* Step (a): s_hat[b][h][i] for every token ("FASA: Frequency-Aware Sparse
@@ -288,6 +289,54 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
                            uint64_t seed, float scale, float* out_host, float* lse_host,
                            void* ws, size_t ws_bytes, const ssa_shape* shape,
                            cudaStream_t stream);
+
+/* A paged, variable-length KV cache (the serving layout): K, V and Ks live in
+ * page pools shared by the batch's sequences,
+ *   K_pool, V_pool [num_pages][n_kv_heads][page_size][head_dim]
+ *   Ks_pool        [num_pages][n_kv_heads][page_size][d_sel]
+ * (contiguous, 16-byte aligned), and token t of sequence b is slot
+ * t % page_size of page block_table[b][t / page_size].  Sequence b holds
+ * seq_lens[b] tokens, 0 <= seq_lens[b] <= shape.ctx_len; shape.ctx_len bounds
+ * every sequence (the workspace, the score rows and the list capacity are
+ * sized by it) and must not exceed max_pages * page_size.  The block-table
+ * entries of the pages a sequence's tokens fall in must be page ids in
+ * [0, num_pages); the others are not read.  block_table and seq_lens are
+ * device memory, read by the kernels, so they may be updated on the stream
+ * between steps without a host round trip. */
+typedef struct {
+    int32_t page_size;           /* tokens per page: a power of two, 16 <= page_size <= 2^20 */
+    int32_t max_pages;           /* entries per sequence in block_table (>= 1) */
+    int64_t num_pages;           /* pages in each pool; num_pages * page_size < 2^31 */
+    const int32_t* block_table;  /* [batch][max_pages] page ids */
+    const int32_t* seq_lens;     /* [batch] tokens per sequence */
+} ssa_paged_kv;
+
+/* The whole step over a paged, variable-length cache (ssa_paged_kv): every
+ * unit (b, h_kv) gets the step of ssa_decode over its own seq_lens[b] tokens
+ * (the same scores, strata and Philox draws -- counters (j, h_kv, b, 0) with
+ * j the token's position in its sequence -- and attention; Z is summed over
+ * the plan's tiles of ctx_len, so it can differ from a contiguous call with
+ * ctx_len = seq_lens[b] in its last bits).  With every seq_lens[b] equal to
+ * ctx_len the results equal ssa_decode's on the same data bit for bit.  A unit with
+ * top_k >= seq_lens[b] keeps all its tokens with p = 1; an empty sequence
+ * gives zero outputs and lse = -inf.  shape's four stride fields must be 0
+ * (the pools' layout is fixed above).  When k_new and v_new are given
+ * ([batch][n_kv_heads][head_dim], as in ssa_append) the chain's first
+ * kernel first writes the new token at position seq_lens[b] - 1 of every
+ * non-empty sequence (its K, V and Ks rows, in its page), so seq_lens
+ * already counts it; else they are NULL.  s_hat_opt [batch][n_kv_heads]
+ * [ctx_len] receives the scores of positions < seq_lens[b] (the rest of each
+ * row is not written); idx_opt / p_opt / count_opt as in ssa_decode, with
+ * token positions within the sequence.  A length outside [0, ctx_len] or a
+ * page id outside [0, num_pages) sets SSA_DEV_BAD_INDEX (the length is
+ * clamped, the page replaced by page 0: no access leaves the pools).  K and
+ * V pools may be pinned host memory (the memory tiers above). */
+ssa_status ssa_decode_paged(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K_pool,
+                            ssa_bf16* V_pool, ssa_bf16* Ks_pool, const ssa_paged_kv* pages,
+                            const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale,
+                            float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
+                            int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes,
+                            const ssa_shape* shape, cudaStream_t stream);
 
 /* Size of the library's built-in scratch array used by ssa_decode_static. */
 #define SSA_STATIC_SCRATCH_BYTES (64u << 20)

@@ -45,17 +45,19 @@ struct UnitSel {
     bool sampling;
 };
 
-// Entries [c0, c0 + n) of this CTA's list (n <= LIST): staged through
+// Entries [c0, c0 + n) of this CTA's list (n <= LIST) from source `mode`
+// (0 the selection, 1 all tokens, 2 the caller's list): staged through
 // ridx / rval (cp.async, one wave), decided, and the kept ones written in
-// list order to cidx / clp (log p) [0, nk).  Returns nk (every thread).
+// list order to cidx (the token, or with a paged cache its pool token) /
+// clp (log p) [0, nk).  Returns nk (every thread).
 // Source 0: the list is the concatenation of the tile's warp slices, pre[]
 // their exclusive prefix (pre[kSelWarps] = length).  With a compact list
 // requested, the kept (index, p) pairs also go to the unit's staging area at
 // stage_at.  NT threads; ends with a block barrier.
-template <int LIST, int NT>
-__device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int64_t c0, int n, int64_t stage_at,
-                            const uint32_t* pre, const UnitSel& us, int32_t* ridx, float* rval, int32_t* cidx,
-                            float* clp, uint32_t* scan)
+template <int LIST, int NT, bool PAGED>
+__device__ int stage_decide(const Params& p, int mode, int u, int b, int h, int tile, int64_t c0, int n,
+                            int64_t stage_at, const uint32_t* pre, const UnitSel& us, int32_t* ridx, float* rval,
+                            int32_t* cidx, float* clp, uint32_t* scan)
 {
     constexpr int PER = (LIST + NT - 1) / NT;   // entries per thread at most
     static_assert(PER <= 32, "one keep bit per entry in a word");
@@ -65,7 +67,7 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int6
     uint32_t* status = ws_status(p);
     const int32_t* sidx = ws_sel_idx(p) + (size_t)u * pl.np;
     const float* sp = ws_sel_p(p) + (size_t)u * pl.np;
-    if (p.src_mode == 0) {
+    if (mode == 0) {
 #pragma unroll 1
         for (int i = tid; i < n; i += NT) {
             const int64_t pos = c0 + i;
@@ -78,7 +80,7 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int6
             cp_async_4(ridx + i, sidx + at);
             cp_async_4(rval + i, sp + at);
         }
-    } else if (p.src_mode == 2) {
+    } else if (mode == 2) {
 #pragma unroll 1
         for (int i = tid; i < n; i += NT) {
             cp_async_4(ridx + i, p.idx_in + (int64_t)u * p.cap + c0 + i);
@@ -99,14 +101,14 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int6
         int32_t j;
         float pv;
         bool keep;
-        if (p.src_mode == 1) {
+        if (mode == 1) {
             j = (int32_t)(c0 + i);
             pv = 1.0f;
             keep = true;
         } else {
             j = ridx[i];
             pv = rval[i];
-            if (p.src_mode == 0) {
+            if (mode == 0) {
                 const bool is_cand = ((uint32_t)j & kCandFlag) != 0u;
                 j = (int32_t)((uint32_t)j & ~kCandFlag);
                 keep = false;
@@ -140,16 +142,33 @@ __device__ int stage_decide(const Params& p, int u, int b, int h, int tile, int6
             ++kcount;
         }
     }
-    // the kept entries in list order
+    // the kept entries in list order (a paged cache's block-table reads for
+    // them all go out first, together)
     uint32_t nk;
     uint32_t at = block_excl_scan<NT>(kcount, scan, nk);
+    int32_t pt[PER];
+    if constexpr (PAGED) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            pt[e] = 0;
+            if (e < e1 - e0 && ((kbits >> e) & 1u))
+                pt[e] = pool_token(p, b, (mode == 1) ? c0 + e0 + e : (int64_t)ridx[e0 + e]);
+        }
+    }
 #pragma unroll 1
     for (int e = 0; e < e1 - e0; ++e) {
         if (!((kbits >> e) & 1u)) continue;
         const int i = e0 + e;
-        const int32_t j = (p.src_mode == 1) ? (int32_t)(c0 + i) : ridx[i];
-        const float pv = (p.src_mode == 1) ? 1.0f : rval[i];
-        cidx[at] = j;
+        const int32_t j = (mode == 1) ? (int32_t)(c0 + i) : ridx[i];
+        const float pv = (mode == 1) ? 1.0f : rval[i];
+        if constexpr (PAGED) {
+            int32_t ptv = 0;   // pt[e], picked without indexing the array by a variable
+#pragma unroll
+            for (int x = 0; x < PER; ++x) ptv = (x == e) ? pt[x] : ptv;
+            cidx[at] = ptv;
+        } else {
+            cidx[at] = j;
+        }
         clp[at] = logf(pv);
         if (p.idx_out) {
             if (stage_at + at < pl.N)
@@ -213,7 +232,7 @@ constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST>::SMEM; }
 // the MMAs (and owns the tensor memory), warps 5 .. 15 gather the K and V
 // rows.  Chunk g uses buffers g & 1; barrier phases count chunks over the
 // whole CTA.  Grid: U * C CTAs, C = pl.ntile per unit, one wave.
-template <int G, int D, int LIST>
+template <int G, int D, int LIST, bool PAGED>
 __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_constant__ Params p)
 {
     using CF = UCfg<G, D, LIST>;
@@ -276,12 +295,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     UnitCtrl* ctrl = ws_ctrl(p) + u;
     UnitSel us{0u, -1, 0.0f, 0.0f, false};
     int64_t lo = 0, hi = 0;
-    if (p.src_mode == 0) {
-        SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
-        // the stratum's size: k, or (top-p) found from the unit's score masses
-        const uint32_t k_unit = (p.strata == 2) ? topp_size(p, u, r, sh, smem)
-                                                : (uint32_t)min(p.top_k, (int64_t)0xffffffff);
-        const TileSel ts = tile_pass(p, u, r, k_unit, sh, smem);
+    const int64_t nu = unit_len<PAGED>(p, b);   // the unit's tokens
+    int mode = p.src_mode;
+    SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
+    // the stratum's size: k, or (top-p) found from the unit's score masses;
+    // a paged cache's unit whose stratum holds all its tokens keeps every one
+    // with p = 1 (a sequence shorter than k)
+    uint32_t k_unit = 0;
+    if (mode == 0) {
+        k_unit = (p.strata == 2) ? topp_size(p, u, r, nu, sh, smem) : (uint32_t)min(p.top_k, (int64_t)0xffffffff);
+        if (PAGED && (int64_t)k_unit >= nu) mode = 1;
+    }
+    if (mode == 0) {
+        const TileSel ts = tile_pass(p, u, r, nu, k_unit, sh, smem);
         if (tid == 0) {
             uint32_t run = 0;
             for (int w = 0; w < kSelWarps; ++w) {
@@ -298,7 +324,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         // (every CTA computes the same result)
         if (tid == 0 && !wait_geq_bounded(&ctrl->arrive, (uint32_t)C)) flag(status, DEV_TIMEOUT);
         __syncthreads();
-        resolve_unit(p, u, ts.f1, ts.above1, ts.target, ts.m, sh, reinterpret_cast<uint2*>(smem));
+        resolve_unit(p, u, nu, ts.f1, ts.above1, ts.target, ts.m, sh, reinterpret_cast<uint2*>(smem));
         __syncthreads();
         us.theta = sh.r_theta;
         us.cut = sh.r_cut;
@@ -306,9 +332,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         us.Z = sh.r_Z;
         SSA_MARK(4);
         hi = pre[kSelWarps];
-    } else if (p.src_mode == 1) {
-        lo = min(pl.N, (int64_t)r * pl.tt);
-        hi = min(pl.N, lo + pl.tt);
+    } else if (mode == 1) {
+        lo = min(nu, (int64_t)r * pl.tt);
+        hi = min(nu, lo + pl.tt);
     } else {
         const int64_t c = p.count_in[u];
         const int64_t total = c < 0 ? 0 : (c > p.cap ? p.cap : c);
@@ -317,9 +343,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     SSA_MARK(11);
     us.sampling = p.budget > 0.0f && us.Z > 0.0f;
-    const int64_t stage_base = (p.src_mode == 0) ? (int64_t)r * pl.tt : lo;   // the compact list's staging
-    const uint16_t* Kb = p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
-    const uint16_t* Vb = p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
+    const int64_t stage_base = (mode == 0) ? (int64_t)r * pl.tt : lo;   // the compact list's staging
+    // row j of the unit: Kb + j * D (a paged cache: the pool row of pool token j)
+    const uint16_t* Kb = PAGED ? p.K : p.K + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
+    const uint16_t* Vb = PAGED ? p.V : p.V + (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh;
 
     // epilogue state: running (m, l) per head (the same in every epilogue
     // thread) and this thread's head dim of the accumulator
@@ -339,8 +366,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         const int n = (int)min((int64_t)LIST, hi - c0);
         int32_t* ridx = reinterpret_cast<int32_t*>(smem + CF::OFF_RAW);
         float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4);
-        const int nk = stage_decide<LIST, kSelThreads>(p, u, b, h, r, c0, n, stage_base + kept, pre, us, ridx, rval,
-                                                       cidx, clp, scan);
+        const int nk = stage_decide<LIST, kSelThreads, PAGED>(p, mode, u, b, h, r, c0, n, stage_base + kept, pre, us, ridx,
+                                                       rval, cidx, clp, scan);
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
@@ -365,7 +392,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     const int i = q / PPR, pc = q % PPR;
                     const int row = c * CF::CH + i;
                     const bool valid = row < nk;
-                    const int64_t j = valid ? (int64_t)cidx[row] : 0;
+                    int64_t j = valid ? (int64_t)cidx[row] : 0;
+                    if constexpr (PAGED) j = valid ? pool_row(p, h, (int32_t)j) : 0;
                     const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
                     cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, valid);
                     cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, valid);

@@ -20,7 +20,9 @@
 //   warp 0   takes the stages, publishes each one's (unit, j) and issues its
 //            TMA copies: two 256-token boxes of the summary (swizzled to the
 //            64- or 32-byte row width so that the tensor cores read them as
-//            K-major operands), into a ring;
+//            K-major operands), into a ring; with a paged cache one box per
+//            page piece (min(page_size, 256) tokens, a lane each), placed
+//            where the 256-token box would put those rows;
 //   warp 3   writes each stage's 1 KB query operand (the unit's G query
 //            heads on the summary channels, same swizzle) beside it;
 //   warp 1   issues tcgen05.mma (M = 128 tokens, N = 16 query-head slots,
@@ -50,7 +52,6 @@ struct Params {
     float top_p;               // strata 2: the stratum's share of the softmax of the scores
     int32_t q_staged;          // q is copied from q_host into the workspace by K0: read it after the wait
     const uint16_t* q_host;    // the step's query in pinned host memory (q_staged), [Bt][Hq][d]
-    float z_uniform;           // strata 1: the remainder's size N - min(k, N) as fp32
     const uint16_t* q;         // [Bt][Hq][d]
     const uint16_t* K;         // [Bt][Hkv][N][d] with the strides below
     const uint16_t* V;
@@ -81,6 +82,18 @@ struct Params {
     uint16_t* app_Ks;
     int64_t app_pos;
     int64_t ks_sb, ks_sh;
+    // paged, variable-length cache: K, V and Ks are page pools
+    // [num_pages][Hkv][page_size][d or d_sel]; token t of sequence b sits in
+    // page block_table[b][t >> log_ps] at slot t & (page_size - 1), and
+    // sequence b holds seq_lens[b] <= pl.N tokens (the append, when given,
+    // writes position seq_lens[b] - 1)
+    int32_t paged;
+    int32_t log_ps;
+    int32_t max_pages;         // block-table entries per sequence
+    int32_t log_box;           // log2 of the summary's TMA box height, min(page_size, 256)
+    int64_t num_pages;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
 };
 
 __device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
@@ -97,6 +110,54 @@ __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinter
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
 __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
 
+// Strata 1 (top-k + uniform): the remainder's size n - min(k, n) in fp32,
+// the normaliser Z of p = min(1, B / Z) for a unit of n tokens.
+__device__ __forceinline__ float uniform_z(const Params& p, int64_t n)
+{
+    return (float)(n - min(p.top_k, n));
+}
+
+// Tokens of sequence b: pl.N, or (PAGED) seq_lens[b]; a length outside
+// [0, pl.N] is flagged and clamped.  The kernels that read a paged cache are
+// separate instantiations (PAGED), so that the contiguous ones carry none of
+// its code.
+template <bool PAGED>
+__device__ __forceinline__ int64_t unit_len(const Params& p, int b)
+{
+    if constexpr (!PAGED) return p.pl.N;
+    const int32_t n = __ldg(p.seq_lens + b);
+    if (n < 0 || (int64_t)n > p.pl.N) {
+        flag(ws_status(p), DEV_BAD_INDEX);
+        return n < 0 ? 0 : p.pl.N;
+    }
+    return n;
+}
+
+// The pool page holding token t of sequence b (t < pl.N); a page id outside
+// [0, num_pages) is flagged and replaced by page 0, so that no access leaves
+// the pools.
+__device__ __forceinline__ int32_t page_of(const Params& p, int b, int64_t t)
+{
+    const int32_t pg = __ldg(p.block_table + (int64_t)b * p.max_pages + (t >> p.log_ps));
+    if ((uint64_t)(uint32_t)pg >= (uint64_t)p.num_pages) {
+        flag(ws_status(p), DEV_BAD_INDEX);
+        return 0;
+    }
+    return pg;
+}
+
+// Token t of sequence b as a pool token: page * page_size + slot (below 2^31).
+__device__ __forceinline__ int32_t pool_token(const Params& p, int b, int64_t t)
+{
+    return (page_of(p, b, t) << p.log_ps) | (int32_t)(t & ((1 << p.log_ps) - 1));
+}
+
+// The row (in head_dim or d_sel units) of pool token pt of KV head h in a pool.
+__device__ __forceinline__ int64_t pool_row(const Params& p, int h, int32_t pt)
+{
+    return ((((int64_t)(pt >> p.log_ps)) * p.Hkv + h) << p.log_ps) + (pt & ((1 << p.log_ps) - 1));
+}
+
 // ---------------------------------------------------------------------------
 // K0: zero the unit's control block and histograms.  One CTA per unit.  It
 // lets the next kernel launch at once: K1 streams the summary meanwhile and
@@ -106,14 +167,26 @@ __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpr
 // ("FASA: Frequency-Aware Sparse Attention", section 3, Stage 1: a token's
 // dominant channels are stored contiguously when it is appended):
 //   K[b][h][pos] = k_new[b][h],  V[b][h][pos] = v_new[b][h],
-//   Ks[b][h][pos][j] = k_new[b][h][S_ch[h][j]].
-// An out-of-range channel is flagged and clamped.
+//   Ks[b][h][pos][j] = k_new[b][h][S_ch[h][j]],
+// pos = app_pos, or (paged) the sequence's last position seq_lens[b] - 1 in
+// its page (nothing for an empty sequence).  An out-of-range channel is
+// flagged and clamped.
 __device__ __forceinline__ void append_unit(const Params& p, int u, int tid, int nthreads)
 {
     const int b = u / p.Hkv, h = u % p.Hkv;
     const int d = p.d;
     const int64_t src = ((int64_t)b * p.Hkv + h) * d;
-    const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh + p.app_pos * d;
+    int64_t dst, ks_dst;
+    if (p.paged) {   // the last of the sequence's tokens, in its page
+        const int64_t pos = unit_len<true>(p, b) - 1;
+        if (pos < 0) return;
+        const int64_t row = pool_row(p, h, pool_token(p, b, pos));
+        dst = row * d;
+        ks_dst = row * p.d_sel;
+    } else {
+        dst = (int64_t)b * p.kv_sb + (int64_t)h * p.kv_sh + p.app_pos * d;
+        ks_dst = (int64_t)b * p.ks_sb + (int64_t)h * p.ks_sh + p.app_pos * p.d_sel;
+    }
     const int nq = d / 8;   // 16-byte pieces of a row
     for (int i = tid; i < 2 * nq; i += nthreads) {
         if (i < nq)
@@ -127,7 +200,7 @@ __device__ __forceinline__ void append_unit(const Params& p, int u, int tid, int
             flag(ws_status(p), DEV_BAD_INDEX);
             ch = ch < 0 ? 0 : d - 1;
         }
-        p.app_Ks[(int64_t)b * p.ks_sb + (int64_t)h * p.ks_sh + p.app_pos * p.d_sel + j] = p.k_new[src + ch];
+        p.app_Ks[ks_dst + j] = p.k_new[src + ch];
     }
 }
 
@@ -211,28 +284,64 @@ constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL, HIST>::SMEM; }
 // the CTAs in (unit, j) order; the stages j >= sf of all units form a queue, in
 // (unit, j) order, that the CTAs drain kGrab at a time once their own share is
 // done (a counter in unit 0's control block, zeroed by K0), so that CTAs that
-// stream faster take more of it.
+// stream faster take more of it.  A unit of n tokens has ceil(n / 512) stages,
+// sf = 3/4 of them (rounded down) static: the same for every unit of a
+// contiguous cache, per sequence for a paged one, whose stages are then
+// located through a cursor over the sequences.
+__host__ __device__ constexpr int32_t stages_of(int64_t n) { return (int32_t)((n + kStageTok - 1) / kStageTok); }
+__host__ __device__ constexpr int32_t static_of(int32_t nst) { return (int32_t)((int64_t)nst * 3 / 4); }
+
+// The sequence whose units hold index g of one part (static or queue) of a
+// paged schedule: its first index, stages per unit in the part, first stage
+// and length.
+struct K1Cursor {
+    int b;
+    int64_t base;
+    int32_t per, off, len;
+};
+
+// PAGED: every method is warp-collective (warp 0, all lanes, same results);
+// else thread 0 of the CTA runs them.
+template <bool PAGED>
 struct K1Sched {
     int64_t s_cur, s_end;      // this CTA's static stages [s_cur, s_end)
     int64_t d_cur, d_end;      // the current queue chunk
     int64_t pending;           // the next chunk's start (a grab in flight), or -1
-    int32_t sf, nd;            // static / queued stages per unit
     int64_t dtotal;            // queued stages in all
     uint32_t* counter;
     bool waited;
+    K1Cursor sc, dc;           // paged: the static and the queue cursor
 
-    __device__ void init(const Plan& pl, uint32_t* ctr)
+    __device__ void init(const Params& p, uint32_t* ctr)
     {
-        sf = pl.sf;
-        nd = pl.nst - pl.sf;
-        dtotal = (int64_t)pl.U * nd;
-        const int64_t st = (int64_t)pl.U * sf;
+        const Plan& pl = p.pl;
+        int64_t st;
+        if constexpr (!PAGED) {
+            st = (int64_t)pl.U * pl.sf;
+            dtotal = (int64_t)pl.U * (pl.nst - pl.sf);
+        } else {
+            long long a = 0, d = 0;
+            for (int b = (int)(threadIdx.x & 31); b < p.Bt; b += 32) {
+                const int32_t nst = stages_of(unit_len<true>(p, b)), sf = static_of(nst);
+                a += sf;
+                d += nst - sf;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, o);
+                d += __shfl_xor_sync(0xffffffffu, d, o);
+            }
+            st = (int64_t)a * p.Hkv;
+            dtotal = (int64_t)d * p.Hkv;
+        }
         s_cur = st * blockIdx.x / gridDim.x;
         s_end = st * (blockIdx.x + 1) / gridDim.x;
         d_cur = d_end = 0;
         pending = -1;
         counter = ctr;
         waited = false;
+        sc = K1Cursor{-1, 0, 0, 0, 0};
+        dc = sc;
     }
     __device__ int64_t grab()
     {
@@ -240,17 +349,72 @@ struct K1Sched {
             grid_dep_wait();   // K0 has zeroed the counter
             waited = true;
         }
-        return (int64_t)atomicAdd(counter, (uint32_t)kGrab);
+        if constexpr (!PAGED) return (int64_t)atomicAdd(counter, (uint32_t)kGrab);
+        uint32_t v = 0;
+        if ((threadIdx.x & 31) == 0) v = atomicAdd(counter, (uint32_t)kGrab);
+        return (int64_t)__shfl_sync(0xffffffffu, v, 0);
     }
-    // the next stage (unit, j); false at the end of the work
-    __device__ bool next(int& u, int& j)
+    // paged: move cursor c forward to the sequence holding index g of its
+    // part, 32 sequences at a time; false if no sequence does
+    __device__ bool seek(const Params& p, K1Cursor& c, int64_t g, bool queue)
+    {
+        const int lane = (int)(threadIdx.x & 31);
+#pragma unroll 1
+        while (g >= c.base + (int64_t)p.Hkv * c.per) {
+            if (c.b + 1 >= p.Bt) return false;
+            const int bb = c.b + 1 + lane;
+            int32_t len = 0, per = 0, off = 0;
+            if (bb < p.Bt) {
+                len = (int32_t)unit_len<true>(p, bb);
+                const int32_t nst = stages_of(len), sf = static_of(nst);
+                per = queue ? nst - sf : sf;
+                off = queue ? sf : 0;
+            }
+            const long long w = (long long)p.Hkv * per;
+            long long incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int64_t start = c.base + (int64_t)p.Hkv * c.per;   // sequence c.b + 1's first index
+            const uint32_t hit = __ballot_sync(0xffffffffu, bb < p.Bt && g < start + incl);
+            const int l = hit ? __ffs(hit) - 1 : min(31, p.Bt - 1 - (c.b + 1));
+            c.b = c.b + 1 + l;
+            c.base = start + __shfl_sync(0xffffffffu, incl - w, l);
+            c.per = __shfl_sync(0xffffffffu, per, l);
+            c.off = __shfl_sync(0xffffffffu, off, l);
+            c.len = __shfl_sync(0xffffffffu, len, l);
+        }
+        return true;
+    }
+    // index g of a part as (unit, j) and the unit's length
+    __device__ bool locate(const Params& p, int64_t g, bool queue, int& u, int& j, int64_t& len)
+    {
+        const Plan& pl = p.pl;
+        if constexpr (!PAGED) {
+            const int32_t per = queue ? pl.nst - pl.sf : pl.sf;
+            u = (int)(g / per);
+            j = (queue ? pl.sf : 0) + (int)(g % per);
+            len = pl.N;
+            return true;
+        } else {
+            K1Cursor& c = queue ? dc : sc;
+            if (!seek(p, c, g, queue)) return false;
+            const int64_t r = g - c.base;
+            u = c.b * p.Hkv + (int)(r / c.per);
+            j = c.off + (int)(r % c.per);
+            len = c.len;
+            return true;
+        }
+    }
+    // the next stage (unit, j) and its unit's length; false at the end of the work
+    __device__ bool next(const Params& p, int& u, int& j, int64_t& len)
     {
         if (s_cur < s_end) {
             const int64_t g = s_cur++;
-            u = (int)(g / sf);
-            j = (int)(g % sf);
             if (s_cur + 1 >= s_end && pending < 0 && dtotal > 0) pending = grab();   // one stage ahead
-            return true;
+            return locate(p, g, false, u, j, len);
         }
         if (d_cur == d_end) {
             if (dtotal == 0) return false;
@@ -260,14 +424,11 @@ struct K1Sched {
             d_end = min(pending + kGrab, dtotal);
             pending = grab();   // the next chunk's grab goes out now
         }
-        const int64_t d = d_cur++;
-        u = (int)(d / nd);
-        j = sf + (int)(d % nd);
-        return true;
+        return locate(p, d_cur++, true, u, j, len);
     }
 };
 
-template <int G, int DSEL, bool HIST, bool UBUF>
+template <int G, int DSEL, bool HIST, bool UBUF, bool PAGED>
 __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid_constant__ Params p)
 {
     using CF = K1Cfg<DSEL, HIST>;
@@ -294,51 +455,78 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
 
-    // the producer (thread 0): takes stage c, publishes its (unit, j) and
-    // issues its TMA copies (two 256-token boxes); false at the end marker
-    K1Sched sch;
+    // the producer (thread 0, or with a paged cache warp 0): takes stage c,
+    // publishes its (unit, j) and issues its TMA copies: two 256-token boxes
+    // of a contiguous summary, or one box per page (at most 256 tokens, a
+    // lane each) of a paged one, skipping the boxes past the sequence's end;
+    // false at the end marker
+    K1Sched<PAGED> sch;
     int c_issued = 0;
     bool ended = false;
     auto produce = [&](int c) -> bool {
         const int st = c % S;
-        if (c >= S && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+        if (c >= S) {
+            if (lane == 0 && !mbar_wait_bounded(&empty[st], (uint32_t)((c / S) - 1) & 1u)) flag(status, DEV_TIMEOUT);
+            if constexpr (PAGED) __syncwarp();
+        }
         int u = -1, j = 0;
-        if (!sch.next(u, j)) u = -1;
-        info[c % kInfo] = make_int2(u, j);
-        mbar_arrive(&ready[st]);
+        int64_t len = 0;
+        if (!sch.next(p, u, j, len)) u = -1;
+        if (lane == 0) {
+            info[c % kInfo] = make_int2(u, j);
+            mbar_arrive(&ready[st]);
+        }
         if (u < 0) {
-            mbar_arrive(&full[st]);   // the end marker carries no copies
+            if (lane == 0) mbar_arrive(&full[st]);   // the end marker carries no copies
             return false;
         }
         const int b = u / p.Hkv, h = u % p.Hkv;
-        mbar_arrive_expect_tx(&full[st], CF::STAGE);
         unsigned char* dst = ring + (size_t)st * CF::STAGE;
         const uint64_t pol = l2_policy_evict_first();
-        tma_load_4d(dst, &p.ks_map, 0, j * kStageTok, h, b, &full[st], pol);
-        tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
+        if constexpr (!PAGED) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[st], CF::STAGE);
+                tma_load_4d(dst, &p.ks_map, 0, j * kStageTok, h, b, &full[st], pol);
+                tma_load_4d(dst + CF::BOX, &p.ks_map, 0, j * kStageTok + 256, h, b, &full[st], pol);
+            }
+        } else {
+            const int64_t t0 = (int64_t)j * kStageTok;
+            const int nbox = (int)((min((int64_t)kStageTok, len - t0) + (1 << p.log_box) - 1) >> p.log_box);
+            const uint32_t box_bytes = (CF::ROW << p.log_box);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)nbox * box_bytes);
+            __syncwarp();
+            for (int i = lane; i < nbox; i += 32) {
+                const int64_t t = t0 + ((int64_t)i << p.log_box);
+                tma_load_4d(dst + (size_t)i * box_bytes, &p.ks_map, 0, (int)(t & ((1 << p.log_ps) - 1)), h,
+                            page_of(p, b, t), &full[st], pol);
+            }
+        }
         return true;
     };
-    if (tid == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 2);    // the summary copies (with their bytes) + the query operand
-            mbar_init(&empty[i], 1);
-            mbar_init(&ready[i], 1);
+    if (PAGED ? warp == 0 : tid == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < S; ++i) {
+                mbar_init(&full[i], 2);    // the summary copies (with their bytes) + the query operand
+                mbar_init(&empty[i], 1);
+                mbar_init(&ready[i], 1);
+            }
+            for (int i = 0; i < NB; ++i) {
+                mbar_init(&tfull[i], 1);
+                mbar_init(&tempty[i], k1EpiThreads / 32);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&hdone[i], k1EpiThreads / 32);
+                mbar_init(&hfree[i], kHistWarps);
+            }
+            hctl[2] = 0;
+            fence_mbar_init();
+            tma_prefetch_desc(&p.ks_map);
         }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], k1EpiThreads / 32);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&hdone[i], k1EpiThreads / 32);
-            mbar_init(&hfree[i], kHistWarps);
-        }
-        hctl[2] = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&p.ks_map);
+        if constexpr (PAGED) __syncwarp();
         // the first stage's copies go out before the block-wide set-up ends;
         // the rest of the ring follows it (each issue takes a few hundred
         // cycles, and the query operand waits for the set-up barrier)
-        sch.init(pl, &ws_ctrl(p)[0].k1_next);
+        sch.init(p, &ws_ctrl(p)[0].k1_next);
         for (; c_issued < kPreIssue && !ended; ++c_issued) ended = !produce(c_issued);
     }
     if constexpr (HIST) {
@@ -363,7 +551,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
         nsel = (lane < DSEL) ? __ldg(p.sel_ch + (int64_t)hh * DSEL + lane) : 0;
     };
     int first_u = -1;
-    if (warp == 3) {
+    if (warp == 3 && !PAGED) {
         const int64_t st = (int64_t)pl.U * pl.sf;
         const int64_t g0 = st * blockIdx.x / gridDim.x;
         if (g0 < st * (blockIdx.x + 1) / gridDim.x) {
@@ -383,7 +571,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
 
     if (warp == 0) {
         // the producer carries on from where the set-up left it
-        if (lane == 0) {
+        if (PAGED || lane == 0) {
 #pragma unroll 1
             for (int c = c_issued; !ended; ++c) ended = !produce(c);
         }
@@ -519,6 +707,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
         uint32_t ub = 0u, uh = 0u;          // the unit's batch and KV head
         float* srow = nullptr;
         uint16_t* urow = nullptr;
+        int64_t nu = 0;                     // the unit's tokens
         const uint32_t tl = ((uint32_t)(quarter * 32) << 16) + (uint32_t)tile * 16u;   // lane quarter, tile columns
 #pragma unroll 1
         for (int c = 0;; ++c) {
@@ -547,6 +736,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
                 ub = (uint32_t)(u / p.Hkv);
                 uh = (uint32_t)(u % p.Hkv);
                 srow = p.s_dst + (int64_t)u * pl.N;
+                nu = unit_len<PAGED>(p, (int)ub);
                 if constexpr (UBUF) urow = ws_ubuf(p) + (int64_t)u * pl.np;
             }
             if constexpr (HIST) ++run;
@@ -570,7 +760,7 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[nb]);
-            if (t < pl.N) {
+            if (t < nu) {
                 const float s = best * p.scale;
                 if (!isfinite(s)) flag(status, DEV_NONFINITE);
                 srow[t] = s;

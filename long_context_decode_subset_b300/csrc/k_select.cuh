@@ -194,13 +194,13 @@ __device__ __noinline__ void resolve_ties(const Params& p, int u, uint32_t pre24
     __syncthreads();
 }
 
-__device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, uint32_t above1, uint32_t target, float m,
-                                         SelShared& sh, uint2* cs)
+__device__ __noinline__ void resolve_unit(const Params& p, int u, int64_t nu, uint32_t f1, uint32_t above1,
+                                         uint32_t target, float m, SelShared& sh, uint2* cs)
 {
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
-    const bool want_z = p.budget > 0.0f && p.strata != 1;   // the uniform sampler's Z is N - k
+    const bool want_z = p.budget > 0.0f && p.strata != 1;   // the uniform sampler's Z is n - k
     const TilePart* tp = reinterpret_cast<const TilePart*>(ws_zpart(p)) + (size_t)u * pl.tcap;
     // one wave of loads: the tiles' candidate counts and shares of Z (two
     // tiles per thread: at most kMaxTiles tiles) and the candidates' level-2
@@ -394,7 +394,7 @@ __device__ __noinline__ void resolve_unit(const Params& p, int u, uint32_t f1, u
         sh.r_theta = theta;
         sh.r_cut = (int32_t)idx_cut;
         sh.r_m = m;
-        sh.r_Z = (p.strata == 1) ? p.z_uniform : __fadd_rn(hh, ll);
+        sh.r_Z = (p.strata == 1) ? uniform_z(p, nu) : __fadd_rn(hh, ll);
     }
 }
 
@@ -540,8 +540,8 @@ __device__ MassPick mass_pick(const unsigned long long* h, double target, bool f
 // histogram h.  Shared memory: NB * 20 bytes of histogram, then 16 warps'
 // 256-score staging (16 KB).
 template <int NB>
-__device__ void mass_level(const Params& p, int u, int tile, float M, uint32_t prefix, int hi_shift, int lo_shift,
-                           unsigned long long* h, unsigned char* smem)
+__device__ void mass_level(const Params& p, int u, int tile, int64_t nu, float M, uint32_t prefix, int hi_shift,
+                           int lo_shift, unsigned long long* h, unsigned char* smem)
 {
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -569,7 +569,7 @@ __device__ void mass_level(const Params& p, int u, int tile, float M, uint32_t p
         __syncwarp();
 #pragma unroll 1
         for (int i = lane; i < n; i += 32) {
-            if (base + c0 + i >= pl.N) continue;
+            if (base + c0 + i >= nu) continue;
             const float sv = stg[i];
             const uint32_t k = okey(sv);
             if (hi_shift < 32 && (k >> hi_shift) != prefix) continue;
@@ -604,9 +604,11 @@ __device__ __forceinline__ void mass_level_arrive(const Params& p, int u, int le
     __syncthreads();
 }
 
-// The size of unit u's top-p stratum (every CTA of the unit returns the same
-// value, at least 1).  Block-wide; uses the first 96 KB of `smem`.
-__device__ __noinline__ uint32_t topp_size(const Params& p, int u, int tile, SelShared& sh, unsigned char* smem)
+// The size of unit u's top-p stratum over its nu tokens (every CTA of the
+// unit returns the same value, at least 1).  Block-wide; uses the first 96 KB
+// of `smem`.
+__device__ __noinline__ uint32_t topp_size(const Params& p, int u, int tile, int64_t nu, SelShared& sh,
+                                           unsigned char* smem)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     unsigned long long* h0 = ws_topp(p) + (size_t)u * kTopPBins * 3;
@@ -630,17 +632,17 @@ __device__ __noinline__ uint32_t topp_size(const Params& p, int u, int tile, Sel
         M = 3.4028234663852886e38f;
     }
     // level 0: the 12-bit order-key buckets
-    mass_level<4096>(p, u, tile, M, 0u, 32, 20, h0, smem);
+    mass_level<4096>(p, u, tile, nu, M, 0u, 32, 20, h0, smem);
     mass_level_arrive(p, u, 0);
     const MassPick a = mass_pick<4096>(h0, (double)p.top_p, true, sh);
     const double t1 = (double)p.top_p * a.total - a.mass_above;   // the target left inside bucket a
     // level 1: the next 12 bits of bucket a's members
-    mass_level<4096>(p, u, tile, M, a.bin, 20, 8, h1, smem);
+    mass_level<4096>(p, u, tile, nu, M, a.bin, 20, 8, h1, smem);
     mass_level_arrive(p, u, 1);
     const MassPick b = mass_pick<4096>(h1, t1, false, sh);
     const double t2 = t1 - b.mass_above;
     // level 2: the last 8 bits of the members sharing those 24 bits
-    mass_level<256>(p, u, tile, M, (a.bin << 12) | b.bin, 8, 0, h2, smem);
+    mass_level<256>(p, u, tile, nu, M, (a.bin << 12) | b.bin, 8, 0, h2, smem);
     mass_level_arrive(p, u, 2);
     const MassPick c = mass_pick<256>(h2, t2, false, sh);
     // the crossing key's ties have equal terms: the stratum takes the fewest
@@ -671,8 +673,8 @@ struct TileSel {
 // Philox prefixes); the resolve stages candidates in the same bytes.
 constexpr uint32_t kSelStageBytes = (uint32_t)kSelWarps * kSlice * 2u * 6u;
 
-__device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint32_t k_unit, SelShared& sh,
-                                          unsigned char* k2dyn)
+__device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, int64_t nu, uint32_t k_unit,
+                                          SelShared& sh, unsigned char* k2dyn)
 {
     const Plan& pl = p.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -681,11 +683,13 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint
     SSA_MARK(2);
 
     const int64_t base = (int64_t)tile * pl.tt + (int64_t)warp * W2;   // this warp's first token
+    // the part of the slice inside the unit's nu tokens (chunks past it are not walked)
+    const int Wv = (int)max((int64_t)0, min((int64_t)W2, nu - base));
     const float* S = p.s_src + (int64_t)u * pl.N;
     const uint16_t* ub = ws_ubuf(p) + (size_t)u * pl.np + base;
     const float B = p.budget;
     const bool sampling = B > 0.0f;
-    const bool uniform = p.strata == 1;   // every remainder token has the same p: e = 1, Z = N - k
+    const bool uniform = p.strata == 1;   // every remainder token has the same p: e = 1, Z = n - k
     // Each warp stages its slice kSlice tokens at a time (scores and Philox
     // prefixes, cp.async) into two buffers: the next chunk's copies are in
     // flight while the current one is walked.  The first chunk's copies go
@@ -712,7 +716,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint
         }
         cp_async_commit();
     };
-    stage(0);   // the caller runs the pass only when N > 0
+    if (Wv > 0) stage(0);
 
     // bucket f1 of the k-th score (the largest when k = 0): each thread reads
     // 8 bins of the unit's histogram, top bin first
@@ -773,7 +777,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint
         for (int w = 0; w < kSelWarps; ++w) zlb += sh.zlb[w];
         zlb *= 0.999f;
     }
-    if (uniform) zlb = p.z_uniform;   // the exact normaliser
+    if (uniform) zlb = uniform_z(p, nu);   // the exact normaliser
     // u >= prefix * 2^-16 >= B e / Z_lb >= p (any Z >= Z_lb): the token cannot be drawn
     const float bound_scale = (zlb > 0.0f) ? __fdiv_ru(B, zlb) : INFINITY;
     SSA_MARK(17);
@@ -789,10 +793,10 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint
     // the prefix test in units of 2^-16: prefix < B e / Z_lb * 2^16 (a power-of-two scale, exact)
     const float bound16 = __fmul_rn(bound_scale, 65536.0f);
 #pragma unroll 1
-    for (int c0 = 0; c0 < W2; c0 += kSlice) {
+    for (int c0 = 0; c0 < Wv; c0 += kSlice) {
         // the next chunk's copies go out before this one is walked
         if (c0 / kSlice < 4) SSA_MARKG(16 + c0 / kSlice);
-        if (c0 + kSlice < W2) {
+        if (c0 + kSlice < Wv) {
             __syncwarp();
             stage(c0 + kSlice);
             cp_async_wait<1>();
@@ -803,8 +807,8 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, uint
         const float* csc = ssc + ((c0 / kSlice) & 1) * kSlice;
         const uint16_t* csu = su + ((c0 / kSlice) & 1) * kSlice;
         const int n = min(kSlice, W2 - c0);   // a multiple of 32
-        // tokens [0, nvalid) of the chunk are in the cache (the last tile's tail is not)
-        const int nvalid = (int)min((int64_t)n, pl.N - (base + c0));
+        // tokens [0, nvalid) of the chunk are in the cache (the unit's tail past nu is not)
+        const int nvalid = (int)min((int64_t)n, nu - (base + c0));
         const uint32_t t0 = (uint32_t)(base + c0);   // token indices fit 31 bits
         // each lane takes four consecutive tokens of a 128-token group; the
         // group's kept tokens are listed in index order at the warp's

@@ -117,7 +117,16 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     return pl;
 }
 
-ssa_status check_shape(const ssa_shape* s)
+// Which stride fields a shape must carry: a contiguous cache's, all zero (a
+// paged cache), or either (the calls that only size things).
+enum StrideRule { kStridesContig, kStridesZero, kStridesAny };
+
+bool zero_strides(const ssa_shape* s)
+{
+    return s->kv_stride_b == 0 && s->kv_stride_h == 0 && s->ks_stride_b == 0 && s->ks_stride_h == 0;
+}
+
+ssa_status check_shape(const ssa_shape* s, StrideRule rule = kStridesContig)
 {
     if (!s) return SSA_ERR_INVALID_ARG;
     if (s->batch < 0 || s->n_kv_heads < 1 || s->n_q_heads < 1 || s->reserved != 0) return SSA_ERR_INVALID_ARG;
@@ -128,6 +137,8 @@ ssa_status check_shape(const ssa_shape* s)
     if (s->d_sel != 16 && s->d_sel != 32) return SSA_ERR_UNSUPPORTED;
     if (s->ctx_len < 0 || s->ctx_len > (int64_t)INT32_MAX - 4096) return SSA_ERR_INVALID_ARG;
     if ((int64_t)s->batch * s->n_kv_heads > (int64_t)INT32_MAX / (kMaxTiles * 2)) return SSA_ERR_UNSUPPORTED;
+    if (rule != kStridesContig && zero_strides(s)) return SSA_OK;
+    if (rule == kStridesZero) return SSA_ERR_INVALID_ARG;
     const int64_t N = s->ctx_len;
     if (s->kv_stride_h < N * s->head_dim || s->ks_stride_h < N * s->d_sel) return SSA_ERR_INVALID_ARG;
     if (s->kv_stride_b < (int64_t)(s->n_kv_heads - 1) * s->kv_stride_h + N * s->head_dim) return SSA_ERR_INVALID_ARG;
@@ -188,7 +199,6 @@ int64_t set_strata(ssa::Params& p, int strata, int64_t top_k, float top_p, int64
         }
     }
     p.top_k = top_k;
-    p.z_uniform = (float)(N - std::min<int64_t>(top_k, N));
     return top_k;
 }
 bool bad_scale(float scale) { return !(scale > 0.0f) || !std::isfinite(scale); }
@@ -229,44 +239,97 @@ ssa_status encode_summary_map(CUtensorMap* map, const ssa_bf16* Ks, const ssa_sh
     return r == CUDA_SUCCESS ? SSA_OK : SSA_ERR_CUDA;
 }
 
-typedef void (*kfn_t)(ssa::Params);
-
-template <int G, int DSEL>
-kfn_t pick_score_hd(bool hist)
+// A paged summary pool [num_pages][Hkv][page_size][d_sel] as a 4-D tensor:
+// boxes of min(page_size, 256) tokens of one page and head, swizzled as above
+// (a box lands where the 256-token box would put its rows).
+ssa_status encode_paged_map(CUtensorMap* map, const ssa_bf16* Ks_pool, const ssa_paged_kv& pg, const ssa_shape& s)
 {
-    return hist ? &score_kernel<G, DSEL, true, true> : &score_kernel<G, DSEL, false, false>;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return SSA_ERR_CUDA;
+    const cuuint64_t row = (cuuint64_t)s.d_sel * 2;
+    cuuint64_t dims[4] = {(cuuint64_t)s.d_sel, (cuuint64_t)pg.page_size, (cuuint64_t)s.n_kv_heads,
+                          (cuuint64_t)pg.num_pages};
+    cuuint64_t strides[3] = {row, row * (cuuint64_t)pg.page_size, row * (cuuint64_t)pg.page_size * s.n_kv_heads};
+    cuuint32_t box[4] = {(cuuint32_t)s.d_sel, (cuuint32_t)std::min(pg.page_size, 256), 1u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<ssa_bf16*>(Ks_pool), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           s.d_sel == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SSA_OK : SSA_ERR_CUDA;
 }
 
-kfn_t pick_score(int G, int dsel, bool hist)
+int log2_exact(int64_t v)
+{
+    int l = 0;
+    while (((int64_t)1 << l) < v) ++l;
+    return l;
+}
+
+// A paged cache's description, checked against the shape.
+ssa_status check_paged(const ssa_paged_kv* pg, const ssa_shape& s)
+{
+    if (!pg || !pg->block_table || !pg->seq_lens) return SSA_ERR_INVALID_ARG;
+    const int64_t ps = pg->page_size;
+    if (ps < 16 || ps > (1 << 20) || (ps & (ps - 1)) != 0) return SSA_ERR_INVALID_ARG;
+    if (pg->max_pages < 1 || pg->num_pages < 1) return SSA_ERR_INVALID_ARG;
+    if (pg->num_pages > (int64_t)INT32_MAX / ps) return SSA_ERR_INVALID_ARG;   // pool tokens fit 31 bits
+    if (s.ctx_len > (int64_t)pg->max_pages * ps) return SSA_ERR_INVALID_ARG;
+    return SSA_OK;
+}
+
+typedef void (*kfn_t)(ssa::Params);
+
+template <int G, int DSEL, bool PAGED>
+kfn_t pick_score_hd(bool hist)
+{
+    return hist ? &score_kernel<G, DSEL, true, true, PAGED> : &score_kernel<G, DSEL, false, false, PAGED>;
+}
+
+template <bool PAGED>
+kfn_t pick_score_p(int G, int dsel, bool hist)
 {
     switch (G) {
-        case 1: return dsel == 16 ? pick_score_hd<1, 16>(hist) : pick_score_hd<1, 32>(hist);
-        case 2: return dsel == 16 ? pick_score_hd<2, 16>(hist) : pick_score_hd<2, 32>(hist);
-        case 4: return dsel == 16 ? pick_score_hd<4, 16>(hist) : pick_score_hd<4, 32>(hist);
-        default: return dsel == 16 ? pick_score_hd<8, 16>(hist) : pick_score_hd<8, 32>(hist);
+        case 1: return dsel == 16 ? pick_score_hd<1, 16, PAGED>(hist) : pick_score_hd<1, 32, PAGED>(hist);
+        case 2: return dsel == 16 ? pick_score_hd<2, 16, PAGED>(hist) : pick_score_hd<2, 32, PAGED>(hist);
+        case 4: return dsel == 16 ? pick_score_hd<4, 16, PAGED>(hist) : pick_score_hd<4, 32, PAGED>(hist);
+        default: return dsel == 16 ? pick_score_hd<8, 16, PAGED>(hist) : pick_score_hd<8, 32, PAGED>(hist);
     }
 }
 
-template <int G>
+// The score kernel for this group size, summary width, histogram choice and cache layout.
+kfn_t pick_score(int G, int dsel, bool hist, bool paged)
+{
+    return paged ? pick_score_p<true>(G, dsel, hist) : pick_score_p<false>(G, dsel, hist);
+}
+
+template <int G, bool PAGED>
 kfn_t unit_fn(int d, uint32_t* smem)
 {
     if (d == 128) {
         *smem = unit_smem_bytes<G, 128, 4096>();
-        return &unit_kernel<G, 128, 4096>;
+        return &unit_kernel<G, 128, 4096, PAGED>;
     }
     *smem = unit_smem_bytes<G, 64, 4096>();
-    return &unit_kernel<G, 64, 4096>;
+    return &unit_kernel<G, 64, 4096, PAGED>;
 }
 
-// The unit kernel for this group size and head_dim, and its dynamic shared memory.
-kfn_t pick_unit(int G, int d, uint32_t* smem)
+template <bool PAGED>
+kfn_t pick_unit_p(int G, int d, uint32_t* smem)
 {
     switch (G) {
-        case 1: return unit_fn<1>(d, smem);
-        case 2: return unit_fn<2>(d, smem);
-        case 4: return unit_fn<4>(d, smem);
-        default: return unit_fn<8>(d, smem);
+        case 1: return unit_fn<1, PAGED>(d, smem);
+        case 2: return unit_fn<2, PAGED>(d, smem);
+        case 4: return unit_fn<4, PAGED>(d, smem);
+        default: return unit_fn<8, PAGED>(d, smem);
     }
+}
+
+// The unit kernel for this group size, head_dim and cache layout, and its
+// dynamic shared memory.
+kfn_t pick_unit(int G, int d, uint32_t* smem, bool paged = false)
+{
+    return paged ? pick_unit_p<true>(G, d, smem) : pick_unit_p<false>(G, d, smem);
 }
 
 // Raise `fn`'s dynamic shared-memory limit to `smem` (static plus dynamic
@@ -352,7 +415,8 @@ ssa_status launch_score(const ssa::Params& p, const ssa_shape& s, bool hist, cud
 {
     const uint32_t smem = s.d_sel == 32 ? (hist ? k1_smem_bytes<32, true>() : k1_smem_bytes<32, false>())
                                         : (hist ? k1_smem_bytes<16, true>() : k1_smem_bytes<16, false>());
-    return launch(pick_score(p.pl.G, s.d_sel, hist), p.pl.k1_grid, k1_threads(hist), smem, p, stream, dependent);
+    return launch(pick_score(p.pl.G, s.d_sel, hist, p.paged != 0), p.pl.k1_grid, k1_threads(hist), smem, p, stream,
+                  dependent);
 }
 
 // CTAs of `fn` resident per SM (cached per kernel, shared-memory size and device).
@@ -408,7 +472,7 @@ ssa::Plan unit_plan(const ssa_shape& s)
 ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream, bool dependent)
 {
     uint32_t smem = 0;
-    kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem);
+    kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem, p.paged != 0);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
     return launch(fn, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, smem, p, stream, dependent);
 }
@@ -501,13 +565,13 @@ int ssa_version(void) { return 200; }
 size_t ssa_workspace_bytes(const ssa_shape* shape, int64_t list_cap)
 {
     (void)list_cap;
-    if (check_shape(shape) != SSA_OK) return 0;
+    if (check_shape(shape, kStridesAny) != SSA_OK) return 0;
     return make_plan(*shape, 0).total;
 }
 
 size_t ssa_select_capacity(const ssa_shape* shape)
 {
-    if (check_shape(shape) != SSA_OK) return 0;
+    if (check_shape(shape, kStridesAny) != SSA_OK) return 0;
     return (size_t)shape->ctx_len;
 }
 
@@ -648,15 +712,17 @@ void set_append(ssa::Params& p, const AppendArgs& a, int64_t pos, const ssa_shap
     p.ks_sh = s.ks_stride_h;
 }
 
-ssa_status decode_impl(const AppendArgs* app, int strata, float top_p, bool host_io, const ssa_bf16* q, const ssa_bf16* K,
-                       const ssa_bf16* V,
-                       const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed,
-                       float scale, float* out, float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt,
-                       int32_t* count_opt, int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
-                       cudaStream_t stream)
+// The step.  `pg` (may be null) describes a paged cache: K, V and Ks are
+// then its pools.
+ssa_status decode_impl(const AppendArgs* app, const ssa_paged_kv* pg, int strata, float top_p, bool host_io,
+                       const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
+                       const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale, float* out,
+                       float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
+                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
 {
-    ssa_status st = check_shape(shape);
+    ssa_status st = check_shape(shape, pg ? kStridesZero : kStridesContig);
     if (st != SSA_OK) return st;
+    if (pg && (st = check_paged(pg, *shape)) != SSA_OK) return st;
     const bool empty = shape->ctx_len == 0;  // nothing is read from the cache
     if (!q || !sel_ch || !out || !lse || (!empty && (!K || !V || !Ks))) return SSA_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
@@ -669,10 +735,23 @@ ssa_status decode_impl(const AppendArgs* app, int strata, float top_p, bool host
     if (!device_readable(K, true) || !device_readable(V, true) || !device_readable(Ks, false) ||
         !device_readable(q, host_io) || !device_readable(out, host_io) || !device_readable(lse, host_io))
         return SSA_ERR_INVALID_ARG;
+    if (pg && (!device_readable(pg->block_table, false) || !device_readable(pg->seq_lens, false)))
+        return SSA_ERR_INVALID_ARG;
     if (pl.U == 0) return SSA_OK;
     char* w = static_cast<char*>(ws);
     ssa::Params prm = base_params(*shape, pl, ws);
-    if (!empty && (st = encode_summary_map(&prm.ks_map, Ks, *shape)) != SSA_OK) return st;
+    if (pg) {
+        prm.paged = 1;
+        prm.log_ps = log2_exact(pg->page_size);
+        prm.log_box = std::min(prm.log_ps, 8);
+        prm.max_pages = pg->max_pages;
+        prm.num_pages = pg->num_pages;
+        prm.block_table = pg->block_table;
+        prm.seq_lens = pg->seq_lens;
+    }
+    if (!empty && (st = pg ? encode_paged_map(&prm.ks_map, Ks, *pg, *shape) : encode_summary_map(&prm.ks_map, Ks, *shape)) !=
+                      SSA_OK)
+        return st;
     prm.q = q;
     if (host_io) {   // the first kernel stages the query from host memory into the workspace
         prm.q = reinterpret_cast<const ssa_bf16*>(w + pl.o_hq);
@@ -699,10 +778,11 @@ ssa_status decode_impl(const AppendArgs* app, int strata, float top_p, bool host
     prm.src_mode = prm.dense ? 1 : 0;
     prm.attend = 1;
     if (app) {
-        // K0 writes the new token at ctx_len - 1.  The score kernel reads that
-        // summary row only from its shared queue (the last stage is never in
-        // a CTA's static share: sf < number of stages), i.e. after its wait
-        // for K0; the attention reads rows after its own wait.
+        // K0 writes the new token at ctx_len - 1 (paged: at each sequence's
+        // last position).  The score kernel reads that summary row only from
+        // its shared queue (the last stage of a unit is never in a CTA's
+        // static share: sf < number of stages), i.e. after its wait for K0;
+        // the attention reads rows after its own wait.
         if (pl.sf >= pl.nst) return SSA_ERR_UNSUPPORTED;
         set_append(prm, *app, shape->ctx_len - 1, *shape);
     }
@@ -725,7 +805,7 @@ ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
                       float* lse, float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                       int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
 {
-    return decode_impl(nullptr, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out,
+    return decode_impl(nullptr, nullptr, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out,
                        lse, s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
@@ -736,7 +816,7 @@ ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
                              const ssa_shape* shape, cudaStream_t stream)
 {
     if (bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
-    return decode_impl(nullptr, strata, top_p, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+    return decode_impl(nullptr, nullptr, strata, top_p, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
                        s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
@@ -750,8 +830,23 @@ ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa
     if (shape->ctx_len < 1 || !k_new || !v_new || !K || !V || !Ks) return SSA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SSA_ERR_INVALID_ARG;
     const AppendArgs app{k_new, v_new, K, V, Ks};
-    return decode_impl(&app, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
+    return decode_impl(&app, nullptr, SSA_STRATA_SSA, 0.0f, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
                        nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
+}
+
+ssa_status ssa_decode_paged(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K_pool,
+                            ssa_bf16* V_pool, ssa_bf16* Ks_pool, const ssa_paged_kv* pages, const int32_t* sel_ch,
+                            int64_t top_k, float budget, uint64_t seed, float scale, float* out, float* lse,
+                            float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt, int64_t list_cap,
+                            void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
+{
+    if (!pages || (k_new == nullptr) != (v_new == nullptr)) return SSA_ERR_INVALID_ARG;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return SSA_ERR_INVALID_ARG;
+    if (k_new && shape && shape->ctx_len < 1) return SSA_ERR_INVALID_ARG;
+    const AppendArgs app{k_new, v_new, K_pool, V_pool, Ks_pool};
+    return decode_impl(k_new ? &app : nullptr, pages, SSA_STRATA_SSA, 0.0f, false, q, K_pool,
+                       V_pool, Ks_pool, sel_ch, top_k, budget, seed, scale, out, lse, s_hat_opt, idx_opt, p_opt,
+                       count_opt, list_cap, ws, ws_bytes, shape, stream);
 }
 
 ssa_status ssa_append(const ssa_bf16* k_new, const ssa_bf16* v_new, const int32_t* sel_ch, int64_t pos,
@@ -783,7 +878,7 @@ ssa_status ssa_decode_host(const ssa_bf16* q_host, const ssa_bf16* K, const ssa_
     // pinned, mapped buffers: the kernels read q from host memory and write
     // out / lse into it (no copy is enqueued)
     if (device_readable(q_host, true) && device_readable(out_host, true) && device_readable(lse_host, true))
-        return decode_impl(nullptr, SSA_STRATA_SSA, 0.0f, true, q_host, K, V, Ks, sel_ch, top_k, budget, seed, scale,
+        return decode_impl(nullptr, nullptr, SSA_STRATA_SSA, 0.0f, true, q_host, K, V, Ks, sel_ch, top_k, budget, seed, scale,
                            out_host, lse_host, nullptr, nullptr, nullptr, nullptr, 0, ws, ws_bytes, shape, stream);
     // otherwise one staged copy in, the step, two staged copies out
     const ssa::Plan pl = make_plan(*shape, 0);
@@ -857,7 +952,7 @@ ssa_status ssa_get_device_status(void* ws, cudaStream_t stream, uint32_t* flags_
 ssa_status ssa_query_plan(const ssa_shape* shape, int32_t* score_ctas, int32_t* tiles_per_unit,
                           int32_t* attend_ctas_per_unit)
 {
-    const ssa_status st = check_shape(shape);
+    const ssa_status st = check_shape(shape, kStridesAny);
     if (st != SSA_OK) return st;
     const ssa::Plan pl = unit_plan(*shape);
     if (score_ctas) *score_ctas = pl.k1_grid;

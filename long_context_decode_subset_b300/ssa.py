@@ -29,7 +29,7 @@ EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
     "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append", "ssa_select_capacity",
-    "ssa_select_strata", "ssa_decode_strata",
+    "ssa_select_strata", "ssa_decode_strata", "ssa_decode_paged",
 ]
 STRATA_SSA, STRATA_UNIFORM, STRATA_TOP_P = 0, 1, 2
 
@@ -46,6 +46,13 @@ class ssa_shape(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("d_sel", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("ctx_len", ctypes.c_int64), ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64),
         ("ks_stride_b", ctypes.c_int64), ("ks_stride_h", ctypes.c_int64),
+    ]
+
+
+class ssa_paged_kv(ctypes.Structure):
+    _fields_ = [
+        ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
     ]
 
 
@@ -83,6 +90,8 @@ def load_library():
         "ssa_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
         "ssa_query_plan": ([SP, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], ctypes.c_int),
         "ssa_decode_static": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, SP, P], ctypes.c_int),
+        "ssa_decode_paged": ([P, P, P, P, P, P, ctypes.POINTER(ssa_paged_kv), P, i64, f32, u64, f32, P, P, P, P, P,
+                              P, i64, P, sz, SP, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -325,6 +334,47 @@ def ssa_decode_append(q, k_new, v_new, K, V, Ks, sel_ch, top_k: int, budget: flo
                                             _ptr(sel_ch), int(top_k), float(budget), int(seed) & (2**64 - 1),
                                             float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                             ctypes.byref(shape), _stream(stream)), "ssa_decode_append")
+    return out, lse
+
+
+def paged_shape(q: torch.Tensor, K_pool: torch.Tensor, Ks_pool: torch.Tensor, ctx_len: int) -> ssa_shape:
+    """Shape of a paged step: q [Bt][Hq][d], pools [num_pages][Hkv][page_size][d / d_sel], longest sequence ctx_len
+    (the stride fields are 0)."""
+    Bt, Hq, d = q.shape
+    _, Hkv, _, _ = K_pool.shape
+    return ssa_shape(Bt, Hq, Hkv, d, Ks_pool.shape[-1], 0, int(ctx_len), 0, 0, 0, 0)
+
+
+def ssa_decode_paged(q, K_pool, V_pool, Ks_pool, block_table, seq_lens, sel_ch, top_k: int, budget: float, seed: int,
+                     scale: float, ctx_len: int, k_new=None, v_new=None, out=None, lse=None, s_hat=None, idx=None,
+                     p=None, count=None, list_cap: int = 0, ws=None, stream=None):
+    """The step over a paged, variable-length cache; returns (out, lse).
+
+    K_pool, V_pool [num_pages][Hkv][page_size][d] and Ks_pool [num_pages][Hkv][page_size][d_sel] (contiguous),
+    block_table [Bt][max_pages] and seq_lens [Bt] int32 on the device, ctx_len >= every seq_lens[b].  With k_new /
+    v_new [Bt][Hkv][d] the new token is first written at position seq_lens[b] - 1 of each sequence."""
+    for t in (K_pool, V_pool, Ks_pool, block_table, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("pools, block table and lengths must be contiguous")
+    num_pages, Hkv, page_size, d = K_pool.shape
+    Bt, Hq, _ = q.shape
+    if tuple(block_table.shape[:1]) != (Bt,) or tuple(seq_lens.shape) != (Bt,):
+        raise ValueError("block_table must be [Bt][max_pages] and seq_lens [Bt]")
+    shape = paged_shape(q, K_pool, Ks_pool, ctx_len)
+    pages = ssa_paged_kv(page_size, block_table.shape[1], num_pages, block_table.data_ptr(), seq_lens.data_ptr())
+    if out is None:
+        out = torch.empty((Bt, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Bt, Hq), dtype=torch.float32, device=q.device)
+    cap = list_cap if list_cap > 0 else (idx.shape[-1] if idx is not None else 0)
+    if ws is None:
+        ws = workspace(shape, cap, q.device)
+    _check(load_library().ssa_decode_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_pool), _ptr(V_pool),
+                                           _ptr(Ks_pool), ctypes.byref(pages), _ptr(sel_ch), int(top_k),
+                                           float(budget), int(seed) & (2**64 - 1), float(scale), _ptr(out),
+                                           _ptr(lse), _ptr(s_hat), _ptr(idx), _ptr(p), _ptr(count), int(cap),
+                                           _ptr(ws), ws.numel(), ctypes.byref(shape), _stream(stream)),
+           "ssa_decode_paged")
     return out, lse
 
 

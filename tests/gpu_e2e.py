@@ -46,24 +46,27 @@ def gpu_decode(w, k, B, seed, Ks=None, list_cap=0):
     return dict(out=out, lse=lse, s_hat=s_hat, idx=idx, p=p, count=count, status=st, flags=flags)
 
 
-def unit_arrays(oracle_mod, w, b, h):
-    """Host copies of one unit's inputs (q heads, K, V, the oracle's own key summary, channels)."""
+def unit_arrays(oracle_mod, w, b, h, n=None):
+    """Host copies of one unit's inputs (q heads, its first n (default: all) K and V rows, the oracle's own key
+    summary of them, channels)."""
     G = w["q"].shape[1] // w["K"].shape[1]
-    Kb = u16(w["K"][b, h])
+    n = w["K"].shape[2] if n is None else n
+    Kb = u16(w["K"][b, h, :n])
     sel_h = w["sel_ch"][h].cpu().numpy()
     Ksb = oracle_mod.pack_summary(Kb[None, None], sel_h[None], sel_h.size)[0, 0]
-    return u16(w["q"][b, h * G:(h + 1) * G]), Kb, u16(w["V"][b, h]), Ksb, sel_h
+    return u16(w["q"][b, h * G:(h + 1) * G]), Kb, u16(w["V"][b, h, :n]), Ksb, sel_h
 
 
-def check_unit(oracle_mod, w, g, b, h, k, B, seed, stats):
-    """Oracle for unit (b, h) computed from scratch; compare with the GPU's results."""
-    qh, Kb, Vb, Ksb, sel_h = unit_arrays(oracle_mod, w, b, h)
+def check_unit(oracle_mod, w, g, b, h, k, B, seed, stats, n=None):
+    """Oracle for unit (b, h) over its first n tokens (default: all) computed from scratch; compare with the GPU's
+    results."""
+    qh, Kb, Vb, Ksb, sel_h = unit_arrays(oracle_mod, w, b, h, n)
     G, d = qh.shape
     N = Kb.shape[0]
     scale = w["scale"]
     s_ora = oracle_mod.score(qh[None], Ksb[None, None], sel_h[None], scale)[0, 0]
     tol = score_bound(qh[None], Ksb[None, None], sel_h[None], scale)[0, 0]
-    s_gpu = g["s_hat"][b, h].cpu().numpy()
+    s_gpu = g["s_hat"][b, h, :N].cpu().numpy()
     err = np.abs(s_gpu.astype(np.float64) - s_ora.astype(np.float64))
     assert np.all(err <= tol), f"unit ({b},{h}) score error {np.max(err / tol):.2f} x tol"
     delta = float(err.max()) if N else 0.0

@@ -184,3 +184,46 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "invalid argument" in r.stdout
+
+
+def _paged_call(lib, shape, pages, **over):
+    f = 1 << 20  # never dereferenced: every call below must fail validation first
+    args = dict(q=f, k_new=None, v_new=None, K=f, V=f, Ks=f, sel=f, k=10, B=10.0, ws=f, ws_bytes=1 << 40)
+    args.update(over)
+    return lib.ssa_decode_paged(P(args["q"]), P(args["k_new"]), P(args["v_new"]), P(args["K"]), P(args["V"]),
+                                P(args["Ks"]), ctypes.byref(pages) if pages is not None else None, P(args["sel"]),
+                                args["k"], args["B"], 0, 0.1, P(f), P(f), None, None, None, None, 0, P(args["ws"]),
+                                args["ws_bytes"], ctypes.byref(shape), None)
+
+
+def test_paged_entry_point_validates():
+    lib = ssa.load_library()
+    s = binding.ssa_shape(2, 32, 8, 128, 32, 0, 4096, 0, 0, 0, 0)   # a paged step's shape: strides 0
+    f = 1 << 20
+
+    def pages(**kw):
+        d = dict(page_size=64, max_pages=64, num_pages=200, block_table=f, seq_lens=f)
+        d.update(kw)
+        return binding.ssa_paged_kv(d["page_size"], d["max_pages"], d["num_pages"], d["block_table"], d["seq_lens"])
+
+    # the sizing calls take the stride-free shape
+    assert ssa.ssa_workspace_bytes(s) == ssa.ssa_workspace_bytes(_shape())
+    assert lib.ssa_select_capacity(ctypes.byref(s)) == 4096
+    assert _paged_call(lib, s, pages(), ws_bytes=16) == 3                  # the checks pass up to the workspace
+    assert _paged_call(lib, s, None) == 1                                   # no page description
+    assert _paged_call(lib, s, pages(block_table=0)) == 1
+    assert _paged_call(lib, s, pages(seq_lens=0)) == 1
+    for bad_ps in (0, 8, 24, 100, 1 << 21):
+        assert _paged_call(lib, s, pages(page_size=bad_ps)) == 1, bad_ps
+    assert _paged_call(lib, s, pages(max_pages=63)) == 1                    # 63 * 64 < ctx_len
+    assert _paged_call(lib, s, pages(max_pages=0)) == 1
+    assert _paged_call(lib, s, pages(num_pages=0)) == 1
+    assert _paged_call(lib, s, pages(num_pages=(1 << 31) // 64)) == 1       # pool tokens past 2^31 - 1
+    assert _paged_call(lib, s, pages(num_pages=(1 << 31) // 64 - 1), ws_bytes=16) == 3
+    assert _paged_call(lib, s, pages(), k_new=f) == 1                       # k_new without v_new
+    assert _paged_call(lib, s, pages(), k_new=f + 2, v_new=f) == 1          # misaligned
+    assert _paged_call(lib, s, pages(), K=f + 2) == 1
+    assert _paged_call(lib, s, pages(), k=-1) == 1
+    strided = _shape()                                                      # a contiguous shape's strides
+    assert _paged_call(lib, strided, pages()) == 1
+    assert _decode(lib, s) == 1                                             # ... and ssa_decode wants them

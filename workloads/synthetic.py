@@ -218,3 +218,41 @@ def generate(cfg: WorkloadConfig, seed: int = 0, device="cpu") -> dict:
             V[b, h] = torch.randn((N, d), generator=gen_v, device=device, dtype=torch.float32).to(torch.bfloat16)
     return dict(cfg=cfg, q=q, K=K, V=V, sel_ch=sel_ch, needles=needles, scale=cfg.scale,
                 top_k=cfg.top_k, budget=cfg.budget, seed=seed)
+
+
+def to_paged(K: torch.Tensor, V: torch.Tensor, Ks: torch.Tensor, lens, page_size: int, seed: int = 0,
+             spare_pages: int = 2) -> dict:
+    """A paged, variable-length copy of a contiguous cache (the serving layout of a batch of sequences).
+
+    Sequence b keeps its first lens[b] tokens, cut into pages of page_size tokens; the pages of all sequences are
+    placed in a random order in pools K_pool / V_pool [num_pages][Hkv][page_size][d] and Ks_pool [..][d_sel].  Slots
+    past a sequence's end and `spare_pages` unused pages hold random values, and the block-table entries past a
+    sequence's pages hold an out-of-range page id: none of them may be read.  Layout only: no value is computed."""
+    Bt, Hkv, N, d = K.shape
+    dsel = Ks.shape[-1]
+    dev = K.device
+    need = [(int(n) + page_size - 1) // page_size for n in lens]
+    max_pages = max(1, (N + page_size - 1) // page_size)
+    num_pages = sum(need) + spare_pages
+    g = torch.Generator().manual_seed(seed * 7919 + page_size)
+    order = torch.randperm(num_pages, generator=g).tolist()
+    gd = torch.Generator(device=dev).manual_seed(seed * 104729 + page_size)
+
+    def noise(*shape):
+        return torch.randn(shape, generator=gd, device=dev).to(torch.bfloat16)
+
+    K_pool, V_pool = noise(num_pages, Hkv, page_size, d), noise(num_pages, Hkv, page_size, d)
+    Ks_pool = noise(num_pages, Hkv, page_size, dsel)
+    table = torch.full((Bt, max_pages), 2**31 - 1, dtype=torch.int32)
+    i = 0
+    for b in range(Bt):
+        for pi in range(need[b]):
+            pg = order[i]
+            i += 1
+            t0, t1 = pi * page_size, min(int(lens[b]), (pi + 1) * page_size)
+            K_pool[pg, :, :t1 - t0] = K[b, :, t0:t1]
+            V_pool[pg, :, :t1 - t0] = V[b, :, t0:t1]
+            Ks_pool[pg, :, :t1 - t0] = Ks[b, :, t0:t1]
+            table[b, pi] = pg
+    return dict(K_pool=K_pool, V_pool=V_pool, Ks_pool=Ks_pool, block_table=table.to(dev),
+                seq_lens=torch.tensor([int(n) for n in lens], dtype=torch.int32, device=dev), page_size=page_size)
