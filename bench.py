@@ -56,6 +56,11 @@ def parse_args():
                     "27b_128k_dense", help="further workloads timed for the per-config records ('' = none)")
     ap.add_argument("--host-tier", default="ministral8b_32k",
                     help="workload timed with K/V in pinned host memory ('' = none)")
+    ap.add_argument("--paged", type=int, default=256,
+                    help="page size of the paged-cache records of the main workload (0 = none)")
+    ap.add_argument("--plain-steps", type=int, default=0,
+                    help="only run this many decode steps of --workload (L2 flushed before each) and exit: "
+                         "the program the ncu summaries under profiles/ capture")
     return ap.parse_args()
 
 
@@ -416,6 +421,52 @@ def time_steps(cfg, steps: int, warmup: int, dev, host_kv: bool = False):
     return us, rows, clk.summary()
 
 
+def time_paged(cfg, steps: int, warmup: int, dev, page_size: int, lens):
+    """Mean us per ssa_decode_paged step of workload `cfg` laid out in pages of `page_size` tokens with sequence
+    lengths `lens` (L2 flushed before every step, seed = step index), and the mean rows selected."""
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    w = workloads.generate(cfg, 0, dev)
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    pg = workloads.to_paged(w["K"], w["V"], Ks, lens, page_size, seed=1)
+    q, sel = w["q"], w["sel_ch"]
+    del w, Ks
+    shape = ssa.paged_shape(q, pg["K_pool"], pg["Ks_pool"], cfg.ctx_len)
+    ws = ssa.workspace(shape, 0, dev)
+    out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((cfg.batch, cfg.n_q_heads), dtype=torch.float32, device=dev)
+    counts = torch.zeros((steps, cfg.units), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, count=None):
+        ssa.ssa_decode_paged(q, pg["K_pool"], pg["V_pool"], pg["Ks_pool"], pg["block_table"], pg["seq_lens"], sel,
+                             cfg.top_k, cfg.budget, i, cfg.scale, cfg.ctx_len, out=out, lse=lse, count=count, ws=ws,
+                             stream=stream)
+    for i in range(warmup):
+        flush.fill_(i & 0xff)
+        step(1_000_000 + i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(20_000_000)
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            step(i, counts[i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    rows = counts.sum(dim=1).double().mean().item()
+    return us, rows, clk.summary()
+
+
 def config_record(cfg, us, rows, peak, clocks):
     ab = algorithmic_bytes(cfg, rows)
     gbs = ab / (us * 1e-6) / 1e9
@@ -502,7 +553,7 @@ def run_ours(args):
         "append_step": {"value": round(statistics.fmean(m["append_us"]), 3), "unit": UNIT,
                         "api": "ssa_decode_append (the new token's K/V and summary rows written by the chain's "
                                "first kernel, then the step over all tokens)"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,   # per timed step: the initialiser, the score kernel, the unit kernel
         "clocks": m["clocks"],
         "wall_s": round(wall, 2),
     }
@@ -547,6 +598,24 @@ def run_ours(args):
                    host_link_gbs=round(rows * cfgh.head_dim * 4 / (us * 1e-6) / 1e9, 1))
         line["host_tier"] = rec
         torch.cuda.empty_cache()
+    if rank == 0 and args.paged:
+        # the same workload as a paged cache (pool pages in a random order): every sequence full (the contiguous
+        # step's work), then ragged lengths; bytes are counted over the tokens the sequences hold
+        line["paged"] = []
+        steps_p = max(20, min(args.steps, 300))
+        n = cfg.ctx_len
+        for kind, lens in (("full", [n] * cfg.batch),
+                           ("ragged", [max(1, (n * (i + 1)) // (cfg.batch + 1)) for i in range(cfg.batch)])):
+            us, rows, clk = time_paged(cfg, steps_p, max(3, min(args.warmup, 10)), dev, args.paged, lens)
+            summary = cfg.n_kv_heads * sum(lens) * cfg.d_sel * 2
+            ab = summary + rows * cfg.head_dim * 4 + cfg.batch * cfg.n_q_heads * (cfg.head_dim * 6 + 4)
+            gbs = ab / (us * 1e-6) / 1e9
+            line["paged"].append({
+                "workload": cfg.name, "lengths": kind, "seq_lens": lens, "page_size": args.paged,
+                "value": round(us, 3), "unit": UNIT, "steps": steps_p, "rows_selected_per_step": round(rows, 1),
+                "algorithmic_bytes_per_step": int(ab), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "clocks": clk, "api": "ssa_decode_paged"})
+            torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle as it stands, on this host's cores, on a bounded sample of the same workload
         w = workloads.generate(cfg, 0, dev)
@@ -575,6 +644,29 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_plain(args):
+    """args.plain_steps decode steps of the workload, nothing timed (for ncu)."""
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    cfg = workloads.CONFIGS[args.workload]
+    dev = torch.device("cuda", 0)
+    w = workloads.generate(cfg, 0, dev)
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    q, K, V, sel = w["q"], w["K"], w["V"], w["sel_ch"]
+    ws = ssa.workspace(ssa.shape_of(q, K, Ks), 0, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for i in range(args.plain_steps):
+        flush.fill_(i & 0xff)
+        ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, ws=ws)
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    print(json.dumps({"plain_steps": args.plain_steps, "workload": cfg.name}), flush=True)
 
 
 def run_reference(args):
@@ -641,6 +733,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.plain_steps > 0:
+        run_plain(args)
     else:
         run_ours(args)
 

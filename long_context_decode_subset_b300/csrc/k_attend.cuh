@@ -45,6 +45,34 @@ struct UnitSel {
     bool sampling;
 };
 
+// A paged cache's tile of pages: the block-table entries [p0, p0 + n) of
+// sequence b in shared memory (n = 0 when they do not fit: then the table
+// is read from global memory).
+struct PageCache {
+    const int32_t* ent;
+    int64_t p0;
+    int32_t n;
+};
+
+// Token t of sequence b as a pool token (page * page_size + slot), its page
+// id from the cache when there; an id outside [0, num_pages) is flagged and
+// replaced by page 0.
+__device__ __forceinline__ int32_t pool_token_c(const Params& p, const PageCache& pc, int b, int64_t t)
+{
+    const int64_t pi = t >> p.log_ps;
+    int32_t pg;
+    if (pi - pc.p0 >= 0 && pi - pc.p0 < pc.n) {
+        pg = pc.ent[pi - pc.p0];
+        if ((uint64_t)(uint32_t)pg >= (uint64_t)p.num_pages) {
+            flag(ws_status(p), DEV_BAD_INDEX);
+            pg = 0;
+        }
+    } else {
+        pg = page_of(p, b, t);
+    }
+    return (pg << p.log_ps) | (int32_t)(t & ((1 << p.log_ps) - 1));
+}
+
 // Entries [c0, c0 + n) of this CTA's list (n <= LIST) from source `mode`
 // (0 the selection, 1 all tokens, 2 the caller's list): staged through
 // ridx / rval (cp.async, one wave), decided, and the kept ones written in
@@ -57,7 +85,7 @@ struct UnitSel {
 template <int LIST, int NT, bool PAGED>
 __device__ int stage_decide(const Params& p, int mode, int u, int b, int h, int tile, int64_t c0, int n,
                             int64_t stage_at, const uint32_t* pre, const UnitSel& us, int32_t* ridx, float* rval,
-                            int32_t* cidx, float* clp, uint32_t* scan)
+                            int32_t* cidx, float* clp, uint32_t* scan, const PageCache& pc)
 {
     constexpr int PER = (LIST + NT - 1) / NT;   // entries per thread at most
     static_assert(PER <= 32, "one keep bit per entry in a word");
@@ -152,7 +180,7 @@ __device__ int stage_decide(const Params& p, int mode, int u, int b, int h, int 
         for (int e = 0; e < PER; ++e) {
             pt[e] = 0;
             if (e < e1 - e0 && ((kbits >> e) & 1u))
-                pt[e] = pool_token(p, b, (mode == 1) ? c0 + e0 + e : (int64_t)ridx[e0 + e]);
+                pt[e] = pool_token_c(p, pc, b, (mode == 1) ? c0 + e0 + e : (int64_t)ridx[e0 + e]);
         }
     }
 #pragma unroll 1
@@ -195,7 +223,9 @@ static_assert((5 + kUGatherWarps) * 32 == kSelThreads, "the attention roles fill
 // the row's 64-dim plane.  At head_dim 64 only the first plane is gathered:
 // S reads only it, and O's rows for dims 64..127 (from the second plane,
 // whatever it holds) are never read back.
-template <int G, int D, int LIST>   // LIST: list entries staged at a time (1024 or 4096)
+constexpr int kPageCache = 2048;   // block-table entries of its tile a CTA keeps in shared memory (paged)
+
+template <int G, int D, int LIST, bool PAGED = false>   // LIST: list entries staged at a time (1024 or 4096)
 struct UCfg {
     static constexpr int CH = 128;                                 // listed rows per chunk
     static constexpr uint32_t PLANE = CH * 128u;                   // 64 dims x 128 rows, 128-byte swizzle
@@ -215,7 +245,9 @@ struct UCfg {
     static constexpr uint32_t NBAR = 10;                           // kv_full, kv_free, s_full, p_ready, o_full (x2)
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;      // tensor-memory slot, counts
     static constexpr uint32_t OFF_PRE = OFF_MISC + 64u;            // the tile list's slice prefix
-    static constexpr uint32_t SMEM = OFF_PRE + (uint32_t)(kSelWarps + 1) * 4u + 1024u;   // + alignment slack
+    static constexpr uint32_t OFF_PCACHE = (OFF_PRE + (uint32_t)(kSelWarps + 1) * 4u + 15u) & ~15u;   // paged
+    static constexpr uint32_t OFF_ROFF = OFF_PCACHE + (PAGED ? kPageCache * 4u : 0u);   // paged: 2 x CH row offsets
+    static constexpr uint32_t SMEM = OFF_ROFF + (PAGED ? 2u * CH * 8u : 0u) + 1024u;     // + alignment slack
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 16);       // S = K Q^T
     static constexpr uint32_t IDESC_O = idesc_bf16_f32_amn(128, 16);   // O^T = V^T P
     static constexpr uint32_t TCOLS = 64;                          // S x2 (cols 0-31), O x2 (cols 32-63)
@@ -224,8 +256,9 @@ struct UCfg {
     static_assert(D == 64 || D == 128, "head_dim");
 };
 
-template <int G, int D, int LIST>
-constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST>::SMEM; }
+template <int G, int D, int LIST, bool PAGED = false>
+constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST, PAGED>::SMEM; }
+
 
 // Thread roles in the attention (kSelThreads): warps 0-3 epilogue
 // (tensor-memory lanes = chunk rows for S, = head dims for O), warp 4 issues
@@ -235,7 +268,7 @@ constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST>::SMEM; }
 template <int G, int D, int LIST, bool PAGED>
 __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_constant__ Params p)
 {
-    using CF = UCfg<G, D, LIST>;
+    using CF = UCfg<G, D, LIST, PAGED>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -282,6 +315,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         *reinterpret_cast<uint4*>(smem + CF::OFF_Q + (pc >> 3) * CF::QPLANE + n * 128 + (((pc & 7) ^ (n & 7)) << 4)) = v;
         fence_proxy_async_smem();
     }
+    // a paged cache: the sequence's length and the block-table entries of this
+    // CTA's tile go to shared memory before the wait (the chain's kernels do
+    // not write them)
+    PageCache pc{nullptr, 0, 0};
+    int64_t nu = pl.N;   // the unit's tokens
+    if constexpr (PAGED) {
+        nu = unit_len<true>(p, b);
+        int32_t* ent = reinterpret_cast<int32_t*>(smem + CF::OFF_PCACHE);
+        const int64_t t0 = (int64_t)r * pl.tt, t1 = min(nu, t0 + pl.tt);
+        pc.ent = ent;
+        pc.p0 = t0 >> p.log_ps;
+        const int64_t np = t1 > t0 ? ((t1 - 1) >> p.log_ps) - pc.p0 + 1 : 0;
+        pc.n = np <= kPageCache ? (int32_t)np : 0;
+        for (int i = tid; i < pc.n; i += kSelThreads) ent[i] = __ldg(p.block_table + (int64_t)b * p.max_pages + pc.p0 + i);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -295,7 +343,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     UnitCtrl* ctrl = ws_ctrl(p) + u;
     UnitSel us{0u, -1, 0.0f, 0.0f, false};
     int64_t lo = 0, hi = 0;
-    const int64_t nu = unit_len<PAGED>(p, b);   // the unit's tokens
     int mode = p.src_mode;
     SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
     // the stratum's size: k, or (top-p) found from the unit's score masses;
@@ -366,8 +413,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         const int n = (int)min((int64_t)LIST, hi - c0);
         int32_t* ridx = reinterpret_cast<int32_t*>(smem + CF::OFF_RAW);
         float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4);
-        const int nk = stage_decide<LIST, kSelThreads, PAGED>(p, mode, u, b, h, r, c0, n, stage_base + kept, pre, us, ridx,
-                                                       rval, cidx, clp, scan);
+        const int nk = stage_decide<LIST, kSelThreads, PAGED>(p, mode, u, b, h, r, c0, n, stage_base + kept, pre, us,
+                                                              ridx, rval, cidx, clp, scan, pc);
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
@@ -387,13 +434,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                 }
                 unsigned char* kd = smem + CF::OFF_K + bf * CF::KV;
                 unsigned char* vd = smem + CF::OFF_V + bf * CF::KV;
+                int64_t* roff = reinterpret_cast<int64_t*>(smem + CF::OFF_ROFF) + bf * CF::CH;
+                if constexpr (PAGED) {
+                    // the chunk's pool rows, once per row (double-buffered: a buffer is rewritten only after
+                    // every gather thread has passed the next chunk's barrier)
+                    if (gt < CF::CH) {
+                        const int row = c * CF::CH + gt;
+                        roff[gt] = row < nk ? pool_row(p, h, cidx[row]) : 0;
+                    }
+                    named_bar_sync(2, 32 * kUGatherWarps);
+                }
 #pragma unroll 1
                 for (int q = gt; q < CF::CH * PPR; q += 32 * kUGatherWarps) {
                     const int i = q / PPR, pc = q % PPR;
                     const int row = c * CF::CH + i;
                     const bool valid = row < nk;
-                    int64_t j = valid ? (int64_t)cidx[row] : 0;
-                    if constexpr (PAGED) j = valid ? pool_row(p, h, (int32_t)j) : 0;
+                    int64_t j;
+                    if constexpr (PAGED) j = roff[i];
+                    else j = valid ? (int64_t)cidx[row] : 0;
                     const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
                     cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, valid);
                     cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, valid);

@@ -551,11 +551,19 @@ __global__ void __launch_bounds__(k1_threads(HIST), 1) score_kernel(const __grid
         nsel = (lane < DSEL) ? __ldg(p.sel_ch + (int64_t)hh * DSEL + lane) : 0;
     };
     int first_u = -1;
-    if (warp == 3 && !PAGED) {
-        const int64_t st = (int64_t)pl.U * pl.sf;
-        const int64_t g0 = st * blockIdx.x / gridDim.x;
-        if (g0 < st * (blockIdx.x + 1) / gridDim.x) {
-            first_u = (int)(g0 / pl.sf);
+    if (warp == 3) {
+        if constexpr (!PAGED) {
+            const int64_t st = (int64_t)pl.U * pl.sf;
+            const int64_t g0 = st * blockIdx.x / gridDim.x;
+            if (g0 < st * (blockIdx.x + 1) / gridDim.x) first_u = (int)(g0 / pl.sf);
+        } else {   // the first static stage's unit, found as the producer finds it
+            K1Sched<true> s3;
+            s3.init(p, nullptr);
+            int uu, jj;
+            int64_t ll;
+            if (s3.s_cur < s3.s_end && s3.locate(p, s3.s_cur, false, uu, jj, ll)) first_u = uu;
+        }
+        if (first_u >= 0) {
             if (p.q_staged) grid_dep_wait();   // K0 copies the query into the workspace
             fetch_q(first_u);
         }

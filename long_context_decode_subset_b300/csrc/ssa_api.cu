@@ -307,10 +307,10 @@ template <int G, bool PAGED>
 kfn_t unit_fn(int d, uint32_t* smem)
 {
     if (d == 128) {
-        *smem = unit_smem_bytes<G, 128, 4096>();
+        *smem = unit_smem_bytes<G, 128, 4096, PAGED>();
         return &unit_kernel<G, 128, 4096, PAGED>;
     }
-    *smem = unit_smem_bytes<G, 64, 4096>();
+    *smem = unit_smem_bytes<G, 64, 4096, PAGED>();
     return &unit_kernel<G, 64, 4096, PAGED>;
 }
 
