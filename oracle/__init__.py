@@ -69,6 +69,9 @@ def _load():
             lib.oracle_select_unit_m.restype = i64
             lib.oracle_attend_unit.argtypes = [P, P, P, i32, i32, P, P, i64, f32, P, P]
             lib.oracle_attend_unit.restype = None
+            lib.oracle_attend_unit_early_stop.argtypes = [P, P, P, i32, i32, P, P, P, i64, f32, f32, i64, i64,
+                                                          P, P, P]
+            lib.oracle_attend_unit_early_stop.restype = i64
             lib.oracle_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i64, i64, i64, i64,
                                           i64, i64, f32, u64, f32, P, P, P, P, P, P, i64, P, P]
             lib.oracle_decode.restype = ctypes.c_int
@@ -284,6 +287,29 @@ def attend_unit(q_heads, Kb, Vb, idx, p, scale: float):
     _load().oracle_attend_unit(_ptr(q_heads), _ptr(Kb), _ptr(Vb), G, d, _ptr(idx), _ptr(p),
                                idx.size, float(scale), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def attend_unit_early_stop(q_heads, Kb, Vb, idx, p, s, scale: float, tau: float, block: int = 128,
+                           force_blocks: int = -1):
+    """Corrected attention over one unit's selected rows with S2O-style early stopping ("S2O ...", technical
+    summary, Method section 2): rows ordered by s descending (ties by list position), blocks of `block` rows,
+    stop after the first block whose gain is below tau times the accumulated denominator for every head.
+    Returns (out fp32 [G][d], lse fp32 [G], blocks processed, per-block max gain ratio)."""
+    q_heads = _c(q_heads, np.uint16)
+    Kb = _c(Kb, np.uint16)
+    Vb = _c(Vb, np.uint16)
+    idx = _c(idx, np.int32)
+    p = _c(p, np.float32)
+    s = _c(s, np.float32)
+    G, d = q_heads.shape
+    n = idx.size
+    out = np.zeros((G, d), np.float32)
+    lse = np.zeros(G, np.float32)
+    ratios = np.zeros(max(1, -(-n // block)), np.float32)
+    used = _load().oracle_attend_unit_early_stop(_ptr(q_heads), _ptr(Kb), _ptr(Vb), G, d, _ptr(idx), _ptr(p),
+                                                 _ptr(s), n, float(scale), float(tau), int(block),
+                                                 int(force_blocks), _ptr(out), _ptr(lse), _ptr(ratios))
+    return out, lse, int(used), ratios[:-(-n // block)]
 
 
 def decode(q, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale: float,

@@ -26,7 +26,11 @@
  *         tokens only, at their original positions.
  *  [S2O]  "S2O: early stopping for sparse attention via online permutation"
  *         (gist.science 2602.22575), technical summary, Method section 3
- *         (kernel): the online-softmax state (m, l, acc).
+ *         (kernel): the online-softmax state (m, l, acc); Method section 2
+ *         (early stop): blocks are processed in descending estimated
+ *         importance, the marginal gain of each processed block is tracked,
+ *         and the computation ends once that gain falls below a preset
+ *         threshold tau relative to the accumulated score.
  *  [Philox] J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
  *         Random Numbers: As Easy as 1, 2, 3", SC'11: the Philox-4x32
  *         counter-based generator (round function, multipliers and Weyl key
@@ -56,6 +60,15 @@
  *  - attention over the selected rows with logit
  *    scale * q.K_i - log p_i, in double; lse = log of the corrected
  *    denominator.
+ *  - early stop (S2O section 2 applied to the selected rows of one unit):
+ *    the rows are ordered by orderkey(s) descending, ties by position in
+ *    the list; block b is rows [b * block, (b + 1) * block) of that order;
+ *    for each query head g, after block b the gain D_g(b) is the block's
+ *    share of the corrected softmax denominator and L_g(b) the denominator
+ *    over blocks 0..b (both at a common reference point), and the step stops
+ *    after the first block b with D_g(b) < tau * L_g(b) for every head g
+ *    (block b included; block 0 is always processed; tau = 0 never stops).
+ *    The output is the corrected attention over the processed blocks.
  *
  * Parity pins for every function here live in tests/test_oracle_*.py.
  */
@@ -419,6 +432,94 @@ void oracle_attend_unit(const uint16_t* q_heads /* [G][d] */, const uint16_t* Kb
         lse[g] = (float)(mx + log(den));
     }
     free(acc); free(logit);
+}
+
+/* Attention over the selected rows with S2O-style early stopping (see the
+ * reading in the header).  s [count]: the rows' estimated scores, giving the
+ * order.  ratio_out [ceil(count / block)] (may be NULL) receives, for every
+ * block b of the order, max over g of D_g(b) / L_g(b) as if no block had
+ * been skipped.  force_blocks >= 0 processes exactly that many blocks
+ * (clamped to the number of blocks) instead of applying tau.  Returns the
+ * number of blocks processed. */
+typedef struct { uint32_t key; int64_t pos; } es_order_t;
+
+static int es_order_cmp(const void* a, const void* b)
+{
+    const es_order_t* x = (const es_order_t*)a;
+    const es_order_t* y = (const es_order_t*)b;
+    if (x->key != y->key) return x->key > y->key ? -1 : 1;   /* key descending */
+    return x->pos < y->pos ? -1 : (x->pos > y->pos ? 1 : 0); /* then position ascending */
+}
+
+int64_t oracle_attend_unit_early_stop(const uint16_t* q_heads /* [G][d] */, const uint16_t* Kb, const uint16_t* Vb,
+                                      int32_t G, int32_t d, const int32_t* idx, const float* p, const float* s,
+                                      int64_t count, float scale, float tau, int64_t block, int64_t force_blocks,
+                                      float* out /* [G][d] */, float* lse /* [G] */, float* ratio_out)
+{
+    const int64_t nb = count > 0 ? (count + block - 1) / block : 0;
+    es_order_t* ord = (es_order_t*)malloc(sizeof(es_order_t) * (size_t)(count > 0 ? count : 1));
+    double* logit = (double*)malloc(sizeof(double) * (size_t)(count > 0 ? count : 1) * (size_t)G);
+    double* M = (double*)malloc(sizeof(double) * (size_t)G);
+    double* L = (double*)malloc(sizeof(double) * (size_t)G);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)G * (size_t)d);
+    for (int64_t i = 0; i < count; ++i) { ord[i].key = oracle_orderkey(s[i]); ord[i].pos = i; }
+    qsort(ord, (size_t)count, sizeof(es_order_t), es_order_cmp);
+    /* the corrected logits of every row, in the order */
+    for (int64_t r = 0; r < count; ++r) {
+        const int64_t i = ord[r].pos;
+        const uint16_t* kr = Kb + (int64_t)idx[i] * d;
+        for (int32_t g = 0; g < G; ++g) {
+            double dot = 0.0;
+            for (int32_t c = 0; c < d; ++c) dot += bf16_value(q_heads[g * d + c]) * bf16_value(kr[c]);
+            logit[r * G + g] = (double)scale * dot - log((double)p[i]);
+        }
+    }
+    /* the gain ratio of every block, as if none were skipped */
+    for (int32_t g = 0; g < G; ++g) { M[g] = -INFINITY; L[g] = 0.0; }
+    int64_t used = -1;
+    for (int64_t b = 0; b < nb; ++b) {
+        const int64_t r0 = b * block, r1 = (r0 + block < count) ? r0 + block : count;
+        double worst = 0.0;
+        for (int32_t g = 0; g < G; ++g) {
+            double mb = -INFINITY;
+            for (int64_t r = r0; r < r1; ++r) if (logit[r * G + g] > mb) mb = logit[r * G + g];
+            const double mn = mb > M[g] ? mb : M[g];
+            double D = 0.0;
+            for (int64_t r = r0; r < r1; ++r) D += exp(logit[r * G + g] - mn);
+            const double Ln = (M[g] == -INFINITY ? 0.0 : L[g] * exp(M[g] - mn)) + D;
+            const double ratio = Ln > 0.0 ? D / Ln : 0.0;
+            if (ratio > worst) worst = ratio;
+            M[g] = mn;
+            L[g] = Ln;
+        }
+        if (ratio_out) ratio_out[b] = (float)worst;
+        if (used < 0 && force_blocks < 0 && worst < (double)tau) used = b + 1;
+    }
+    if (force_blocks >= 0) used = force_blocks < nb ? force_blocks : nb;
+    if (used < 0) used = nb;
+    /* the corrected attention over the first `used` blocks */
+    const int64_t rows = used * block < count ? used * block : count;
+    for (int32_t g = 0; g < G; ++g) {
+        if (rows == 0) {
+            for (int32_t c = 0; c < d; ++c) out[g * d + c] = 0.0f;
+            lse[g] = -INFINITY;
+            continue;
+        }
+        double mx = -INFINITY;
+        for (int64_t r = 0; r < rows; ++r) if (logit[r * G + g] > mx) mx = logit[r * G + g];
+        double den = 0.0;
+        for (int32_t c = 0; c < d; ++c) acc[c] = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            const double w = exp(logit[r * G + g] - mx);
+            const uint16_t* vr = Vb + (int64_t)idx[ord[r].pos] * d;
+            den += w;
+            for (int32_t c = 0; c < d; ++c) acc[c] += w * bf16_value(vr[c]);
+        }
+        for (int32_t c = 0; c < d; ++c) out[g * d + c] = (float)(acc[c] / den);
+        lse[g] = (float)(mx + log(den));
+    }
+    free(acc); free(L); free(M); free(logit); free(ord);
+    return used;
 }
 
 /* ------------------------------------------------------------------ */
