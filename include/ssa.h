@@ -77,7 +77,10 @@
  * library allocates no device memory (ssa_decode_static's built-in array,
  * below, is part of the loaded module).  The results of a call depend only
  * on its arguments: the workspace needs no initialisation (each call resets
- * what it uses) and carries nothing from one call to the next.  What the
+ * what it uses) and carries nothing from one call to the next, apart from
+ * the device status word at its start, which collects flags until
+ * ssa_get_device_status reads and clears it (clear a new workspace once,
+ * with that call or by zeroing it, before reading flags).  What the
  * library does keep, per process, is launch bookkeeping that never changes
  * a result: the kernels' raised shared-memory limits and occupancy queries
  * (per kernel and device), the driver entry point that encodes tensor maps,
@@ -239,16 +242,43 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       float scale, float* out, float* lse,
                       void* ws, size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream);
 
+/* Step (c) with S2O-style early stopping ("S2O: early stopping for sparse
+ * attention via online permutation", technical summary, Method section 2:
+ * blocks processed in descending estimated importance, the marginal gain of
+ * each tracked, the computation ended once that gain falls below a preset
+ * threshold tau relative to the accumulated score).  Each unit's rows
+ * (idx / p / count as in ssa_attend, idx ascending as ssa_select writes
+ * them) are ordered by their scores s_hat[b][h][idx] ([batch][n_kv_heads]
+ * [ctx_len], e.g. from ssa_score) descending, ties by list position, and
+ * attended in blocks of 128 rows of that order; after block b the gain of
+ * head g is the block's share D_g(b) of the corrected softmax denominator
+ * L_g(b) over blocks 0..b, and the step stops after the first block with
+ * D_g(b) < tau * L_g(b) for every head g of the unit (block 0 is always
+ * kept; tau = 0 keeps every block, i.e. ssa_attend's result up to the
+ * summation order; tau > 1 keeps block 0 only).  out / lse are the corrected
+ * attention over the kept blocks; blocks_opt [batch][n_kv_heads] (may be
+ * NULL) receives the number of blocks kept.  One CTA per unit attends, in
+ * order, and reads no row of a block after the stop.  A unit's list holds at
+ * most 32768 rows here: a longer one keeps its first 32768 entries and sets
+ * SSA_DEV_OVERFLOW.  tau must be >= 0 (+inf allowed). */
+ssa_status ssa_attend_early_stop(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                                 const int32_t* idx, const float* p, const int32_t* count, int64_t list_cap,
+                                 const float* s_hat, float tau, float scale, float* out, float* lse,
+                                 int32_t* blocks_opt, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                                 cudaStream_t stream);
+
 /* The whole step, (a) -> (b) -> (c) ("Stratified Sparse Attention speeds up
  * decoding 2.96x on a 1M context": estimate, stratify, sample, correct; the
  * arguments follow its problem statement: query, KV cache, k, budget B,
- * seed), enqueued on `stream` as a chain of
- * kernels (initialise, score, threshold bucket, decide, attend; each after
- * the first is a programmatic dependent launch).  s_hat_opt, idx_opt,
+ * seed), enqueued on `stream` as a chain of three kernels: initialise;
+ * score (streams the key summary); and the unit kernel, whose CTAs per unit
+ * select, decide and attend, then merge their partial results.  Each after
+ * the first is a programmatic dependent launch.  s_hat_opt, idx_opt,
  * p_opt, count_opt may be NULL; when given they receive the intermediate
  * results (idx_opt / p_opt need list_cap entries per unit and are given
  * together).  A step that selects every token (top_k >= ctx_len or
- * budget = +inf) skips the selection kernels. */
+ * budget = +inf) skips the selection (and the score kernel when s_hat_opt
+ * is NULL). */
 ssa_status ssa_decode(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                       const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
                       uint64_t seed, float scale, float* out, float* lse,
@@ -264,6 +294,17 @@ ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
                              float* s_hat_opt, int32_t* idx_opt, float* p_opt, int32_t* count_opt,
                              int64_t list_cap, void* ws, size_t ws_bytes, const ssa_shape* shape,
                              cudaStream_t stream);
+
+/* The whole step with the early-stopping attention of ssa_attend_early_stop
+ * in place of step (c): scores and selection as ssa_decode, then each unit's
+ * selected rows (the top-k stratum and the drawn remainder, each with its
+ * p) ordered by score and attended block by block until the gain test with
+ * tau stops it.  blocks_opt as in ssa_attend_early_stop. */
+ssa_status ssa_decode_early_stop(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
+                                 const ssa_bf16* Ks, const int32_t* sel_ch, int64_t top_k, float budget,
+                                 uint64_t seed, float scale, float tau, float* out, float* lse,
+                                 int32_t* blocks_opt, void* ws, size_t ws_bytes, const ssa_shape* shape,
+                                 cudaStream_t stream);
 
 /* Append and decode in one chain: the new token (k_new, v_new, as in
  * ssa_append) is written at position ctx_len - 1 of K, V and Ks by the

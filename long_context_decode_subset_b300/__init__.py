@@ -9,4 +9,5 @@ from .ssa import (  # noqa: F401
     ssa_decode_host, ssa_get_device_status, ssa_query_plan, default_scale, EXPORTS, LIB_PATH,
     ssa_append, ssa_decode_append, ssa_select_capacity, ssa_select_strata, ssa_decode_strata,
     STRATA_SSA, STRATA_UNIFORM, STRATA_TOP_P, ssa_paged_kv, paged_shape, ssa_decode_paged,
+    ssa_attend_early_stop, ssa_decode_early_stop,
 )

@@ -265,9 +265,16 @@ constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST, PAGED>::SMEM; }
 // the MMAs (and owns the tensor memory), warps 5 .. 15 gather the K and V
 // rows.  Chunk g uses buffers g & 1; barrier phases count chunks over the
 // whole CTA.  Grid: U * C CTAs, C = pl.ntile per unit, one wave.
-template <int G, int D, int LIST, bool PAGED>
+// The unit kernel's variants: a contiguous cache, a paged one, and the
+// early-stop attention (a contiguous cache, the caller's lists in descending
+// score order, one CTA per unit).
+constexpr int kVarContig = 0, kVarPaged = 1, kVarEarlyStop = 2;
+
+template <int G, int D, int LIST, int VAR>
 __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_constant__ Params p)
 {
+    constexpr bool PAGED = VAR == kVarPaged;
+    constexpr bool ES = VAR == kVarEarlyStop;
     using CF = UCfg<G, D, LIST, PAGED>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -300,6 +307,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
             mbar_init(&p_ready[i], 4);   // one arrive per epilogue warp
             mbar_init(&o_full[i], 1);
         }
+        misc[6] = 0xffffffffu;   // early stop: the block after which the attention stops (none yet)
         fence_mbar_init();
     }
     if (warp == 4 && p.attend) tmem_alloc(&misc[0], CF::TCOLS);
@@ -406,6 +414,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     int gbase = 0;        // chunks done before this list chunk
     int64_t kept = 0;
+    bool es_stopped = false;   // early stop: the epilogue has kept its last block
+    int32_t es_blocks = 0;     // ... and the blocks it kept
     const uint32_t k_a = smem_addr(smem + CF::OFF_K), v_a = smem_addr(smem + CF::OFF_V);
     const uint32_t q_a = smem_addr(smem + CF::OFF_Q), p_a = smem_addr(smem + CF::OFF_P);
 #pragma unroll 1
@@ -435,6 +445,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                 unsigned char* kd = smem + CF::OFF_K + bf * CF::KV;
                 unsigned char* vd = smem + CF::OFF_V + bf * CF::KV;
                 int64_t* roff = reinterpret_cast<int64_t*>(smem + CF::OFF_ROFF) + bf * CF::CH;
+                // early stop: the chunks past the last kept block are not read (their buffers are zero-filled)
+                const int lim = ES ? ((uint32_t)g > *reinterpret_cast<volatile uint32_t*>(&misc[6]) ? 0 : nk) : nk;
                 if constexpr (PAGED) {
                     // the chunk's pool rows, once per row (double-buffered: a buffer is rewritten only after
                     // every gather thread has passed the next chunk's barrier)
@@ -452,9 +464,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     int64_t j;
                     if constexpr (PAGED) j = roff[i];
                     else j = valid ? (int64_t)cidx[row] : 0;
+                    const bool load = ES ? row < lim : valid;
                     const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
-                    cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, valid);
-                    cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, valid);
+                    cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, load);
+                    cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, load);
                 }
                 cp_async_mbar_arrive(&kv_full[bf]);
             }
@@ -583,20 +596,35 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     for (int k = 0; k < 2 * G; ++k) o[k] = __uint_as_float(rr[k]);
                 }
                 tc_fence_before();
+                bool below = true;   // early stop: this block's share is under tau for every head
+                if (!ES || !es_stopped) {
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    const float mn = fmaxf(m_run[gg], mc[gg]);
-                    const float ar = (m_run[gg] == -INFINITY) ? 0.0f : expf(m_run[gg] - mn);
-                    const float ac = (mc[gg] == -INFINITY) ? 0.0f : expf(mc[gg] - mn);
-                    acc[gg] = acc[gg] * ar + (o[gg] + o[G + gg]) * ac;
-                    l_run[gg] = l_run[gg] * ar + lc[gg] * ac;
-                    m_run[gg] = mn;
+                    for (int gg = 0; gg < G; ++gg) {
+                        const float mn = fmaxf(m_run[gg], mc[gg]);
+                        const float ar = (m_run[gg] == -INFINITY) ? 0.0f : expf(m_run[gg] - mn);
+                        const float ac = (mc[gg] == -INFINITY) ? 0.0f : expf(mc[gg] - mn);
+                        acc[gg] = acc[gg] * ar + (o[gg] + o[G + gg]) * ac;
+                        l_run[gg] = l_run[gg] * ar + lc[gg] * ac;
+                        m_run[gg] = mn;
+                        if constexpr (ES) below = below && (lc[gg] * ac < p.tau * l_run[gg]);
+                    }
+                }
+                if constexpr (ES) {
+                    if (!es_stopped) {
+                        ++es_blocks;
+                        if (below) {
+                            es_stopped = true;
+                            if (tid == 0) *reinterpret_cast<volatile uint32_t*>(&misc[6]) = (uint32_t)g;
+                        }
+                    }
                 }
             }
         }
         gbase += nc;
         __syncthreads();   // every role is done with this list chunk
+        if (ES && *reinterpret_cast<volatile uint32_t*>(&misc[6]) != 0xffffffffu) break;   // stopped early
     }
+    if (ES && tid == 0 && p.blocks_out) p.blocks_out[u] = es_blocks;
     SSA_MARK(8);
 
     // this CTA's partial (acc per head dim, then (m, l) per head) in the
@@ -736,6 +764,93 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     SSA_MARK(9);
     SSA_GT(7);
+}
+
+// ---------------------------------------------------------------------------
+// the early-stop order
+// ---------------------------------------------------------------------------
+// ("S2O: early stopping for sparse attention via online permutation",
+// technical summary, Method section 2: blocks are processed in descending
+// estimated importance.)  One CTA of kOrderThreads per unit sorts the unit's
+// list (idx_in / p_in, count_in entries, row stride cap) by its rows'
+// scores s_src[u][idx] descending, ties by list position -- a bitonic sort
+// of (order key, position) pairs in shared memory -- and writes the ordered
+// list to the workspace's selection rows (stride pl.np) and its length to
+// the early-stop counts.  Lists longer than kOrderCap (or than a row) keep
+// their first entries and set SSA_DEV_OVERFLOW; an index outside [0, N)
+// sets SSA_DEV_BAD_INDEX and sorts last.  The input may be those same rows:
+// every read of a pass ends before its writes begin.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderCap = 32768;
+constexpr uint32_t kOrderSmem = (uint32_t)kOrderCap * 6u;   // keys (4 B) and positions (2 B)
+
+__global__ void __launch_bounds__(kOrderThreads, 1) order_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(16) unsigned char osm[];
+    uint32_t* key = reinterpret_cast<uint32_t*>(osm);
+    uint16_t* pos = reinterpret_cast<uint16_t*>(osm + (size_t)kOrderCap * 4);
+    const Plan& pl = p.pl;
+    const int u = blockIdx.x, tid = threadIdx.x;
+    uint32_t* status = ws_status(p);
+    grid_dep_wait();   // the lists may come from the previous kernel
+    int64_t n = p.count_in[u];
+    n = n < 0 ? 0 : (n > p.cap ? p.cap : n);
+    const int64_t room = min((int64_t)kOrderCap, pl.np);
+    if (n > room) {
+        if (tid == 0) flag(status, DEV_OVERFLOW);
+        n = room;
+    }
+    int n2 = 2;
+    while (n2 < n) n2 <<= 1;
+    const int32_t* idx = p.idx_in + (int64_t)u * p.cap;
+    const float* pin = p.p_in + (int64_t)u * p.cap;
+    const float* srow = p.s_src + (int64_t)u * pl.N;
+    for (int i = tid; i < n2; i += kOrderThreads) {
+        uint32_t k = 0xffffffffu;
+        if (i < n) {
+            const int32_t j = idx[i];
+            if (j >= 0 && (int64_t)j < pl.N) k = ~okey(srow[j]);
+            else flag(status, DEV_BAD_INDEX);
+        }
+        key[i] = k;
+        pos[i] = (uint16_t)(i < n ? i : 0xffff);
+    }
+    __syncthreads();
+    // ascending (key, position): descending score, then list position
+#pragma unroll 1
+    for (int k = 2; k <= n2; k <<= 1) {
+#pragma unroll 1
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll 1
+            for (int i = tid; i < n2; i += kOrderThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint32_t ka = key[i], kb = key[l];
+                    const uint16_t pa = pos[i], pb = pos[l];
+                    const bool gt = ka > kb || (ka == kb && pa > pb);
+                    if (gt == ((i & k) == 0)) {
+                        key[i] = kb;
+                        key[l] = ka;
+                        pos[i] = pb;
+                        pos[l] = pa;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // the ordered list, one array at a time through the key buffer
+    int32_t* oidx = ws_sel_idx(p) + (size_t)u * pl.np;
+    float* op = ws_sel_p(p) + (size_t)u * pl.np;
+    for (int i = tid; i < n; i += kOrderThreads) key[i] = (uint32_t)idx[pos[i]];
+    __syncthreads();
+    for (int i = tid; i < n; i += kOrderThreads) oidx[i] = (int32_t)key[i];
+    __syncthreads();
+    for (int i = tid; i < n; i += kOrderThreads) key[i] = __float_as_uint(pin[pos[i]]);
+    __syncthreads();
+    for (int i = tid; i < n; i += kOrderThreads) op[i] = __uint_as_float(key[i]);
+    if (tid == 0) ws_es_count(p)[u] = (int32_t)n;
+    grid_dep_launch();
 }
 
 // Append-time summary: Ks[b][h][i][j] = K[b][h][i][sel_ch[h][j]].

@@ -94,6 +94,12 @@ struct Params {
     int64_t num_pages;
     const int32_t* block_table;
     const int32_t* seq_lens;
+    // early stop (the unit kernel's early-stop variant): the list of each
+    // unit is in descending score order; the attention stops after the first
+    // 128-row block whose share of the softmax denominator is below tau for
+    // every head, and writes the number of blocks it kept to blocks_out [U]
+    float tau;
+    int32_t* blocks_out;
 };
 
 __device__ __forceinline__ uint32_t* ws_status(const Params& p) { return reinterpret_cast<uint32_t*>(p.ws + p.pl.o_status); }
@@ -109,6 +115,7 @@ __device__ __forceinline__ uint2* ws_cand(const Params& p) { return reinterpret_
 __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_sel_idx); }
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
 __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
+__device__ __forceinline__ int32_t* ws_es_count(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_es); }
 
 // Strata 1 (top-k + uniform): the remainder's size n - min(k, n) in fp32,
 // the normaliser Z of p = min(1, B / Z) for a unit of n tokens.
@@ -225,6 +232,7 @@ __global__ void __launch_bounds__(256) init_kernel(const __grid_constant__ Param
     }
     uint4* z = reinterpret_cast<uint4*>(ws_ctrl(p) + u);
     if (tid < (int)(sizeof(UnitCtrl) / 16)) z[tid] = make_uint4(0, 0, 0, 0);
+    if (p.src_mode != 0) return;   // no selection: no histograms
     uint4* h1 = reinterpret_cast<uint4*>(ws_hist1(p) + (size_t)u * kBins);
     uint4* h2 = reinterpret_cast<uint4*>(ws_hist2(p) + (size_t)u * kBins);
     for (int i = tid; i < kBins / 4; i += 256) {

@@ -113,6 +113,7 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     pl.o_hout = take((size_t)heads * D * 4);
     pl.o_hlse = take((size_t)heads * 4);
     pl.o_topp = take((size_t)U * kTopPUnitBytes);
+    pl.o_es = take((size_t)U * 4);
     pl.total = o;
     return pl;
 }
@@ -303,33 +304,37 @@ kfn_t pick_score(int G, int dsel, bool hist, bool paged)
     return paged ? pick_score_p<true>(G, dsel, hist) : pick_score_p<false>(G, dsel, hist);
 }
 
-template <int G, bool PAGED>
+template <int G, int VAR>
 kfn_t unit_fn(int d, uint32_t* smem)
 {
     if (d == 128) {
-        *smem = unit_smem_bytes<G, 128, 4096, PAGED>();
-        return &unit_kernel<G, 128, 4096, PAGED>;
+        *smem = unit_smem_bytes<G, 128, 4096, VAR == kVarPaged>();
+        return &unit_kernel<G, 128, 4096, VAR>;
     }
-    *smem = unit_smem_bytes<G, 64, 4096, PAGED>();
-    return &unit_kernel<G, 64, 4096, PAGED>;
+    *smem = unit_smem_bytes<G, 64, 4096, VAR == kVarPaged>();
+    return &unit_kernel<G, 64, 4096, VAR>;
 }
 
-template <bool PAGED>
-kfn_t pick_unit_p(int G, int d, uint32_t* smem)
+template <int VAR>
+kfn_t pick_unit_v(int G, int d, uint32_t* smem)
 {
     switch (G) {
-        case 1: return unit_fn<1, PAGED>(d, smem);
-        case 2: return unit_fn<2, PAGED>(d, smem);
-        case 4: return unit_fn<4, PAGED>(d, smem);
-        default: return unit_fn<8, PAGED>(d, smem);
+        case 1: return unit_fn<1, VAR>(d, smem);
+        case 2: return unit_fn<2, VAR>(d, smem);
+        case 4: return unit_fn<4, VAR>(d, smem);
+        default: return unit_fn<8, VAR>(d, smem);
     }
 }
 
-// The unit kernel for this group size, head_dim and cache layout, and its
-// dynamic shared memory.
-kfn_t pick_unit(int G, int d, uint32_t* smem, bool paged = false)
+// The unit kernel for this group size, head_dim and variant (kVarContig,
+// kVarPaged, kVarEarlyStop), and its dynamic shared memory.
+kfn_t pick_unit(int G, int d, uint32_t* smem, int var = kVarContig)
 {
-    return paged ? pick_unit_p<true>(G, d, smem) : pick_unit_p<false>(G, d, smem);
+    switch (var) {
+        case kVarPaged: return pick_unit_v<kVarPaged>(G, d, smem);
+        case kVarEarlyStop: return pick_unit_v<kVarEarlyStop>(G, d, smem);
+        default: return pick_unit_v<kVarContig>(G, d, smem);
+    }
 }
 
 // Raise `fn`'s dynamic shared-memory limit to `smem` (static plus dynamic
@@ -472,10 +477,38 @@ ssa::Plan unit_plan(const ssa_shape& s)
 ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t stream, bool dependent)
 {
     uint32_t smem = 0;
-    kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem, p.paged != 0);
+    kfn_t fn = pick_unit(p.pl.G, s.head_dim, &smem, p.paged ? kVarPaged : kVarContig);
     if (smem > 227u * 1024u) return SSA_ERR_UNSUPPORTED;
     return launch(fn, (int64_t)p.pl.U * p.pl.ntile, kSelThreads, smem, p, stream, dependent);
 }
+
+// The early-stop attention after the lists are known (prm.idx_in / p_in /
+// count_in / cap, scores prm.s_src): the order kernel sorts each unit's list
+// into the workspace, then the unit kernel's early-stop variant (one CTA per
+// unit) attends over it in that order.  Both wait for the previous kernel.
+ssa_status launch_early_stop(ssa::Params prm, const ssa_shape& s, float tau, int32_t* blocks, cudaStream_t stream)
+{
+    ssa_status st = launch(&order_kernel, prm.pl.U, kOrderThreads, kOrderSmem, prm, stream, true);
+    if (st != SSA_OK) return st;
+    char* w = prm.ws;
+    prm.idx_in = reinterpret_cast<const int32_t*>(w + prm.pl.o_sel_idx);
+    prm.p_in = reinterpret_cast<const float*>(w + prm.pl.o_sel_p);
+    prm.count_in = reinterpret_cast<const int32_t*>(w + prm.pl.o_es);
+    prm.cap = prm.pl.np;
+    prm.pl.ntile = 1;
+    prm.src_mode = 2;
+    prm.attend = 1;
+    prm.idx_out = nullptr;
+    prm.p_out = nullptr;
+    prm.count_out = nullptr;
+    prm.tau = tau;
+    prm.blocks_out = blocks;
+    uint32_t smem = 0;
+    kfn_t fn = pick_unit(prm.pl.G, s.head_dim, &smem, kVarEarlyStop);
+    return launch(fn, prm.pl.U, kSelThreads, smem, prm, stream, true);
+}
+
+bool bad_tau(float tau) { return !(tau >= 0.0f); }
 
 }  // namespace
 
@@ -649,10 +682,10 @@ ssa_status ssa_select_strata(const float* s_hat, int strata, int64_t top_k, floa
     prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
     prm.src_mode = prm.dense ? 1 : 0;
     prm.attend = 0;
-    if (prm.dense) return launch_unit(prm, *shape, stream, false);   // every token, p = 1
-    // K0 zeroes the histograms, the input kernel counts the scores and draws
-    // the Philox prefixes, the unit kernel selects
+    // K0 zeroes the unit counters (and the histograms), the input kernel
+    // counts the scores and draws the Philox prefixes, the unit kernel selects
     if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    if (prm.dense) return launch_unit(prm, *shape, stream, true);   // every token, p = 1
     if ((st = launch(&score_input_kernel, (int64_t)pl.U * pl.ntile, kInThreads, 0, prm, stream, true)) != SSA_OK)
         return st;
     return launch_unit(prm, *shape, stream, true);
@@ -684,7 +717,41 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, c
     prm.lse = lse;
     prm.src_mode = 2;
     prm.attend = 1;
-    return launch_unit(prm, *shape, stream, false);   // one kernel: nothing to zero first
+    // K0 zeroes the unit counters the CTAs of a unit meet on
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    return launch_unit(prm, *shape, stream, true);
+}
+
+ssa_status ssa_attend_early_stop(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const int32_t* idx,
+                                 const float* p, const int32_t* count, int64_t list_cap, const float* s_hat,
+                                 float tau, float scale, float* out, float* lse, int32_t* blocks_opt, void* ws,
+                                 size_t ws_bytes, const ssa_shape* shape, cudaStream_t stream)
+{
+    ssa_status st = check_shape(shape);
+    if (st != SSA_OK) return st;
+    if (!q || !idx || !p || !count || !s_hat || !out || !lse || (shape->ctx_len > 0 && (!K || !V)))
+        return SSA_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
+    if (bad_scale(scale) || bad_tau(tau)) return SSA_ERR_INVALID_ARG;
+    const ssa::Plan pl = unit_plan(*shape);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (!device_readable(K, true) || !device_readable(V, true) || !device_readable(q, false)) return SSA_ERR_INVALID_ARG;
+    if (pl.U == 0) return SSA_OK;
+    ssa::Params prm = base_params(*shape, pl, ws);
+    prm.q = q;
+    prm.K = K;
+    prm.V = V;
+    prm.scale = scale;
+    prm.s_src = s_hat;
+    prm.idx_in = idx;
+    prm.p_in = p;
+    prm.count_in = count;
+    prm.cap = list_cap > 0 ? list_cap : std::max<int64_t>(shape->ctx_len, 1);
+    prm.out = out;
+    prm.lse = lse;
+    prm.src_mode = 2;
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;   // zeroes the unit counters
+    return launch_early_stop(prm, *shape, tau, blocks_opt, stream);
 }
 
 }  // extern "C"
@@ -786,14 +853,13 @@ ssa_status decode_impl(const AppendArgs* app, const ssa_paged_kv* pg, int strata
         if (pl.sf >= pl.nst) return SSA_ERR_UNSUPPORTED;
         set_append(prm, *app, shape->ctx_len - 1, *shape);
     }
-    // K0 zeroes the score kernel's queue and the histograms (and writes the
-    // appended token); a step that keeps every token and wants no scores
-    // runs the unit kernel alone
+    // K0 zeroes the unit counters, the score kernel's queue and the
+    // histograms (and writes the appended token); a step that keeps every
+    // token and wants no scores runs no score kernel
     const bool score = !empty && (!prm.dense || s_hat_opt);
-    const bool init = score || app || host_io;
-    if (init && (st = launch_init(prm, stream)) != SSA_OK) return st;
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
     if (score && (st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
-    return launch_unit(prm, *shape, stream, init);
+    return launch_unit(prm, *shape, stream, true);
 }
 
 }  // namespace
@@ -818,6 +884,57 @@ ssa_status ssa_decode_strata(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf1
     if (bad_strata(strata, top_p)) return SSA_ERR_INVALID_ARG;
     return decode_impl(nullptr, nullptr, strata, top_p, false, q, K, V, Ks, sel_ch, top_k, budget, seed, scale, out, lse,
                        s_hat_opt, idx_opt, p_opt, count_opt, list_cap, ws, ws_bytes, shape, stream);
+}
+
+ssa_status ssa_decode_early_stop(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V, const ssa_bf16* Ks,
+                                 const int32_t* sel_ch, int64_t top_k, float budget, uint64_t seed, float scale,
+                                 float tau, float* out, float* lse, int32_t* blocks_opt, void* ws, size_t ws_bytes,
+                                 const ssa_shape* shape, cudaStream_t stream)
+{
+    ssa_status st = check_shape(shape);
+    if (st != SSA_OK) return st;
+    const bool empty = shape->ctx_len == 0;
+    if (!q || !sel_ch || !out || !lse || (!empty && (!K || !V || !Ks))) return SSA_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16) || !aligned(Ks, 16) || !aligned(q, 16)) return SSA_ERR_INVALID_ARG;
+    if (bad_scalars(top_k, budget) || bad_scale(scale) || bad_tau(tau)) return SSA_ERR_INVALID_ARG;
+    const ssa::Plan pl = unit_plan(*shape);
+    if ((st = check_ws(ws, ws_bytes, pl)) != SSA_OK) return st;
+    if (!device_readable(K, true) || !device_readable(V, true) || !device_readable(Ks, false) ||
+        !device_readable(q, false) || !device_readable(out, false) || !device_readable(lse, false))
+        return SSA_ERR_INVALID_ARG;
+    if (pl.U == 0) return SSA_OK;
+    char* w = static_cast<char*>(ws);
+    ssa::Params prm = base_params(*shape, pl, ws);
+    if (!empty && (st = encode_summary_map(&prm.ks_map, Ks, *shape)) != SSA_OK) return st;
+    prm.q = q;
+    prm.K = K;
+    prm.V = V;
+    prm.sel_ch = sel_ch;
+    prm.scale = scale;
+    prm.budget = budget;
+    prm.seed = seed;
+    top_k = set_strata(prm, SSA_STRATA_SSA, top_k, 0.0f, shape->ctx_len);
+    float* scores = reinterpret_cast<float*>(w + pl.o_scores);
+    prm.s_dst = scores;
+    prm.s_src = scores;
+    prm.out = out;
+    prm.lse = lse;
+    prm.dense = (top_k >= shape->ctx_len || std::isinf(budget)) ? 1 : 0;
+    prm.src_mode = prm.dense ? 1 : 0;
+    // the selection writes each unit's list (ascending index) into the
+    // workspace's selection rows; the early-stop launches order and attend it
+    prm.attend = 0;
+    prm.idx_out = reinterpret_cast<int32_t*>(w + pl.o_sel_idx);
+    prm.p_out = reinterpret_cast<float*>(w + pl.o_sel_p);
+    prm.count_out = reinterpret_cast<int32_t*>(w + pl.o_es);
+    prm.cap = pl.np;
+    if ((st = launch_init(prm, stream)) != SSA_OK) return st;
+    if (!empty && (st = launch_score(prm, *shape, !prm.dense, stream, true)) != SSA_OK) return st;
+    if ((st = launch_unit(prm, *shape, stream, true)) != SSA_OK) return st;
+    prm.idx_in = prm.idx_out;
+    prm.p_in = prm.p_out;
+    prm.count_in = prm.count_out;
+    return launch_early_stop(prm, *shape, tau, blocks_opt, stream);
 }
 
 ssa_status ssa_decode_append(const ssa_bf16* q, const ssa_bf16* k_new, const ssa_bf16* v_new, ssa_bf16* K,

@@ -29,7 +29,8 @@ EXPORTS = [
     "ssa_status_string", "ssa_version", "ssa_workspace_bytes", "ssa_pack_summary", "ssa_score",
     "ssa_select", "ssa_attend", "ssa_decode", "ssa_decode_host", "ssa_get_device_status",
     "ssa_query_plan", "ssa_decode_static", "ssa_append", "ssa_decode_append", "ssa_select_capacity",
-    "ssa_select_strata", "ssa_decode_strata", "ssa_decode_paged",
+    "ssa_select_strata", "ssa_decode_strata", "ssa_decode_paged", "ssa_attend_early_stop",
+    "ssa_decode_early_stop",
 ]
 STRATA_SSA, STRATA_UNIFORM, STRATA_TOP_P = 0, 1, 2
 
@@ -92,6 +93,8 @@ def load_library():
         "ssa_decode_static": ([P, P, P, P, P, i64, f32, u64, f32, P, P, P, SP, P], ctypes.c_int),
         "ssa_decode_paged": ([P, P, P, P, P, P, ctypes.POINTER(ssa_paged_kv), P, i64, f32, u64, f32, P, P, P, P, P,
                               P, i64, P, sz, SP, P], ctypes.c_int),
+        "ssa_attend_early_stop": ([P, P, P, P, P, P, i64, P, f32, f32, P, P, P, P, sz, SP, P], ctypes.c_int),
+        "ssa_decode_early_stop": ([P, P, P, P, P, i64, f32, u64, f32, f32, P, P, P, P, sz, SP, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -258,6 +261,48 @@ def ssa_attend(q, K, V, idx, p, count, scale: float, out=None, lse=None, ws=None
                                      float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                      ctypes.byref(shape), _stream(stream)), "ssa_attend")
     return out, lse
+
+
+def ssa_attend_early_stop(q, K, V, idx, p, count, s_hat, tau: float, scale: float, out=None, lse=None, blocks=None,
+                          ws=None, stream=None):
+    """Corrected attention with S2O-style early stopping; returns (out, lse, blocks kept [Bt][Hkv])."""
+    shape = shape_of(q, K)
+    Bt, Hq, d = q.shape
+    Hkv = K.shape[1]
+    if out is None:
+        out = torch.empty((Bt, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Bt, Hq), dtype=torch.float32, device=q.device)
+    if blocks is None:
+        blocks = torch.empty((Bt, Hkv), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, idx.shape[-1], q.device)
+    _check(load_library().ssa_attend_early_stop(_ptr(q), _ptr(K), _ptr(V), _ptr(idx), _ptr(p), _ptr(count),
+                                                int(idx.shape[-1]), _ptr(s_hat), float(tau), float(scale), _ptr(out),
+                                                _ptr(lse), _ptr(blocks), _ptr(ws), ws.numel(), ctypes.byref(shape),
+                                                _stream(stream)), "ssa_attend_early_stop")
+    return out, lse, blocks
+
+
+def ssa_decode_early_stop(q, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale: float, tau: float,
+                          out=None, lse=None, blocks=None, ws=None, stream=None):
+    """The step with early-stopping attention; returns (out, lse, blocks kept [Bt][Hkv])."""
+    shape = shape_of(q, K, Ks)
+    Bt, Hq, d = q.shape
+    Hkv = K.shape[1]
+    if out is None:
+        out = torch.empty((Bt, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Bt, Hq), dtype=torch.float32, device=q.device)
+    if blocks is None:
+        blocks = torch.empty((Bt, Hkv), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, 0, q.device)
+    _check(load_library().ssa_decode_early_stop(_ptr(q), _ptr(K), _ptr(V), _ptr(Ks), _ptr(sel_ch), int(top_k),
+                                                float(budget), int(seed) & (2**64 - 1), float(scale), float(tau),
+                                                _ptr(out), _ptr(lse), _ptr(blocks), _ptr(ws), ws.numel(),
+                                                ctypes.byref(shape), _stream(stream)), "ssa_decode_early_stop")
+    return out, lse, blocks
 
 
 def ssa_decode(q, K, V, Ks, sel_ch, top_k: int, budget: float, seed: int, scale: float, out=None, lse=None,

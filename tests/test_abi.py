@@ -227,3 +227,25 @@ def test_paged_entry_point_validates():
     strided = _shape()                                                      # a contiguous shape's strides
     assert _paged_call(lib, strided, pages()) == 1
     assert _decode(lib, s) == 1                                             # ... and ssa_decode wants them
+
+
+def test_early_stop_entry_points_validate():
+    lib = ssa.load_library()
+    s = _shape()
+    f = P(1 << 20)
+    cap = 0
+    for tau in (-1.0, float("nan")):
+        assert lib.ssa_attend_early_stop(f, f, f, f, f, f, cap, f, tau, 0.1, f, f, None, f, 1 << 40,
+                                         ctypes.byref(s), None) == 1
+        assert lib.ssa_decode_early_stop(f, f, f, f, f, 5, 1.0, 0, 0.1, tau, f, f, None, f, 1 << 40,
+                                         ctypes.byref(s), None) == 1
+    assert lib.ssa_attend_early_stop(f, f, f, f, f, f, cap, None, 0.1, 0.1, f, f, None, f, 1 << 40,
+                                     ctypes.byref(s), None) == 1          # no scores to order by
+    assert lib.ssa_attend_early_stop(f, f, f, f, f, f, cap, f, 0.1, 0.0, f, f, None, f, 1 << 40,
+                                     ctypes.byref(s), None) == 1          # scale
+    assert lib.ssa_attend_early_stop(f, f, f, f, f, f, cap, f, float("inf"), 0.1, f, f, None, f, 16,
+                                     ctypes.byref(s), None) == 3          # +inf passes, the workspace does not
+    assert lib.ssa_decode_early_stop(f, f, f, f, f, -1, 1.0, 0, 0.1, 0.1, f, f, None, f, 1 << 40,
+                                     ctypes.byref(s), None) == 1
+    assert lib.ssa_decode_early_stop(f, f, f, f, f, 5, 1.0, 0, 0.1, 0.1, f, f, None, f, 16,
+                                     ctypes.byref(s), None) == 3

@@ -204,3 +204,55 @@ def test_decode_parity_with_frequent_histogram_handover(oracle_mod, name, run):
     assert stats.get("units_differing", 0) <= max(1, stats["units"] // 8), stats
     ref = gpu_decode(w, cfg.top_k, cfg.budget, 3)
     assert torch.equal(g["out"], ref["out"]) and torch.equal(g["count"], ref["count"])
+
+
+def test_workspace_reuse_and_junk():
+    """A workspace full of junk (apart from a cleared status word), and one reused across calls of every kind,
+    give the results of a fresh zeroed workspace bit for bit: each call resets the counters its kernels meet
+    on, including the calls that keep every token or attend given lists."""
+    w = case("g4_d128")
+    cfg = w["cfg"]
+    q, K, V, Ks, sel = w["q"], w["K"], w["V"], w["Ks"], w["sel_ch"]
+    shape = ssa.shape_of(q, K, Ks)
+    N = cfg.ctx_len
+
+    def junk_ws(shp):
+        ws = ssa.workspace(shp)
+        ws.fill_(0xA5)
+        ssa.ssa_get_device_status(ws)   # clears the status word
+        return ws
+
+    def dec(ws, k, B, seed, s_hat=None):
+        out = torch.full((cfg.batch, cfg.n_q_heads, cfg.head_dim), float("nan"), device=DEV)
+        lse = torch.full((cfg.batch, cfg.n_q_heads), float("nan"), device=DEV)
+        ssa.ssa_decode(q, K, V, Ks, sel, k, B, seed, cfg.scale, out=out, lse=lse, s_hat=s_hat, ws=ws)
+        return out, lse
+
+    calls = [(cfg.top_k, cfg.budget, 3), (cfg.top_k, math.inf, 0), (N + 5, cfg.budget, 0), (0, cfg.budget, 4)]
+    ref = [dec(None, *c) for c in calls]
+    ws = junk_ws(shape)
+    for _ in range(2):   # the second round finds the first one's counters
+        for c, r in zip(calls, ref):
+            out, lse = dec(ws, *c)
+            assert torch.equal(out, r[0]) and torch.equal(lse, r[1]), c
+    assert ssa.ssa_get_device_status(ws)[0] == 0
+
+    # the stage entry points: selection (sparse and every token) and attention over given lists
+    s_hat = ssa.ssa_score(q, Ks, sel, cfg.scale, K_like=K)
+    s_shape_ws = junk_ws(ssa.ssa.make_shape(cfg.batch, cfg.n_kv_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_sel, N))
+    for k, B in ((cfg.top_k, cfg.budget), (N, cfg.budget)):
+        r_idx, r_p, r_cnt = ssa.ssa_select(s_hat, k, B, 9)
+        for _ in range(2):
+            idx, p, cnt = ssa.ssa_select(s_hat, k, B, 9, ws=s_shape_ws)
+            assert torch.equal(cnt, r_cnt)
+            for b in range(cfg.batch):
+                for h in range(cfg.n_kv_heads):
+                    n = int(cnt[b, h])
+                    assert torch.equal(idx[b, h, :n], r_idx[b, h, :n]) and torch.equal(p[b, h, :n], r_p[b, h, :n])
+    r_out, r_lse = ssa.ssa_attend(q, K, V, r_idx, r_p, r_cnt, cfg.scale)
+    ws = junk_ws(shape)
+    for _ in range(2):
+        out = torch.full_like(r_out, float("nan"))
+        lse = torch.full_like(r_lse, float("nan"))
+        ssa.ssa_attend(q, K, V, r_idx, r_p, r_cnt, cfg.scale, out=out, lse=lse, ws=ws)
+        assert torch.equal(out, r_out) and torch.equal(lse, r_lse)
