@@ -58,6 +58,8 @@ def parse_args():
                     help="workload timed with K/V in pinned host memory ('' = none)")
     ap.add_argument("--paged", type=int, default=256,
                     help="page size of the paged-cache records of the main workload (0 = none)")
+    ap.add_argument("--early-stop", default="1e-3,1e-2",
+                    help="tau values of the early-stopping step records of the main workload ('' = none)")
     ap.add_argument("--plain-steps", type=int, default=0,
                     help="only run this many decode steps of --workload (L2 flushed before each) and exit: "
                          "the program the ncu summaries under profiles/ capture")
@@ -467,6 +469,50 @@ def time_paged(cfg, steps: int, warmup: int, dev, page_size: int, lens):
     return us, rows, clk.summary()
 
 
+def time_early_stop(cfg, steps: int, warmup: int, dev, tau: float):
+    """Mean us per ssa_decode_early_stop step of workload `cfg` (L2 flushed before every step, seed = step
+    index), and the mean fraction of the selected rows' 128-row blocks the attention kept."""
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    w = workloads.generate(cfg, 0, dev)
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    q, K, V, sel = w["q"], w["K"], w["V"], w["sel_ch"]
+    ws = ssa.workspace(ssa.shape_of(q, K, Ks), 0, dev)
+    out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((cfg.batch, cfg.n_q_heads), dtype=torch.float32, device=dev)
+    blocks = torch.zeros((steps, cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device=dev)
+    all_blocks = torch.zeros((4, cfg.batch, cfg.n_kv_heads), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        flush.fill_(i & 0xff)
+        ssa.ssa_decode_early_stop(q, K, V, Ks, sel, cfg.top_k, cfg.budget, 1_000_000 + i, cfg.scale, tau, out=out,
+                                  lse=lse, ws=ws, stream=stream)
+    for i in range(4):   # every block (tau = 0): the denominator of the kept fraction
+        ssa.ssa_decode_early_stop(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, 0.0, out=out, lse=lse,
+                                  blocks=all_blocks[i], ws=ws, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(20_000_000)
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            ssa.ssa_decode_early_stop(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, tau, out=out, lse=lse,
+                                      blocks=blocks[i], ws=ws, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    frac = blocks[:4].double().sum().item() / max(1.0, all_blocks.double().sum().item())
+    return us, frac, clk.summary()
+
+
 def config_record(cfg, us, rows, peak, clocks):
     ab = algorithmic_bytes(cfg, rows)
     gbs = ab / (us * 1e-6) / 1e9
@@ -615,6 +661,16 @@ def run_ours(args):
                 "value": round(us, 3), "unit": UNIT, "steps": steps_p, "rows_selected_per_step": round(rows, 1),
                 "algorithmic_bytes_per_step": int(ab), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                 "clocks": clk, "api": "ssa_decode_paged"})
+            torch.cuda.empty_cache()
+    if rank == 0 and args.early_stop:
+        # the step with S2O-style early stopping of the attention (ssa_decode_early_stop)
+        line["early_stop"] = []
+        for tau in [float(x) for x in args.early_stop.split(",") if x]:
+            steps_e = max(20, min(args.steps, 300))
+            us, frac, clk = time_early_stop(cfg, steps_e, max(3, min(args.warmup, 10)), dev, tau)
+            line["early_stop"].append({"workload": cfg.name, "tau": tau, "value": round(us, 3), "unit": UNIT,
+                                       "steps": steps_e, "blocks_kept_frac": round(frac, 4), "clocks": clk,
+                                       "api": "ssa_decode_early_stop"})
             torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle as it stands, on this host's cores, on a bounded sample of the same workload

@@ -11,8 +11,11 @@ parity tests pin against the oracle.  The uniform hybrid keeps the same
 top-k stratum and draws every other token with p = B / (N - k), with the
 same Philox uniforms (the library's SSA_STRATA_UNIFORM); the top-p stratum
 (SSA_STRATA_TOP_P, top_p = 0.9) keeps the tokens holding 90 % of the
-estimated softmax and samples the rest as SSA does.  The numbers are
-printed as one JSON line; the assertions are only sanity bounds.
+estimated softmax and samples the rest as SSA does.  SSA with S2O-style
+early stopping ("S2O ...", technical summary, Method section 2; the
+library's ssa_decode_early_stop) is reported for a sweep of tau, with the
+fraction of the selected rows' blocks it kept.  The numbers are printed as
+one JSON line; the assertions are only sanity bounds.
 """
 import json
 import math
@@ -42,7 +45,10 @@ def _stats(x):
 def test_error_vs_dense_statistic():
     cfg = workloads.CONFIGS["ministral8b_32k"]
     k, B = cfg.top_k, cfg.budget
+    taus = (1e-4, 1e-3, 1e-2)
     errs = {"ssa": [], "topk": [], "uniform_hybrid": [], "top_p_0.9": []}
+    errs.update({f"ssa_early_stop_{t:g}": [] for t in taus})
+    kept = {t: [] for t in taus}
     for seed in range(3):
         w = workloads.generate(cfg, seed, DEV)
         Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
@@ -56,13 +62,22 @@ def test_error_vs_dense_statistic():
         out_uh, _ = ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.ssa.STRATA_UNIFORM, k, 0.0, B, seed, cfg.scale)
         # the top-p stratum (the tokens holding 90 % of the estimated softmax) with the SSA sampler on the rest
         out_tp, _ = ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.ssa.STRATA_TOP_P, 0, 0.9, B, seed, cfg.scale)
+        for t in taus:
+            out_es, _, blocks = ssa.ssa_decode_early_stop(q, K, V, Ks, sel, k, B, seed, cfg.scale, t)
+            errs[f"ssa_early_stop_{t:g}"].append(_rel_err(out_es, dense))
+            kept[t].append(blocks.float().sum().item())
+        all_blocks = ssa.ssa_decode_early_stop(q, K, V, Ks, sel, k, B, seed, cfg.scale, 0.0)[2].float().sum().item()
+        for t in taus:
+            kept[t][-1] /= all_blocks
         torch.cuda.synchronize()
         errs["ssa"].append(_rel_err(out_ssa, dense))
         errs["topk"].append(_rel_err(out_topk, dense))
         errs["uniform_hybrid"].append(_rel_err(out_uh, dense))
         errs["top_p_0.9"].append(_rel_err(out_tp, dense))
     report = {m: _stats(v) for m, v in errs.items()}
+    for t in taus:
+        report[f"ssa_early_stop_{t:g}"]["blocks_kept_frac"] = float(np.mean(kept[t]))
     report["config"] = {"workload": cfg.name, "top_k": k, "budget": B, "seeds": 3, "heads": int(errs["ssa"][0].size)}
     print("error_vs_dense", json.dumps(report))
-    for m in ("ssa", "topk", "uniform_hybrid", "top_p_0.9"):   # sanity only: heads with a small dense output dominate the tail
+    for m in errs:   # sanity only: heads with a small dense output dominate the tail
         assert math.isfinite(report[m]["mean"]) and report[m]["p50"] < 1.0, (m, report[m])
