@@ -61,8 +61,8 @@ def parse_args():
     ap.add_argument("--early-stop", default="1e-3,1e-2",
                     help="tau values of the early-stopping step records of the main workload ('' = none)")
     ap.add_argument("--plain-steps", type=int, default=0,
-                    help="only run this many decode steps of --workload (L2 flushed before each) and exit: "
-                         "the program the ncu summaries under profiles/ capture")
+                    help="only run this many decode steps of --workload, then as many ssa_score launches (L2 "
+                         "flushed before each), and exit: the program the ncu summaries under profiles/ capture")
     return ap.parse_args()
 
 
@@ -719,6 +719,11 @@ def run_plain(args):
     for i in range(args.plain_steps):
         flush.fill_(i & 0xff)
         ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, ws=ws)
+    # then as many launches of the roofline kernel as the bench times it (ssa_score alone)
+    s_hat = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.ctx_len), dtype=torch.float32, device=dev)
+    for i in range(args.plain_steps):
+        flush.fill_(i & 0xff)
+        ssa.ssa_score(q, Ks, sel, cfg.scale, s_hat=s_hat, ws=ws)
     st, flags = ssa.ssa_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags:#x}")

@@ -257,9 +257,11 @@ ssa_status ssa_attend(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
  * kept; tau = 0 keeps every block, i.e. ssa_attend's result up to the
  * summation order; tau > 1 keeps block 0 only).  out / lse are the corrected
  * attention over the kept blocks; blocks_opt [batch][n_kv_heads] (may be
- * NULL) receives the number of blocks kept.  One CTA per unit attends, in
- * order, and reads no row of a block after the stop.  A unit's list holds at
- * most 32768 rows here: a longer one keeps its first 32768 entries and sets
+ * NULL) receives the number of blocks kept.  The blocks are attended in
+ * parallel (each CTA of the unit a run of them) and the gain test is applied
+ * when their partial results are merged, so every selected row is read; the
+ * test decides which blocks enter the result.  A unit's list holds at most
+ * 32768 rows here: a longer one keeps its first 32768 entries and sets
  * SSA_DEV_OVERFLOW.  tau must be >= 0 (+inf allowed). */
 ssa_status ssa_attend_early_stop(const ssa_bf16* q, const ssa_bf16* K, const ssa_bf16* V,
                                  const int32_t* idx, const float* p, const int32_t* count, int64_t list_cap,

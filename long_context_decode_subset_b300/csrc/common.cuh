@@ -20,6 +20,9 @@
 //               cores; the last CTA of the unit merges the (m, l, acc)
 //               partials.  The grid is one wave (every unit's CTAs resident
 //               at once) and every wait has a time limit.
+// K1 and K2 have separate instantiations for a paged cache (page pools and
+// a block table), and K2 one for the early-stop attention, which follows an
+// ordering kernel (one CTA per unit sorts its list by score).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -57,6 +60,7 @@ constexpr int kBins = 4096;            // 12-bit order-key buckets
 constexpr int kStageTok = 512;         // K1: tokens per pipeline stage (4 MMA tiles of 128)
 constexpr int kTileAlign = 512;        // K2: tiles are multiples of 512 tokens (32 per warp slice)
 constexpr int kMaxTiles = 64;          // K2: tiles (CTAs) per unit at most
+constexpr int kEsMaxRows = 32768;      // early stop: rows of a unit's list the ordering kernel sorts at most
 constexpr int kSelThreads = 512;       // K2 block size; in the selection each warp owns a slice (a list) of the tile
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kInThreads = 256;        // score_input_kernel block size
@@ -94,7 +98,8 @@ struct Plan {
     // workspace byte offsets
     int32_t tcap;        // tiles the per-tile arrays hold per unit (>= ntile)
     size_t o_status, o_ctrl, o_hist1, o_zpart, o_kcnt, o_part, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
-        o_hout, o_hlse, o_topp, o_es, total;
+        o_hout, o_hlse, o_topp, o_es, o_esp, total;
+    int32_t esb;         // early stop: 128-row blocks a unit's ordered list holds at most
 };
 
 // ---------------------------------------------------------------------------

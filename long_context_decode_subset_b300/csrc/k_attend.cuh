@@ -260,6 +260,70 @@ template <int G, int D, int LIST, bool PAGED = false>
 constexpr uint32_t unit_smem_bytes() { return UCfg<G, D, LIST, PAGED>::SMEM; }
 
 
+// Early stop: the number of leading blocks the unit keeps ("S2O ...",
+// technical summary, Method section 2).  parts holds nb block partials
+// (acc [G][D], m [G], l [G]); with M_g the largest m of head g and
+// w_g(b) = l_g(b) exp(m_g(b) - M_g), block b's gain ratio is
+// w_g(b) / sum_{b' <= b} w_g(b'), and the unit stops after the first block
+// whose ratio is below tau for every head (block 0 included always).
+// Block-wide (kSelThreads); uses nb * G * 2 floats of `sm` and misc[6].
+// Every thread returns the count.
+template <int G, int D>
+__device__ __noinline__ int es_keep_blocks(const Params& p, const float* parts, int nb, float* sm, uint32_t* misc)
+{
+    constexpr int PS = G * D + 2 * G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float* w = sm;            // [nb][G]
+    float* mx = sm + nb * G;  // [G]
+    for (int i = tid; i < nb * G; i += kSelThreads) w[i] = __ldcg(parts + (size_t)(i / G) * PS + G * D + (i % G));
+    if (tid == 0) misc[6] = (uint32_t)nb;
+    __syncthreads();
+    // per head (one warp each): the largest m, then the inclusive prefix of w and the test
+    if (warp < G) {
+        float m = -INFINITY;
+        for (int b = lane; b < nb; b += 32) m = fmaxf(m, w[b * G + warp]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) mx[warp] = m;
+    }
+    __syncthreads();
+    if (warp < G) {
+        const float M = mx[warp];
+        float run = 0.0f;
+#pragma unroll 1
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+            const int b = b0 + lane;
+            float wb = 0.0f;
+            if (b < nb) {
+                const float mb = w[b * G + warp];
+                const float lb = __ldcg(parts + (size_t)b * PS + G * D + G + warp);
+                wb = (mb == -INFINITY) ? 0.0f : lb * expf(mb - M);
+            }
+            float incl = wb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float pref = run + incl;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+            // a block of this head is "below" when its share is under tau; kept in the sign of w
+            if (b < nb) w[b * G + warp] = (wb < p.tau * pref) ? 1.0f : 0.0f;
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < nb; b += kSelThreads) {
+        bool all = true;
+#pragma unroll
+        for (int g = 0; g < G; ++g) all = all && w[b * G + g] != 0.0f;
+        if (all) atomicMin(&misc[6], (uint32_t)b);
+    }
+    __syncthreads();
+    const int stop = (int)misc[6];
+    __syncthreads();
+    return stop < nb ? stop + 1 : nb;
+}
+
 // Thread roles in the attention (kSelThreads): warps 0-3 epilogue
 // (tensor-memory lanes = chunk rows for S, = head dims for O), warp 4 issues
 // the MMAs (and owns the tensor memory), warps 5 .. 15 gather the K and V
@@ -307,7 +371,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
             mbar_init(&p_ready[i], 4);   // one arrive per epilogue warp
             mbar_init(&o_full[i], 1);
         }
-        misc[6] = 0xffffffffu;   // early stop: the block after which the attention stops (none yet)
         fence_mbar_init();
     }
     if (warp == 4 && p.attend) tmem_alloc(&misc[0], CF::TCOLS);
@@ -351,6 +414,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     UnitCtrl* ctrl = ws_ctrl(p) + u;
     UnitSel us{0u, -1, 0.0f, 0.0f, false};
     int64_t lo = 0, hi = 0;
+    int32_t es_nb = 0, es_b0 = 0;   // early stop: the unit's blocks, this CTA's first block
     int mode = p.src_mode;
     SelShared& sh = *reinterpret_cast<SelShared*>(smem + CF::OFF_SEL);
     // the stratum's size: k, or (top-p) found from the unit's score masses;
@@ -393,8 +457,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     } else {
         const int64_t c = p.count_in[u];
         const int64_t total = c < 0 ? 0 : (c > p.cap ? p.cap : c);
-        lo = total * r / C;
-        hi = total * (r + 1) / C;
+        if constexpr (ES) {   // whole 128-row blocks of the ordered list
+            es_nb = (int32_t)((total + CF::CH - 1) / CF::CH);
+            es_b0 = (int32_t)((int64_t)es_nb * r / C);
+            lo = (int64_t)es_b0 * CF::CH;
+            hi = min(total, (int64_t)es_nb * (r + 1) / C * CF::CH);
+        } else {
+            lo = total * r / C;
+            hi = total * (r + 1) / C;
+        }
     }
     SSA_MARK(11);
     us.sampling = p.budget > 0.0f && us.Z > 0.0f;
@@ -414,8 +485,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     }
     int gbase = 0;        // chunks done before this list chunk
     int64_t kept = 0;
-    bool es_stopped = false;   // early stop: the epilogue has kept its last block
-    int32_t es_blocks = 0;     // ... and the blocks it kept
     const uint32_t k_a = smem_addr(smem + CF::OFF_K), v_a = smem_addr(smem + CF::OFF_V);
     const uint32_t q_a = smem_addr(smem + CF::OFF_Q), p_a = smem_addr(smem + CF::OFF_P);
 #pragma unroll 1
@@ -445,8 +514,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                 unsigned char* kd = smem + CF::OFF_K + bf * CF::KV;
                 unsigned char* vd = smem + CF::OFF_V + bf * CF::KV;
                 int64_t* roff = reinterpret_cast<int64_t*>(smem + CF::OFF_ROFF) + bf * CF::CH;
-                // early stop: the chunks past the last kept block are not read (their buffers are zero-filled)
-                const int lim = ES ? ((uint32_t)g > *reinterpret_cast<volatile uint32_t*>(&misc[6]) ? 0 : nk) : nk;
                 if constexpr (PAGED) {
                     // the chunk's pool rows, once per row (double-buffered: a buffer is rewritten only after
                     // every gather thread has passed the next chunk's barrier)
@@ -464,7 +531,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     int64_t j;
                     if constexpr (PAGED) j = roff[i];
                     else j = valid ? (int64_t)cidx[row] : 0;
-                    const bool load = ES ? row < lim : valid;
+                    const bool load = valid;
                     const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
                     cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, load);
                     cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, load);
@@ -596,8 +663,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     for (int k = 0; k < 2 * G; ++k) o[k] = __uint_as_float(rr[k]);
                 }
                 tc_fence_before();
-                bool below = true;   // early stop: this block's share is under tau for every head
-                if (!ES || !es_stopped) {
+                if constexpr (ES) {
+                    // early stop: every block's own (m, l, acc) partial; the merge applies the gain test
+                    constexpr int PS = G * D + 2 * G;
+                    float* bp = ws_es_part(p) + ((size_t)u * pl.esb + (size_t)(es_b0 + g)) * PS;
+                    if (tid < D) {
+#pragma unroll
+                        for (int gg = 0; gg < G; ++gg) bp[gg * D + tid] = o[gg] + o[G + gg];
+                    }
+                    if (tid == 0) {
+#pragma unroll
+                        for (int gg = 0; gg < G; ++gg) {
+                            bp[G * D + gg] = mc[gg];
+                            bp[G * D + G + gg] = lc[gg];
+                        }
+                    }
+                } else {
 #pragma unroll
                     for (int gg = 0; gg < G; ++gg) {
                         const float mn = fmaxf(m_run[gg], mc[gg]);
@@ -606,25 +687,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                         acc[gg] = acc[gg] * ar + (o[gg] + o[G + gg]) * ac;
                         l_run[gg] = l_run[gg] * ar + lc[gg] * ac;
                         m_run[gg] = mn;
-                        if constexpr (ES) below = below && (lc[gg] * ac < p.tau * l_run[gg]);
-                    }
-                }
-                if constexpr (ES) {
-                    if (!es_stopped) {
-                        ++es_blocks;
-                        if (below) {
-                            es_stopped = true;
-                            if (tid == 0) *reinterpret_cast<volatile uint32_t*>(&misc[6]) = (uint32_t)g;
-                        }
                     }
                 }
             }
         }
         gbase += nc;
         __syncthreads();   // every role is done with this list chunk
-        if (ES && *reinterpret_cast<volatile uint32_t*>(&misc[6]) != 0xffffffffu) break;   // stopped early
     }
-    if (ES && tid == 0 && p.blocks_out) p.blocks_out[u] = es_blocks;
     SSA_MARK(8);
 
     // this CTA's partial (acc per head dim, then (m, l) per head) in the
@@ -712,6 +781,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     // the partials are staged in shared memory (the K/V chunk buffers) a
     // group at a time with one wave of copies, then merged in rank order
     const float* parts = ws_part(p) + (size_t)u * pl.tcap * PS;
+    int nparts = C;
+    if constexpr (ES) {
+        // the blocks' partials, the first es_keep of them: the gain test on the blocks' (m, l)
+        parts = ws_es_part(p) + (size_t)u * pl.esb * PS;
+        nparts = es_keep_blocks<G, D>(p, parts, es_nb, reinterpret_cast<float*>(smem), misc);
+        if (tid == 0 && p.blocks_out) p.blocks_out[u] = nparts;
+    }
     float* sp = reinterpret_cast<float*>(smem);
     constexpr int KB = (int)(CF::OFF_Q / (PS * 4u));   // partials per group
     static_assert(KB >= 1, "a partial fits the staging");
@@ -723,8 +799,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
 #pragma unroll
     for (int e = 0; e < EPT; ++e) A[e] = 0.0f;
 #pragma unroll 1
-    for (int k0 = 0; k0 < C; k0 += KB) {
-        const int nk = min(KB, C - k0);
+    for (int k0 = 0; k0 < nparts; k0 += KB) {
+        const int nk = min(KB, nparts - k0);
         if (k0 > 0) __syncthreads();   // the previous group is consumed
 #pragma unroll 1
         for (int i = tid; i < nk * PS; i += kSelThreads) cp_async_4(sp + i, parts + (size_t)k0 * PS + i);
@@ -781,7 +857,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
 // sets SSA_DEV_BAD_INDEX and sorts last.  The input may be those same rows:
 // every read of a pass ends before its writes begin.
 constexpr int kOrderThreads = 1024;
-constexpr int kOrderCap = 32768;
+constexpr int kOrderCap = kEsMaxRows;
 constexpr uint32_t kOrderSmem = (uint32_t)kOrderCap * 6u;   // keys (4 B) and positions (2 B)
 
 __global__ void __launch_bounds__(kOrderThreads, 1) order_kernel(const __grid_constant__ Params p)

@@ -95,9 +95,9 @@ struct Params {
     const int32_t* block_table;
     const int32_t* seq_lens;
     // early stop (the unit kernel's early-stop variant): the list of each
-    // unit is in descending score order; the attention stops after the first
-    // 128-row block whose share of the softmax denominator is below tau for
-    // every head, and writes the number of blocks it kept to blocks_out [U]
+    // unit is in descending score order; the attention keeps the blocks of
+    // 128 rows up to the first whose share of the softmax denominator is
+    // below tau for every head, and writes their number to blocks_out [U]
     float tau;
     int32_t* blocks_out;
 };
@@ -116,6 +116,7 @@ __device__ __forceinline__ int32_t* ws_sel_idx(const Params& p) { return reinter
 __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_sel_p); }
 __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
 __device__ __forceinline__ int32_t* ws_es_count(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_es); }
+__device__ __forceinline__ float* ws_es_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_esp); }
 
 // Strata 1 (top-k + uniform): the remainder's size n - min(k, n) in fp32,
 // the normaliser Z of p = min(1, B / Z) for a unit of n tokens.

@@ -114,6 +114,9 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     pl.o_hlse = take((size_t)heads * 4);
     pl.o_topp = take((size_t)U * kTopPUnitBytes);
     pl.o_es = take((size_t)U * 4);
+    // early stop: every block's (acc, m, l) partial
+    pl.esb = (int32_t)((std::min<int64_t>(kEsMaxRows, pl.np) + 127) / 128);
+    pl.o_esp = take((size_t)U * pl.esb * (size_t)(G * D + 2 * G) * 4);
     pl.total = o;
     return pl;
 }
@@ -484,8 +487,10 @@ ssa_status launch_unit(const ssa::Params& p, const ssa_shape& s, cudaStream_t st
 
 // The early-stop attention after the lists are known (prm.idx_in / p_in /
 // count_in / cap, scores prm.s_src): the order kernel sorts each unit's list
-// into the workspace, then the unit kernel's early-stop variant (one CTA per
-// unit) attends over it in that order.  Both wait for the previous kernel.
+// into the workspace, then the unit kernel's early-stop variant attends over
+// it, each CTA a run of whole 128-row blocks, and the last CTA of the unit
+// applies the gain test to the blocks' partials and merges the kept ones.
+// Both wait for the previous kernel.
 ssa_status launch_early_stop(ssa::Params prm, const ssa_shape& s, float tau, int32_t* blocks, cudaStream_t stream)
 {
     ssa_status st = launch(&order_kernel, prm.pl.U, kOrderThreads, kOrderSmem, prm, stream, true);
@@ -495,7 +500,6 @@ ssa_status launch_early_stop(ssa::Params prm, const ssa_shape& s, float tau, int
     prm.p_in = reinterpret_cast<const float*>(w + prm.pl.o_sel_p);
     prm.count_in = reinterpret_cast<const int32_t*>(w + prm.pl.o_es);
     prm.cap = prm.pl.np;
-    prm.pl.ntile = 1;
     prm.src_mode = 2;
     prm.attend = 1;
     prm.idx_out = nullptr;
@@ -505,7 +509,7 @@ ssa_status launch_early_stop(ssa::Params prm, const ssa_shape& s, float tau, int
     prm.blocks_out = blocks;
     uint32_t smem = 0;
     kfn_t fn = pick_unit(prm.pl.G, s.head_dim, &smem, kVarEarlyStop);
-    return launch(fn, prm.pl.U, kSelThreads, smem, prm, stream, true);
+    return launch(fn, (int64_t)prm.pl.U * prm.pl.ntile, kSelThreads, smem, prm, stream, true);
 }
 
 bool bad_tau(float tau) { return !(tau >= 0.0f); }
