@@ -114,8 +114,9 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     pl.o_hlse = take((size_t)heads * 4);
     pl.o_topp = take((size_t)U * kTopPUnitBytes);
     pl.o_es = take((size_t)U * 4);
-    // early stop: every block's (acc, m, l) partial
-    pl.esb = (int32_t)((std::min<int64_t>(kEsMaxRows, pl.np) + 127) / 128);
+    // early stop: every block's (acc, m, l) partial (sized, like the token
+    // arrays, for the largest tiling: the layout does not depend on the plan)
+    pl.esb = (int32_t)((std::min<int64_t>(kEsMaxRows, npmax) + 127) / 128);
     pl.o_esp = take((size_t)U * pl.esb * (size_t)(G * D + 2 * G) * 4);
     pl.total = o;
     return pl;

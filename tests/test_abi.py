@@ -249,3 +249,21 @@ def test_early_stop_entry_points_validate():
                                      ctypes.byref(s), None) == 1
     assert lib.ssa_decode_early_stop(f, f, f, f, f, 5, 1.0, 0, 0.1, 0.1, f, f, None, f, 16,
                                      ctypes.byref(s), None) == 3
+
+
+@pytest.mark.parametrize("tile,split", [(None, None), (None, 1), (None, 5), (None, 64), (512, 64), (1024, 7),
+                                        (4096, 2)])
+def test_workspace_size_does_not_depend_on_the_tiling(monkeypatch, tile, split):
+    """ssa_workspace_bytes is the size every call checks against, whatever tiling the plan picks: the layout
+    is sized for the largest tiling."""
+    if tile:
+        monkeypatch.setenv("SSA_FORCE_TILE", str(tile))
+    if split:
+        monkeypatch.setenv("SSA_FORCE_SPLIT", str(split))
+    lib = ssa.load_library()
+    for shp in (_shape(), _shape(batch=1, n_q_heads=2, n_kv_heads=2, head_dim=64, d_sel=16, ctx_len=1500),
+                _shape(batch=8, n_q_heads=32, n_kv_heads=16, ctx_len=131072)):
+        n = ssa.ssa_workspace_bytes(shp)
+        # the checks pass up to the workspace; then the fake pointers are refused (1), never the size (3)
+        assert _decode(lib, shp, ws_bytes=n) == 1
+        assert _decode(lib, shp, ws_bytes=n - 256) == 3
