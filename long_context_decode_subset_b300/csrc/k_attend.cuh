@@ -225,7 +225,7 @@ static_assert((5 + kUGatherWarps) * 32 == kSelThreads, "the attention roles fill
 // whatever it holds) are never read back.
 constexpr int kPageCache = 2048;   // block-table entries of its tile a CTA keeps in shared memory (paged)
 
-template <int G, int D, int LIST, bool PAGED = false>   // LIST: list entries staged at a time (1024 or 4096)
+template <int G, int D, int LIST, bool PAGED = false>   // LIST: list entries staged at a time
 struct UCfg {
     static constexpr int CH = 128;                                 // listed rows per chunk
     static constexpr uint32_t PLANE = CH * 128u;                   // 64 dims x 128 rows, 128-byte swizzle

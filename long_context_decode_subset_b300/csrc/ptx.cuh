@@ -60,7 +60,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 
 // Wait for phase `parity` of `bar` to complete, for at most `limit_ns`.
 // Returns false on timeout (the caller records it and carries on, so that
-// every CTA still reaches every cluster barrier).
+// every thread still reaches every block barrier).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull)
 {

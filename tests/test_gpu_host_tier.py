@@ -84,3 +84,19 @@ def test_pageable_host_memory_is_refused():
     with pytest.raises(ssa.SsaError) as e:   # the summary must be device memory
         ssa.ssa_decode(q, K, V, Ks.cpu().pin_memory(), sel, cfg.top_k, cfg.budget, 0, cfg.scale)
     assert e.value.status == 1
+
+
+def test_host_resident_paged_pools():
+    """The paged serving layout with its K and V pools in pinned host memory (the summary pool in HBM): the
+    step equals the device-resident paged step bit for bit, ragged lengths included."""
+    cfg = SMALL
+    w = workloads.generate(cfg, 3, "cuda")
+    Ks = ssa.ssa_pack_summary(w["K"], w["sel_ch"])
+    N = cfg.ctx_len
+    pg = workloads.to_paged(w["K"], w["V"], Ks, [N, N // 3 + 5], 128, seed=4)
+    Kh, Vh = _pinned(pg["K_pool"]), _pinned(pg["V_pool"])
+    args = (pg["Ks_pool"], pg["block_table"], pg["seq_lens"], w["sel_ch"], cfg.top_k, cfg.budget, 7, cfg.scale, N)
+    out_d, lse_d = ssa.ssa_decode_paged(w["q"], pg["K_pool"], pg["V_pool"], *args)
+    out_h, lse_h = ssa.ssa_decode_paged(w["q"], Kh, Vh, *args)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d) and torch.equal(lse_h, lse_d)
