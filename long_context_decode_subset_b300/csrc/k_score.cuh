@@ -291,7 +291,8 @@ constexpr uint32_t k1_smem_bytes() { return K1Cfg<DSEL, HIST>::SMEM; }
 
 // K1's work: every unit's stages j < sf are split evenly and contiguously over
 // the CTAs in (unit, j) order; the stages j >= sf of all units form a queue, in
-// (unit, j) order, that the CTAs drain kGrab at a time once their own share is
+// (unit, j) order, that the CTAs drain kGrab at a time (its last `grid` stages
+// one at a time) once their own share is
 // done (a counter in unit 0's control block, zeroed by K0), so that CTAs that
 // stream faster take more of it.  A unit of n tokens has ceil(n / 512) stages,
 // sf = 3/4 of them (rounded down) static: the same for every unit of a
@@ -358,9 +359,9 @@ struct K1Sched {
             grid_dep_wait();   // K0 has zeroed the counter
             waited = true;
         }
-        if constexpr (!PAGED) return (int64_t)atomicAdd(counter, (uint32_t)kGrab);
+        if constexpr (!PAGED) return (int64_t)atomicAdd(counter, 1u);
         uint32_t v = 0;
-        if ((threadIdx.x & 31) == 0) v = atomicAdd(counter, (uint32_t)kGrab);
+        if ((threadIdx.x & 31) == 0) v = atomicAdd(counter, 1u);
         return (int64_t)__shfl_sync(0xffffffffu, v, 0);
     }
     // paged: move cursor c forward to the sequence holding index g of its
@@ -428,9 +429,14 @@ struct K1Sched {
         if (d_cur == d_end) {
             if (dtotal == 0) return false;
             if (pending < 0) pending = grab();
-            if (pending >= dtotal) return false;
-            d_cur = pending;
-            d_end = min(pending + kGrab, dtotal);
+            // ticket t: stages [kGrab t, kGrab t + kGrab) while the queue is long, then single stages for its
+            // last `grid` stages, so that the CTAs run out of work within a stage of one another
+            const int64_t tail = min(dtotal, (int64_t)gridDim.x);
+            const int64_t pairs = (dtotal - tail) / kGrab;
+            const int64_t d0 = pending < pairs ? pending * kGrab : pairs * kGrab + (pending - pairs);
+            if (d0 >= dtotal) return false;
+            d_cur = d0;
+            d_end = pending < pairs ? d0 + kGrab : d0 + 1;
             pending = grab();   // the next chunk's grab goes out now
         }
         return locate(p, d_cur++, true, u, j, len);
