@@ -60,6 +60,8 @@ def parse_args():
                     help="page size of the paged-cache records of the main workload (0 = none)")
     ap.add_argument("--early-stop", default="1e-3,1e-2",
                     help="tau values of the early-stopping step records of the main workload ('' = none)")
+    ap.add_argument("--plain-early-stop", type=float, default=None,
+                    help="with --plain-steps: run ssa_decode_early_stop with this tau instead of ssa_decode")
     ap.add_argument("--plain-steps", type=int, default=0,
                     help="only run this many decode steps of --workload, then as many ssa_score launches (L2 "
                          "flushed before each), and exit: the program the ncu summaries under profiles/ capture")
@@ -718,7 +720,11 @@ def run_plain(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for i in range(args.plain_steps):
         flush.fill_(i & 0xff)
-        ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, ws=ws)
+        if args.plain_early_stop is not None:
+            ssa.ssa_decode_early_stop(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, args.plain_early_stop,
+                                      ws=ws)
+        else:
+            ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, i, cfg.scale, ws=ws)
     # then as many launches of the roofline kernel as the bench times it (ssa_score alone)
     s_hat = torch.empty((cfg.batch, cfg.n_kv_heads, cfg.ctx_len), dtype=torch.float32, device=dev)
     for i in range(args.plain_steps):

@@ -98,8 +98,9 @@ struct Plan {
     // workspace byte offsets
     int32_t tcap;        // tiles the per-tile arrays hold per unit (>= ntile)
     size_t o_status, o_ctrl, o_hist1, o_zpart, o_kcnt, o_part, o_cand, o_sel_idx, o_sel_p, o_scores, o_ubuf, o_hq,
-        o_hout, o_hlse, o_topp, o_es, o_esp, total;
+        o_hout, o_hlse, o_topp, o_es, o_esp, o_ess, total;
     int32_t esb;         // early stop: 128-row blocks a unit's ordered list holds at most
+    int32_t esr;         // early stop: rows a unit's ordered list holds at most (the sort's buffers)
 };
 
 // ---------------------------------------------------------------------------

@@ -849,83 +849,163 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
 // technical summary, Method section 2: blocks are processed in descending
 // estimated importance.)  One CTA of kOrderThreads per unit sorts the unit's
 // list (idx_in / p_in, count_in entries, row stride cap) by its rows'
-// scores s_src[u][idx] descending, ties by list position -- a bitonic sort
-// of (order key, position) pairs in shared memory -- and writes the ordered
-// list to the workspace's selection rows (stride pl.np) and its length to
-// the early-stop counts.  Lists longer than kOrderCap (or than a row) keep
-// their first entries and set SSA_DEV_OVERFLOW; an index outside [0, N)
-// sets SSA_DEV_BAD_INDEX and sorts last.  The input may be those same rows:
-// every read of a pass ends before its writes begin.
+// scores s_src[u][idx] descending, ties by list position, and writes the
+// ordered list to the workspace's selection rows (stride pl.np) and its
+// length to the early-stop counts.
+//
+// The sort is a least-significant-digit radix sort of the 32-bit keys
+// (~order key, so ascending is descending score), four passes of 8 bits,
+// each stable: warp w owns a contiguous run of the elements and walks it 32
+// at a time, an element's rank among the batch's equal digits comes from
+// eight ballots (one per digit bit), and the digits' offsets are an exclusive scan over
+// (digit, warp) -- so equal keys keep their list order.  The elements (key,
+// position) ping-pong between two arrays, in shared memory for lists of up to
+// kOrderSmemRows rows and in the workspace for longer ones (the CTA's own
+// writes, read back after a block barrier).  Lists longer than
+// kOrderCap (or than a row) keep their first entries and set
+// SSA_DEV_OVERFLOW; an index outside [0, N) sets SSA_DEV_BAD_INDEX and sorts
+// last.  The input may be the output rows: every read of the input ends
+// before the first write.
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderCap = kEsMaxRows;
-constexpr uint32_t kOrderSmem = (uint32_t)kOrderCap * 6u;   // keys (4 B) and positions (2 B)
+constexpr int kOrderWarps = kOrderThreads / 32;
+constexpr uint32_t kOrderCounters = (uint32_t)kOrderWarps * 256u * 4u;   // per-warp digit counters
+constexpr int kOrderSmemRows = 12288;   // lists up to this long sort in shared memory, longer ones in the workspace
+constexpr uint32_t kOrderSmem = kOrderCounters + (uint32_t)kOrderWarps * 4u +   // + the scan's scratch
+                                2u * kOrderSmemRows * 8u;                       // + the two element arrays
+
+// The lanes of the warp whose 8-bit digit equals this lane's, among the
+// lanes with `ok` set (eight ballots, one per bit).
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, bool ok)
+{
+    uint32_t peers = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const bool bit = (d >> b) & 1u;
+        const uint32_t m = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
 
 __global__ void __launch_bounds__(kOrderThreads, 1) order_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(16) unsigned char osm[];
-    uint32_t* key = reinterpret_cast<uint32_t*>(osm);
-    uint16_t* pos = reinterpret_cast<uint16_t*>(osm + (size_t)kOrderCap * 4);
+    // [warp][digit] (a warp's digits in different banks): counts, then running offsets
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(osm);
     const Plan& pl = p.pl;
-    const int u = blockIdx.x, tid = threadIdx.x;
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* status = ws_status(p);
+    SSA_MARK(30);
     grid_dep_wait();   // the lists may come from the previous kernel
-    int64_t n = p.count_in[u];
-    n = n < 0 ? 0 : (n > p.cap ? p.cap : n);
+    SSA_MARK(31);
+    int64_t n64 = p.count_in[u];
+    n64 = n64 < 0 ? 0 : (n64 > p.cap ? p.cap : n64);
     const int64_t room = min((int64_t)kOrderCap, pl.np);
-    if (n > room) {
+    if (n64 > room) {
         if (tid == 0) flag(status, DEV_OVERFLOW);
-        n = room;
+        n64 = room;
     }
-    int n2 = 2;
-    while (n2 < n) n2 <<= 1;
+    const int n = (int)n64;
     const int32_t* idx = p.idx_in + (int64_t)u * p.cap;
     const float* pin = p.p_in + (int64_t)u * p.cap;
     const float* srow = p.s_src + (int64_t)u * pl.N;
-    for (int i = tid; i < n2; i += kOrderThreads) {
+    // the element arrays: in shared memory when the list fits, else in the workspace (generic pointers)
+    uint2* bufA;
+    uint2* bufB;
+    if (n <= kOrderSmemRows) {
+        bufA = reinterpret_cast<uint2*>(osm + kOrderCounters + kOrderWarps * 4);
+        bufB = bufA + kOrderSmemRows;
+    } else {
+        bufA = ws_es_sort(p) + (size_t)u * 2 * pl.esr;
+        bufB = bufA + pl.esr;
+    }
+    for (int i = tid; i < n; i += kOrderThreads) {
         uint32_t k = 0xffffffffu;
-        if (i < n) {
-            const int32_t j = idx[i];
-            if (j >= 0 && (int64_t)j < pl.N) k = ~okey(srow[j]);
-            else flag(status, DEV_BAD_INDEX);
-        }
-        key[i] = k;
-        pos[i] = (uint16_t)(i < n ? i : 0xffff);
+        const int32_t j = idx[i];
+        if (j >= 0 && (int64_t)j < pl.N) k = ~okey(srow[j]);
+        else flag(status, DEV_BAD_INDEX);
+        bufA[i] = make_uint2(k, (uint32_t)i);
     }
     __syncthreads();
-    // ascending (key, position): descending score, then list position
+    SSA_MARK(32);
+    const int per = (n + kOrderWarps - 1) / kOrderWarps;   // elements of each warp's run
+    const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
 #pragma unroll 1
-    for (int k = 2; k <= n2; k <<= 1) {
+    for (int shift = 0; shift < 32; shift += 8) {
+        for (int i = tid; i < 256 * kOrderWarps; i += kOrderThreads) cnt[i] = 0u;
+        __syncthreads();
+        // this warp's count of each digit
 #pragma unroll 1
-        for (int j = k >> 1; j > 0; j >>= 1) {
-#pragma unroll 1
-            for (int i = tid; i < n2; i += kOrderThreads) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const uint32_t ka = key[i], kb = key[l];
-                    const uint16_t pa = pos[i], pb = pos[l];
-                    const bool gt = ka > kb || (ka == kb && pa > pb);
-                    if (gt == ((i & k) == 0)) {
-                        key[i] = kb;
-                        key[l] = ka;
-                        pos[i] = pb;
-                        pos[l] = pa;
-                    }
-                }
-            }
-            __syncthreads();
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            const bool ok = i < w1;
+            const uint32_t d = ok ? (bufA[i].x >> shift) & 0xffu : 0u;
+            const uint32_t peers = digit_peers(d, ok);
+            if (ok && lane == __ffs(peers) - 1) cnt[warp * 256 + d] += (uint32_t)__popc(peers);
         }
+        __syncthreads();
+        // exclusive scan over (digit, warp) in that order: thread t holds entries [8t, 8t + 8), entry
+        // d * warps + w stored at cnt[w * 256 + d]
+        {
+            constexpr int E = 256 * kOrderWarps / kOrderThreads;
+            uint32_t v[E], local = 0;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int x = tid * E + e;
+                v[e] = cnt[(x % kOrderWarps) * 256 + x / kOrderWarps];
+                local += v[e];
+            }
+            uint32_t total;
+            uint32_t run = block_excl_scan<kOrderThreads>(local, reinterpret_cast<uint32_t*>(osm + kOrderCounters),
+                                                          total);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int x = tid * E + e;
+                cnt[(x % kOrderWarps) * 256 + x / kOrderWarps] = run;
+                run += v[e];
+            }
+        }
+        __syncthreads();
+        // the stable scatter: this warp's elements in order, each after the earlier equal digits
+#pragma unroll 1
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            const bool ok = i < w1;
+            const uint2 e = ok ? bufA[i] : make_uint2(0u, 0u);
+            const uint32_t d = ok ? (e.x >> shift) & 0xffu : 0u;
+            const uint32_t peers = digit_peers(d, ok);
+            const uint32_t rank = (uint32_t)__popc(peers & lanemask_lt());
+            uint32_t base = 0;
+            if (ok) base = cnt[warp * 256 + d];
+            __syncwarp();
+            if (ok) {
+                bufB[base + rank] = e;
+                if (lane == __ffs(peers) - 1) cnt[warp * 256 + d] = base + (uint32_t)__popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        uint2* t = bufA;
+        bufA = bufB;
+        bufB = t;
+        SSA_MARK(33 + shift / 8);
     }
-    // the ordered list, one array at a time through the key buffer
+    // the ordered list: every read of the input rows, then the writes (the input may be those rows)
     int32_t* oidx = ws_sel_idx(p) + (size_t)u * pl.np;
     float* op = ws_sel_p(p) + (size_t)u * pl.np;
-    for (int i = tid; i < n; i += kOrderThreads) key[i] = (uint32_t)idx[pos[i]];
+    for (int i = tid; i < n; i += kOrderThreads) {
+        const uint32_t ps = bufA[i].y;
+        bufB[i] = make_uint2((uint32_t)idx[ps], __float_as_uint(pin[ps]));
+    }
     __syncthreads();
-    for (int i = tid; i < n; i += kOrderThreads) oidx[i] = (int32_t)key[i];
-    __syncthreads();
-    for (int i = tid; i < n; i += kOrderThreads) key[i] = __float_as_uint(pin[pos[i]]);
-    __syncthreads();
-    for (int i = tid; i < n; i += kOrderThreads) op[i] = __uint_as_float(key[i]);
-    if (tid == 0) ws_es_count(p)[u] = (int32_t)n;
+    for (int i = tid; i < n; i += kOrderThreads) {
+        const uint2 v = bufB[i];
+        oidx[i] = (int32_t)v.x;
+        op[i] = __uint_as_float(v.y);
+    }
+    if (tid == 0) ws_es_count(p)[u] = n;
+    SSA_MARK(37);
     grid_dep_launch();
 }
 

@@ -117,6 +117,7 @@ __device__ __forceinline__ float* ws_sel_p(const Params& p) { return reinterpret
 __device__ __forceinline__ uint16_t* ws_ubuf(const Params& p) { return reinterpret_cast<uint16_t*>(p.ws + p.pl.o_ubuf); }
 __device__ __forceinline__ int32_t* ws_es_count(const Params& p) { return reinterpret_cast<int32_t*>(p.ws + p.pl.o_es); }
 __device__ __forceinline__ float* ws_es_part(const Params& p) { return reinterpret_cast<float*>(p.ws + p.pl.o_esp); }
+__device__ __forceinline__ uint2* ws_es_sort(const Params& p) { return reinterpret_cast<uint2*>(p.ws + p.pl.o_ess); }
 
 // Strata 1 (top-k + uniform): the remainder's size n - min(k, n) in fp32,
 // the normaliser Z of p = min(1, B / Z) for a unit of n tokens.

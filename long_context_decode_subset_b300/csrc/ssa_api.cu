@@ -118,6 +118,9 @@ ssa::Plan make_plan(const ssa_shape& s, int tiles, int fit = 1)
     // arrays, for the largest tiling: the layout does not depend on the plan)
     pl.esb = (int32_t)((std::min<int64_t>(kEsMaxRows, npmax) + 127) / 128);
     pl.o_esp = take((size_t)U * pl.esb * (size_t)(G * D + 2 * G) * 4);
+    // early stop: the order kernel's two arrays of (key, position) per unit
+    pl.esr = (int32_t)std::min<int64_t>(kEsMaxRows, npmax);
+    pl.o_ess = take((size_t)U * 2 * pl.esr * 8);
     pl.total = o;
     return pl;
 }
