@@ -86,3 +86,33 @@ def test_needles_are_planted_where_promised():
     assert pos == [int((j + 0.5) * 4096 / 8) for j in range(8)]
     tiny = workloads.generate(workloads.CONFIGS["tiny"], 0)["needles"][0, 0]
     assert int(tiny.min()) >= 4   # after the sinks
+
+
+def test_to_paged_places_every_token_in_its_page():
+    """The paged layout helper: token t of sequence b is slot t % page_size of page block_table[b][t // page_size]
+    in every pool, each pool page belongs to at most one sequence, and the block-table entries past a
+    sequence's pages hold an id outside the pool."""
+    import torch
+    import workloads
+    g = torch.Generator().manual_seed(0)
+    Bt, Hkv, N, d, ds = 3, 2, 300, 16, 8
+    K = torch.randn((Bt, Hkv, N, d), generator=g).to(torch.bfloat16)
+    V = torch.randn((Bt, Hkv, N, d), generator=g).to(torch.bfloat16)
+    Ks = torch.randn((Bt, Hkv, N, ds), generator=g).to(torch.bfloat16)
+    lens = [N, 37, 0]
+    for ps in (16, 64, 512):
+        pg = workloads.to_paged(K, V, Ks, lens, ps, seed=1)
+        bt = pg["block_table"]
+        num_pages = pg["K_pool"].shape[0]
+        used = []
+        for b, n in enumerate(lens):
+            need = (n + ps - 1) // ps
+            for t in range(n):
+                page, slot = int(bt[b, t // ps]), t % ps
+                assert torch.equal(pg["K_pool"][page, :, slot], K[b, :, t])
+                assert torch.equal(pg["V_pool"][page, :, slot], V[b, :, t])
+                assert torch.equal(pg["Ks_pool"][page, :, slot], Ks[b, :, t])
+            used += [int(x) for x in bt[b, :need]]
+            assert all(int(x) >= num_pages for x in bt[b, need:])
+        assert len(used) == len(set(used)) and all(0 <= x < num_pages for x in used)
+        assert pg["seq_lens"].tolist() == lens
