@@ -8,15 +8,17 @@ ssa_decode call (four kernels: initialise, score, threshold bucket, attend);
 the seed changes every step.  L2 is flushed (a 256 MiB write) before every
 timed step and each step is timed alone with CUDA events on its stream.
 
-Prints one JSON line (rank 0): value (us per step), roofline (the score
+Prints one JSON line (rank 0): value (us per step), graph (the median of
+graph-replayed steps, one step per CUDA graph), roofline (the score
 pass alone against the measured copy bandwidth, with the DRAM traffic
 recorded for these kernel sources), e2e (through ssa_decode_host, host
 memory in and out), append_step (ssa_decode_append, the serving form),
 secondary (the 1M-context workload), configs (the 32K workload and the 27B
-sweep points: us per step, achieved GB/s and roofline fraction each),
-host_tier (the 32K step with K/V in pinned host memory), cpu_baseline (the
-oracle on the host cores) and cpu_dense (dense attention on the same
-cores).  --impl reference
+sweep points: us per step, graph-replayed median, achieved GB/s and roofline
+fraction each, and the oracle on a bounded sample of units, on every host
+thread and on one), host_tier (the 32K step with K/V in pinned host memory),
+cpu_baseline (the oracle on the host cores, with a single-thread figure) and
+cpu_dense (dense attention on the same cores).  --impl reference
 times the CPU oracle instead (the reference arm for this method has no
 runnable upstream code).
 """
@@ -268,6 +270,78 @@ def time_oracle(h, cfg, seconds: float, max_steps: int | None = None):
     return times, oracle.num_threads()
 
 
+def cpu_threads() -> int:
+    """Host threads the oracle runs on (OpenMP's default: every core of this host)."""
+    import oracle
+    return oracle.num_threads()
+
+
+def oracle_sample(w, cfg, cores: int):
+    """The oracle on a bounded sample of workload `cfg`: calls over the first batch rows that hold at least
+    `cores` units (every host thread busy), and calls over one unit on one thread, each scaled to the whole
+    step by its unit count.  Returns the per-config "oracle" record."""
+    import oracle
+
+    Hkv, G = cfg.n_kv_heads, cfg.group
+    nb = min(cfg.batch, -(-min(cfg.units, cores) // Hkv))
+
+    def host(nbatch, nheads):
+        K = u16(w["K"][:nbatch, :nheads])
+        sel = w["sel_ch"][:nheads].cpu().numpy()
+        return dict(q=u16(w["q"][:nbatch, :nheads * G]), K=K, V=u16(w["V"][:nbatch, :nheads]),
+                    Ks=oracle.pack_summary(K, sel, cfg.d_sel), sel=sel)
+
+    h = host(nb, Hkv)
+    t_all, threads = time_oracle(h, cfg, 0.0, max_steps=2)
+    del h
+    h1 = host(1, 1)
+    oracle.set_threads(1)
+    try:
+        t_one, _ = time_oracle(h1, cfg, 0.0, max_steps=2)
+    finally:
+        oracle.set_threads(threads)
+    return {"us_per_step": round(statistics.fmean(t_all) * cfg.units / (nb * Hkv) * 1e6, 1), "threads": threads,
+            "single_thread_us_per_step": round(statistics.fmean(t_one) * cfg.units * 1e6, 1),
+            "sample": f"2 calls over {nb * Hkv} units ({nb} batch rows, {threads} threads) and 2 calls over one unit "
+                      f"(1 thread), each scaled by the step's {cfg.units} units"}
+
+
+def graph_replay_us(decode, replays: int, flush, seeds: int = 4):
+    """Median and mean us of `replays` replays of CUDA graphs that each hold one decode step (`seeds` graphs,
+    seeds 0.. in turn), L2 flushed before every replay.  decode(seed) enqueues one step on the current stream."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # eager warm-up on a side stream, as capture wants
+        for sd in range(seeds):
+            decode(sd)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = []
+    for sd in range(seeds):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            decode(sd)
+        graphs.append(g)
+    stream = torch.cuda.current_stream()
+    for i in range(2 * seeds):
+        flush.fill_(i & 0xff)
+        graphs[i % seeds].replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    torch.cuda._sleep(20_000_000)
+    for i in range(replays):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        graphs[i % seeds].replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    del graphs
+    return statistics.median(times), statistics.fmean(times)
+
+
 def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
     import torch
 
@@ -313,6 +387,13 @@ def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
         raise RuntimeError(f"device status {st} flags {flags:#x}")
     rows = counts.sum(dim=1).double().mean().item()
     res = dict(times_us=times_us, rows=rows, clocks=clk.summary(), w=w, Ks=Ks)
+    res["graph_replays"] = max(100, min(steps, 1000))
+    res["graph_us"] = graph_replay_us(
+        lambda sd: ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, sd, cfg.scale, out=out, lse=lse, ws=ws),
+        res["graph_replays"], flush)
+    st, flags = ssa.ssa_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
 
     # the dominant kernel alone: ssa_score launches the score kernel (TMA + tcgen05) after the
     # one-launch initialiser that zeroes its stage queue
@@ -381,9 +462,10 @@ def measure_ours(cfg, steps: int, warmup: int, dev, with_e2e: bool = True):
     return res
 
 
-def time_steps(cfg, steps: int, warmup: int, dev, host_kv: bool = False):
-    """Mean us per ssa_decode step of workload `cfg` (L2 flushed before every step, seed = step index) and
-    the mean rows selected; with host_kv the K and V rows sit in pinned host memory."""
+def time_steps(cfg, steps: int, warmup: int, dev, host_kv: bool = False, cores: int = 0):
+    """Mean us per ssa_decode step of workload `cfg` (L2 flushed before every step, seed = step index), the
+    mean rows selected, the clocks, and extras: the median of graph-replayed steps and, with cores > 0, the
+    oracle on a bounded sample.  With host_kv the K and V rows sit in pinned host memory."""
     import torch
 
     import long_context_decode_subset_b300 as ssa
@@ -422,7 +504,20 @@ def time_steps(cfg, steps: int, warmup: int, dev, host_kv: bool = False):
         raise RuntimeError(f"device status {st} flags {flags:#x}")
     us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
     rows = counts.sum(dim=1).double().mean().item()
-    return us, rows, clk.summary()
+    extra = {}
+    if not host_kv:
+        med, mean = graph_replay_us(
+            lambda sd: ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, sd, cfg.scale, out=out, lse=lse,
+                                      ws=ws), 100, flush)
+        extra["graph"] = {"median_us": round(med, 3), "mean_us": round(mean, 3), "replays": 100}
+        st, flags = ssa.ssa_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags:#x}")
+    if cores > 0:
+        del flush, ws
+        torch.cuda.empty_cache()
+        extra["oracle"] = oracle_sample(w, cfg, cores)
+    return us, rows, clk.summary(), extra
 
 
 def time_paged(cfg, steps: int, warmup: int, dev, page_size: int, lens):
@@ -468,7 +563,20 @@ def time_paged(cfg, steps: int, warmup: int, dev, page_size: int, lens):
         raise RuntimeError(f"device status {st} flags {flags:#x}")
     us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
     rows = counts.sum(dim=1).double().mean().item()
-    return us, rows, clk.summary()
+    extra = {}
+    if not host_kv:
+        med, mean = graph_replay_us(
+            lambda sd: ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, sd, cfg.scale, out=out, lse=lse,
+                                      ws=ws), 100, flush)
+        extra["graph"] = {"median_us": round(med, 3), "mean_us": round(mean, 3), "replays": 100}
+        st, flags = ssa.ssa_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags:#x}")
+    if cores > 0:
+        del flush, ws
+        torch.cuda.empty_cache()
+        extra["oracle"] = oracle_sample(w, cfg, cores)
+    return us, rows, clk.summary(), extra
 
 
 def time_early_stop(cfg, steps: int, warmup: int, dev, tau: float):
@@ -577,6 +685,10 @@ def run_ours(args):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "us_per_step_median": round(statistics.median(m["times_us"]), 3),
+        "graph": {"median_us": round(m["graph_us"][0], 3), "mean_us": round(m["graph_us"][1], 3),
+                  "replays": m["graph_replays"],
+                  "note": "one ssa_decode step per CUDA graph (4 graphs, seeds 0..3 in turn), L2 flushed before "
+                          "every replay"},
         "us_per_step_p10_p90": [round(sorted(m["times_us"])[len(m["times_us"]) // 10], 3),
                                 round(sorted(m["times_us"])[(9 * len(m["times_us"])) // 10], 3)],
         "rows_selected_per_step": round(m["rows"], 1),
@@ -612,6 +724,11 @@ def run_ours(args):
         steps2 = max(20, min(args.steps, 300))
         m2 = measure_ours(cfg2, steps2, max(3, min(args.warmup, 10)), dev, with_e2e=False)
         us2 = statistics.fmean(m2["times_us"])
+        oracle2 = None
+        if not args.no_cpu_baseline:
+            m2["Ks"] = None
+            torch.cuda.empty_cache()
+            oracle2 = oracle_sample(m2["w"], cfg2, cpu_threads())
         ab2 = algorithmic_bytes(cfg2, m2["rows"])
         line["secondary"] = {
             "workload": cfg2.name, "value": round(us2, 3), "unit": UNIT, "steps": steps2,
@@ -619,7 +736,11 @@ def run_ours(args):
             "frac": round(ab2 / (us2 * 1e-6) / 1e9 / peak, 4),
             "frac_of_8000": round(ab2 / (us2 * 1e-6) / 1e9 / 8000.0, 4),
             "traffic": traffic_for(cfg2.name), "clocks": m2["clocks"],
+            "graph": {"median_us": round(m2["graph_us"][0], 3), "mean_us": round(m2["graph_us"][1], 3),
+                      "replays": m2["graph_replays"]},
         }
+        if oracle2 is not None:
+            line["secondary"]["oracle"] = oracle2
         del m2
         torch.cuda.empty_cache()
         m = None
@@ -629,9 +750,11 @@ def run_ours(args):
         for name in [x for x in args.sweep.split(",") if x]:
             cfgx = workloads.CONFIGS[name]
             steps_x = max(20, min(args.steps, 200))
-            us, rows, clk = time_steps(cfgx, steps_x, max(3, min(args.warmup, 10)), dev)
+            us, rows, clk, extra = time_steps(cfgx, steps_x, max(3, min(args.warmup, 10)), dev,
+                                              cores=0 if args.no_cpu_baseline else cpu_threads())
             rec = config_record(cfgx, us, rows, peak, clk)
             rec["steps"] = steps_x
+            rec.update(extra)
             line["configs"].append(rec)
             torch.cuda.empty_cache()
     if rank == 0 and args.host_tier:
@@ -639,7 +762,7 @@ def run_ours(args):
         # the host link
         cfgh = workloads.CONFIGS[args.host_tier]
         steps_h = max(20, min(args.steps, 100))
-        us, rows, clk = time_steps(cfgh, steps_h, 3, dev, host_kv=True)
+        us, rows, clk, _ = time_steps(cfgh, steps_h, 3, dev, host_kv=True)
         rec = config_record(cfgh, us, rows, peak, clk)
         rec.update(steps=steps_h, kv="pinned host memory (mapped), summary in HBM",
                    row_bytes_per_step=int(rows * cfgh.head_dim * 2 * 2),
@@ -678,11 +801,15 @@ def run_ours(args):
         # the oracle as it stands, on this host's cores, on a bounded sample of the same workload
         w = workloads.generate(cfg, 0, dev)
         h = oracle_host_inputs(w, cfg)
+        one = oracle_sample(w, cfg, cpu_threads())
         del w
         times, cores = time_oracle(h, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": round(statistics.fmean(times) * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full decode steps of {cfg.name} (all {cfg.units} units), seeds 0..{len(times) - 1}",
+            "single_thread": {"value": one["single_thread_us_per_step"], "unit": UNIT, "cores": 1,
+                              "sample": "2 calls over one unit on one thread, scaled by the step's "
+                                        f"{cfg.units} units"},
         }
         # and dense attention over every cached token on the same cores, for context
         import oracle

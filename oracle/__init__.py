@@ -79,6 +79,8 @@ def _load():
             lib.oracle_dense_attention.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -96,6 +98,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> int:
+    """Host threads for later calls (timing runs use 1 for the single-thread figure); returns the count."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def orderkey(x: float) -> int:

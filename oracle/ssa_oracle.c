@@ -599,3 +599,16 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Sets the number of host threads later calls use (n >= 1); returns the count now in force. */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}

@@ -83,3 +83,39 @@ def test_times_are_the_maximum_over_ranks():
         assert rep == {"step_us": 50.0, "e2e_us": 50.0, "aggregate_steps_per_s": 2 * 1e6 / 50.0,
                        "aggregate_e2e_steps_per_s": 2 * 1e6 / 50.0}
     assert bench.max_over_ranks([3.0, 4.0], "cpu") == [3.0, 4.0]   # no process group: unchanged
+
+
+def test_oracle_result_does_not_depend_on_its_thread_count():
+    """The single-thread timing runs the same computation: one host thread gives the all-threads result bit for
+    bit (units are independent; no sum crosses units)."""
+    import numpy as np
+    import oracle
+    import workloads
+    cfg = workloads.make_config("ministral8b_32k", batch=2, n_q_heads=8, n_kv_heads=2, ctx_len=2048, top_k=30,
+                                budget=30.0)
+    w = workloads.generate(cfg, 3, "cpu")
+    h = bench.oracle_host_inputs(w, cfg)
+    args = (h["q"], h["K"], h["V"], h["Ks"], h["sel"], cfg.top_k, cfg.budget, 3, cfg.scale)
+    many = oracle.decode(*args)
+    n = oracle.num_threads()
+    oracle.set_threads(1)
+    try:
+        assert oracle.num_threads() == 1
+        one = oracle.decode(*args)
+    finally:
+        oracle.set_threads(n)
+    assert oracle.num_threads() == n
+    for k in ("out", "lse", "s_hat", "count", "idx", "p"):
+        assert np.array_equal(many[k], one[k]), k
+
+
+def test_oracle_sample_record():
+    import workloads
+    cfg = workloads.make_config("ministral8b_32k", batch=3, n_q_heads=8, n_kv_heads=2, ctx_len=1024, top_k=20,
+                                budget=20.0)
+    w = workloads.generate(cfg, 0, "cpu")
+    rec = bench.oracle_sample(w, cfg, 4)
+    # four threads' worth of units: two batch rows of two heads, scaled by 6 / 4
+    assert "over 4 units (2 batch rows" in rec["sample"] and "6 units" in rec["sample"]
+    assert rec["us_per_step"] > 0 and rec["single_thread_us_per_step"] > 0
+    assert rec["threads"] == bench.cpu_threads()
