@@ -18,7 +18,8 @@ sweep points: us per step, graph-replayed median, achieved GB/s and roofline
 fraction each, and the oracle on a bounded sample of units, on every host
 thread and on one), host_tier (the 32K step with K/V in pinned host memory),
 cpu_baseline (the oracle on the host cores, with a single-thread figure) and
-cpu_dense (dense attention on the same cores).  --impl reference
+cpu_dense (dense attention on the same cores), and error_vs_dense (relative
+L2 error per head against dense attention, over the workload's seeds).  --impl reference
 times the CPU oracle instead (the reference arm for this method has no
 runnable upstream code).
 """
@@ -54,6 +55,8 @@ def parse_args():
     ap.add_argument("--secondary", default="ministral8b_1m", help="second workload reported beside ('' = none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-error-stats", dest="error_stats", action="store_false",
+                    help="skip the error-against-dense record of the main workload")
     ap.add_argument("--sweep", default="ministral8b_32k,27b_128k_10x,27b_128k_20x,27b_128k_50x,27b_128k_100x,"
                     "27b_128k_dense", help="further workloads timed for the per-config records ('' = none)")
     ap.add_argument("--host-tier", default="ministral8b_32k",
@@ -304,6 +307,45 @@ def oracle_sample(w, cfg, cores: int):
             "single_thread_us_per_step": round(statistics.fmean(t_one) * cfg.units * 1e6, 1),
             "sample": f"2 calls over {nb * Hkv} units ({nb} batch rows, {threads} threads) and 2 calls over one unit "
                       f"(1 thread), each scaled by the step's {cfg.units} units"}
+
+
+def error_vs_dense(cfg, dev):
+    """Relative L2 error per query head of the step's output against dense attention (the library's dense
+    limit, B = +inf), mean / p50 / p99 over heads and the workload's seeds, for SSA and, at the same total
+    budget k + B, for pure top-k and the top-k + uniform hybrid."""
+    import numpy as np
+    import torch
+
+    import long_context_decode_subset_b300 as ssa
+    import workloads
+
+    k, B = cfg.top_k, cfg.budget
+    errs = {"ssa": [], "topk_same_budget": [], "uniform_hybrid_same_budget": []}
+
+    def rel(out, ref):
+        num = torch.linalg.vector_norm(out - ref, dim=-1)
+        return (num / torch.linalg.vector_norm(ref, dim=-1).clamp_min(1e-30)).flatten().cpu().numpy()
+
+    for seed in cfg.seeds:
+        w = workloads.generate(cfg, seed, dev)
+        q, K, V, sel = w["q"], w["K"], w["V"], w["sel_ch"]
+        Ks = ssa.ssa_pack_summary(K, sel)
+        dense, _ = ssa.ssa_decode(q, K, V, Ks, sel, k, math.inf, seed, cfg.scale)
+        errs["ssa"].append(rel(ssa.ssa_decode(q, K, V, Ks, sel, k, B, seed, cfg.scale)[0], dense))
+        errs["topk_same_budget"].append(rel(ssa.ssa_decode(q, K, V, Ks, sel, k + int(B), 0.0, seed, cfg.scale)[0],
+                                            dense))
+        errs["uniform_hybrid_same_budget"].append(
+            rel(ssa.ssa_decode_strata(q, K, V, Ks, sel, ssa.STRATA_UNIFORM, k, 0.0, B, seed, cfg.scale)[0], dense))
+        del w, q, K, V, Ks, dense
+        torch.cuda.empty_cache()
+    rec = {}
+    for name, v in errs.items():
+        x = np.concatenate(v)
+        rec[name] = {"mean": round(float(np.mean(x)), 5), "p50": round(float(np.percentile(x, 50)), 5),
+                     "p99": round(float(np.percentile(x, 99)), 5)}
+    rec.update(workload=cfg.name, seeds=list(cfg.seeds), heads_per_seed=cfg.batch * cfg.n_q_heads,
+               reference="dense attention over every token (the library's B = +inf limit, pinned to the oracle)")
+    return rec
 
 
 def graph_replay_us(decode, replays: int, flush, seeds: int = 4):
@@ -563,20 +605,7 @@ def time_paged(cfg, steps: int, warmup: int, dev, page_size: int, lens):
         raise RuntimeError(f"device status {st} flags {flags:#x}")
     us = statistics.fmean(a.elapsed_time(b) * 1e3 for a, b in ev)
     rows = counts.sum(dim=1).double().mean().item()
-    extra = {}
-    if not host_kv:
-        med, mean = graph_replay_us(
-            lambda sd: ssa.ssa_decode(q, K, V, Ks, sel, cfg.top_k, cfg.budget, sd, cfg.scale, out=out, lse=lse,
-                                      ws=ws), 100, flush)
-        extra["graph"] = {"median_us": round(med, 3), "mean_us": round(mean, 3), "replays": 100}
-        st, flags = ssa.ssa_get_device_status(ws)
-        if st != 0:
-            raise RuntimeError(f"device status {st} flags {flags:#x}")
-    if cores > 0:
-        del flush, ws
-        torch.cuda.empty_cache()
-        extra["oracle"] = oracle_sample(w, cfg, cores)
-    return us, rows, clk.summary(), extra
+    return us, rows, clk.summary()
 
 
 def time_early_stop(cfg, steps: int, warmup: int, dev, tau: float):
@@ -744,6 +773,9 @@ def run_ours(args):
         del m2
         torch.cuda.empty_cache()
         m = None
+    if rank == 0 and args.error_stats:
+        line["error_vs_dense"] = error_vs_dense(cfg, dev)
+        torch.cuda.empty_cache()
     if rank == 0 and args.sweep:
         # the other workloads' steps (the per-config records of the measurement plan)
         line["configs"] = []
