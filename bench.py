@@ -295,18 +295,18 @@ def oracle_sample(w, cfg, cores: int):
                     Ks=oracle.pack_summary(K, sel, cfg.d_sel), sel=sel)
 
     h = host(nb, Hkv)
-    t_all, threads = time_oracle(h, cfg, 0.0, max_steps=2)
+    t_all, threads = time_oracle(h, cfg, 0.0, max_steps=3)
     del h
     h1 = host(1, 1)
     oracle.set_threads(1)
     try:
-        t_one, _ = time_oracle(h1, cfg, 0.0, max_steps=2)
+        t_one, _ = time_oracle(h1, cfg, 0.0, max_steps=3)
     finally:
         oracle.set_threads(threads)
-    return {"us_per_step": round(statistics.fmean(t_all) * cfg.units / (nb * Hkv) * 1e6, 1), "threads": threads,
-            "single_thread_us_per_step": round(statistics.fmean(t_one) * cfg.units * 1e6, 1),
-            "sample": f"2 calls over {nb * Hkv} units ({nb} batch rows, {threads} threads) and 2 calls over one unit "
-                      f"(1 thread), each scaled by the step's {cfg.units} units"}
+    return {"us_per_step": round(statistics.median(t_all) * cfg.units / (nb * Hkv) * 1e6, 1), "threads": threads,
+            "single_thread_us_per_step": round(statistics.median(t_one) * cfg.units * 1e6, 1),
+            "sample": f"median of 3 calls over {nb * Hkv} units ({nb} batch rows, {threads} threads) and of 3 calls "
+                      f"over one unit (1 thread), each scaled by the step's {cfg.units} units"}
 
 
 def error_vs_dense(cfg, dev):
@@ -840,7 +840,7 @@ def run_ours(args):
             "value": round(statistics.fmean(times) * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full decode steps of {cfg.name} (all {cfg.units} units), seeds 0..{len(times) - 1}",
             "single_thread": {"value": one["single_thread_us_per_step"], "unit": UNIT, "cores": 1,
-                              "sample": "2 calls over one unit on one thread, scaled by the step's "
+                              "sample": "median of 3 calls over one unit on one thread, scaled by the step's "
                                         f"{cfg.units} units"},
         }
         # and dense attention over every cached token on the same cores, for context
