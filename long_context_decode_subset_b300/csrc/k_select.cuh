@@ -829,35 +829,45 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, int6
             } else {
                 sv[0] = sv[1] = sv[2] = sv[3] = 0.0f;
             }
+            // the four tokens are classified without branches (their chains
+            // interleave); the rare candidates are written after the loop
             uint32_t kbits = 0;
             float val[4];
+            uint32_t kq[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int i = i0 + q;
-                const bool valid = i < nvalid;
+                const bool valid = i0 + q < nvalid;
                 const uint32_t k = okey(sv[q]);
                 const uint32_t b1 = k >> 20;
                 const bool above = valid && b1 > f1.bin;
                 const bool is_cand = valid && b1 == f1.bin;
-                bool keep = above || is_cand;
-                val[q] = above ? INFINITY : sv[q];
-                if (sampling && valid && b1 < f1.bin) {
-                    const float e = uniform ? 1.0f : expf(__fsub_rn(sv[q], m));
-                    if (!uniform) zacc(zh4[q], zl4[q], e);
-                    keep = __fmul_ru(e, bound16) > __uint2float_rn(pr[q]);
-                    val[q] = e;
-                }
-                if (keep) kbits |= 1u << q;
-                if (is_cand) {
-                    const uint32_t t = t0 + (uint32_t)i;
-                    cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(k, t);
-                    atomicAdd(hist2 + ((k >> 8) & 0xfffu), 1u);
-                    kbits |= 0x10u << q;   // a candidate: flagged in the list
+                const bool below = sampling && valid && b1 < f1.bin;
+                const float e = uniform ? 1.0f : expf(__fsub_rn(sv[q], m));
+                if (!uniform) zacc(zh4[q], zl4[q], below ? e : 0.0f);
+                const bool drawn = below && __fmul_ru(e, bound16) > __uint2float_rn(pr[q]);
+                val[q] = above ? INFINITY : (below ? e : sv[q]);
+                kbits |= ((uint32_t)(above || is_cand || drawn) << q) | ((uint32_t)is_cand << (4 + q));
+                kq[q] = k;
+            }
+            if (kbits & 0xf0u) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (kbits & (0x10u << q)) {   // a candidate: flagged in the list
+                        cseg[atomicAdd(&sh.ncand_cta, 1u)] = make_uint2(kq[q], t0 + (uint32_t)(i0 + q));
+                        atomicAdd(hist2 + ((kq[q] >> 8) & 0xfffu), 1u);
+                    }
                 }
             }
-            const uint32_t nk = __popc(kbits & 0xfu);
-            const uint32_t incl = warp_incl_scan(nk);
-            uint32_t o = cnt + incl - nk;
+            // the lane's first list slot: the warp's count so far plus the kept
+            // tokens of the lower lanes, from one ballot per token position
+            const uint32_t lt = lanemask_lt();
+            uint32_t o = cnt, nkw = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t bq = __ballot_sync(0xffffffffu, (kbits >> q) & 1u);
+                o += (uint32_t)__popc(bq & lt);
+                nkw += (uint32_t)__popc(bq);
+            }
             if (kbits & 0xfu) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -869,7 +879,7 @@ __device__ __noinline__ TileSel tile_pass(const Params& p, int u, int tile, int6
                     }
                 }
             }
-            cnt += __shfl_sync(0xffffffffu, incl, 31);
+            cnt += nkw;
         }
     }
     SSA_MARK(18);
