@@ -242,7 +242,7 @@ struct UCfg {
     static constexpr uint32_t OFF_RAW = OFF_LIST + (uint32_t)LIST * 8u;       // raw list staging
     static constexpr uint32_t OFF_RED = OFF_RAW + (uint32_t)LIST * 8u;        // [2][2][4][G] floats
     static constexpr uint32_t OFF_BAR = (OFF_RED + 2u * 2u * 4u * G * 4u + 7u) & ~7u;
-    static constexpr uint32_t NBAR = 10;                           // kv_full, kv_free, s_full, p_ready, o_full (x2)
+    static constexpr uint32_t NBAR = 14;                           // k/v_full, k/v_free, s_full, p_ready, o_full (x2)
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;      // tensor-memory slot, counts
     static constexpr uint32_t OFF_PRE = OFF_MISC + 64u;            // the tile list's slice prefix
     static constexpr uint32_t OFF_PCACHE = (OFF_PRE + (uint32_t)(kSelWarps + 1) * 4u + 15u) & ~15u;   // paged
@@ -348,11 +348,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     float* clp = reinterpret_cast<float*>(smem + CF::OFF_LIST + LIST * 4);
     float* red = reinterpret_cast<float*>(smem + CF::OFF_RED);   // [parity][max | sum][warp][G]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
-    uint64_t* kv_full = bars;
-    uint64_t* kv_free = bars + 2;
-    uint64_t* s_full = bars + 4;
-    uint64_t* p_ready = bars + 6;
-    uint64_t* o_full = bars + 8;
+    uint64_t* k_full = bars;
+    uint64_t* v_full = bars + 2;
+    uint64_t* k_free = bars + 4;
+    uint64_t* v_free = bars + 6;
+    uint64_t* s_full = bars + 8;
+    uint64_t* p_ready = bars + 10;
+    uint64_t* o_full = bars + 12;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + CF::OFF_MISC);   // [0] tensor memory, [2] last, [4..5] offsets
     uint32_t* pre = reinterpret_cast<uint32_t*>(smem + CF::OFF_PRE);
 
@@ -365,8 +367,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 32 * kUGatherWarps);   // every gather thread's copies
-            mbar_init(&kv_free[i], 1);
+            mbar_init(&k_full[i], 32 * kUGatherWarps);   // every gather thread's copies
+            mbar_init(&v_full[i], 32 * kUGatherWarps);
+            mbar_init(&k_free[i], 1);
+            mbar_init(&v_free[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_ready[i], 4);   // one arrive per epilogue warp
             mbar_init(&o_full[i], 1);
@@ -498,21 +502,23 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
             // gather: 16-byte pieces of the chunk's K and V rows into the
-            // 128-byte swizzled planes (rows past the list read as zeros)
+            // 128-byte swizzled planes (rows past the list read as zeros).
+            // K and V buffers are released separately: a chunk's K copies go
+            // out once the S product two chunks back has read its buffer,
+            // its V copies once that chunk's O product has.  Each thread's
+            // copies arrive on k_full / v_full when they land
+            // (cp.async.mbarrier.arrive), so publishing never waits on a
+            // later chunk's buffer.
             const int gt = tid - 160;   // 0 .. 32 * kUGatherWarps - 1
             constexpr int PPR = D / 8;  // pieces per row
-            // each thread's copies of chunk c arrive on kv_full when they land
-            // (cp.async.mbarrier.arrive), so publishing never waits on a later
-            // chunk's buffer
 #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int g = gbase + c, bf = g & 1;
+                const uint32_t ph = (uint32_t)((g - 2) >> 1) & 1u;   // the release of chunk g - 2
                 if (g >= 2) {
-                    if (lane == 0 && !mbar_wait_bounded(&kv_free[bf], (uint32_t)((g - 2) >> 1) & 1u)) flag(status, DEV_TIMEOUT);
+                    if (lane == 0 && !mbar_wait_bounded(&k_free[bf], ph)) flag(status, DEV_TIMEOUT);
                     __syncwarp();
                 }
-                unsigned char* kd = smem + CF::OFF_K + bf * CF::KV;
-                unsigned char* vd = smem + CF::OFF_V + bf * CF::KV;
                 int64_t* roff = reinterpret_cast<int64_t*>(smem + CF::OFF_ROFF) + bf * CF::CH;
                 if constexpr (PAGED) {
                     // the chunk's pool rows, once per row (double-buffered: a buffer is rewritten only after
@@ -523,27 +529,33 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     }
                     named_bar_sync(2, 32 * kUGatherWarps);
                 }
+                auto copy_rows = [&](unsigned char* dst, const uint16_t* src) {
 #pragma unroll 1
-                for (int q = gt; q < CF::CH * PPR; q += 32 * kUGatherWarps) {
-                    const int i = q / PPR, pc = q % PPR;
-                    const int row = c * CF::CH + i;
-                    const bool valid = row < nk;
-                    int64_t j;
-                    if constexpr (PAGED) j = roff[i];
-                    else j = valid ? (int64_t)cidx[row] : 0;
-                    const bool load = valid;
-                    const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
-                    cp_async_16_zfill(kd + off, Kb + j * D + pc * 8, load);
-                    cp_async_16_zfill(vd + off, Vb + j * D + pc * 8, load);
+                    for (int q = gt; q < CF::CH * PPR; q += 32 * kUGatherWarps) {
+                        const int i = q / PPR, pc = q % PPR;
+                        const int row = c * CF::CH + i;
+                        const bool valid = row < nk;
+                        int64_t j;
+                        if constexpr (PAGED) j = roff[i];
+                        else j = valid ? (int64_t)cidx[row] : 0;
+                        const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
+                        cp_async_16_zfill(dst + off, src + j * D + pc * 8, valid);
+                    }
+                };
+                copy_rows(smem + CF::OFF_K + bf * CF::KV, Kb);
+                cp_async_mbar_arrive(&k_full[bf]);
+                if (g >= 2) {
+                    if (lane == 0 && !mbar_wait_bounded(&v_free[bf], ph)) flag(status, DEV_TIMEOUT);
+                    __syncwarp();
                 }
-                cp_async_mbar_arrive(&kv_full[bf]);
+                copy_rows(smem + CF::OFF_V + bf * CF::KV, Vb);
+                cp_async_mbar_arrive(&v_full[bf]);
             }
             cp_async_wait<0>();
         } else if (warp == 4) {
             if (lane == 0) {
-                auto mma_s = [&](int g) {   // S[g & 1] = K_g Q^T
+                auto mma_s = [&](int g) {   // S[g & 1] = K_g Q^T; releases K_g's buffer
                     const int bf = g & 1;
-                    if (!mbar_wait_bounded(&kv_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
                     fence_proxy_async_smem();   // the copies (generic proxy) before the MMA's reads
                     tc_fence_after();
 #pragma unroll
@@ -554,17 +566,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                                     CF::IDESC_S, ks > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[bf]);
+                    tc_commit(&k_free[bf]);
                 };
-                // S of chunk g, then (once P_g is written) O of chunk g: the MMA
-                // that frees a K/V buffer never waits on a later chunk's copies
-#pragma unroll 1
-                for (int c = 0; c < nc; ++c) {
-                    const int g = gbase + c, bf = g & 1;
-                    mma_s(g);
-                    if (!mbar_wait_bounded(&p_ready[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
+                auto mma_o = [&](int g) {   // O^T[g & 1] = V_g^T P_g; releases V_g's buffer
+                    const int bf = g & 1;
+                    fence_proxy_async_smem();
                     tc_fence_after();
-                    // O^T[g & 1] = V_g^T P_g: A = the V rows read MN-major (64-dim
-                    // atoms PLANE apart, 8-row groups 1 KB apart), 16 rows a step
+                    // A = the V rows read MN-major (64-dim atoms PLANE apart,
+                    // 8-row groups 1 KB apart), 16 rows a step
 #pragma unroll
                     for (int ks = 0; ks < CF::CH / 16; ++ks) {
                         const uint32_t a = v_a + bf * CF::KV + ks * 2048u;
@@ -573,121 +582,187 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                                     smem_desc_kmajor_swz(bp, 128), CF::IDESC_O, ks > 0 ? 1u : 0u);
                     }
                     tc_commit(&o_full[bf]);
-                    tc_commit(&kv_free[bf]);
+                    tc_commit(&v_free[bf]);
+                };
+                // Whichever product can go out next does: S of chunk cs once
+                // its K rows have landed (at most one chunk ahead of O: two S
+                // buffers), O of chunk co once P is written and its V rows
+                // have landed.  S of chunk g + 1 thus runs while the
+                // epilogue turns S of chunk g into P, and O of chunk g while
+                // it works on chunk g + 1.
+                int cs = 0, co = 0;
+                uint64_t t0 = 0;
+                bool idle = false;
+#pragma unroll 1
+                while (co < nc) {
+                    const int gs = gbase + cs, go = gbase + co;
+                    const bool s_next = cs < nc && cs <= co + 1;
+                    if (s_next && mbar_test_wait(&k_full[gs & 1], (uint32_t)(gs >> 1) & 1u)) {
+                        mma_s(gs);
+                        ++cs;
+                        idle = false;
+                    } else if (co < cs && mbar_test_wait(&p_ready[go & 1], (uint32_t)(go >> 1) & 1u) &&
+                               mbar_test_wait(&v_full[go & 1], (uint32_t)(go >> 1) & 1u)) {
+                        mma_o(go);
+                        ++co;
+                        idle = false;
+                    } else if (!idle) {
+                        t0 = global_timer_ns();
+                        idle = true;
+                    } else if (global_timer_ns() - t0 > 2000000000ull) {
+                        // a wait ran out: record it and go on in order
+                        flag(status, DEV_TIMEOUT);
+                        if (s_next) {
+                            mma_s(gs);
+                            ++cs;
+                        } else {
+                            mma_o(go);
+                            ++co;
+                        }
+                        idle = false;
+                    } else {
+                        __nanosleep(32);
+                    }
                 }
             }
         } else {
-            // epilogue (tid = tensor-memory lane)
+            // epilogue (tid = tensor-memory lane).  Iteration c turns S of
+            // chunk c into P (softmax) and then folds O of chunk c - 1, so
+            // that the O product of a chunk runs while the next chunk's
+            // softmax does; (mc, lc) of the chunk waiting for its fold are
+            // kept in mcP, lcP.
             const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+            float mcP[G], lcP[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                mcP[gg] = -INFINITY;
+                lcP[gg] = 0.0f;
+            }
 #pragma unroll 1
-            for (int c = 0; c < nc; ++c) {
-                const int g = gbase + c, bf = g & 1;
-                if (lane == 0 && !mbar_wait_bounded(&s_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
-                __syncwarp();
-                tc_fence_after();
-                float s[G];
-                {
-                    uint32_t rr[8];
-                    tmem_ld_x8(lane_base + bf * 16u, rr);
-                    tmem_ld_wait();
-                    tmem_regs_ready(rr);
-#pragma unroll
-                    for (int gg = 0; gg < G; ++gg) s[gg] = __uint_as_float(rr[gg]);
-                }
-                const int row = c * CF::CH + tid;
-                const bool valid = row < nk;
-                const float lp = valid ? clp[row] : 0.0f;
-                float x[G], mc[G], lc[G];
+            for (int c = 0; c <= nc; ++c) {
+                float mc[G], lc[G];
 #pragma unroll
                 for (int gg = 0; gg < G; ++gg) {
-                    x[gg] = valid ? s[gg] * p.scale - lp : -INFINITY;
-                    float mx = x[gg];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    if (lane == 0) red[((bf * 2 + 0) * 4 + warp) * G + gg] = mx;
+                    mc[gg] = -INFINITY;
+                    lc[gg] = 0.0f;
                 }
-                named_bar_sync(1, 128);
+                if (c < nc) {
+                    const int g = gbase + c, bf = g & 1;
+                    if (lane == 0 && !mbar_wait_bounded(&s_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
+                    __syncwarp();
+                    tc_fence_after();
+                    float s[G];
+                    {
+                        uint32_t rr[8];
+                        tmem_ld_x8(lane_base + bf * 16u, rr);
+                        tmem_ld_wait();
+                        tmem_regs_ready(rr);
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    float mx = red[((bf * 2 + 0) * 4 + 0) * G + gg];
-#pragma unroll
-                    for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[((bf * 2 + 0) * 4 + w) * G + gg]);
-                    mc[gg] = mx;
-                }
-                // P = exp(x - m_chunk) as bf16 hi + lo, columns gg and G + gg of
-                // the K-major B operand (128-byte swizzle, two 64-row planes)
-                unsigned char* pb = smem + CF::OFF_P + bf * 2u * CF::QPLANE + (tid >> 6) * CF::QPLANE;
-                const int r64 = tid & 63;
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    const float w = (valid && mc[gg] != -INFINITY) ? expf(x[gg] - mc[gg]) : 0.0f;
-                    const __nv_bfloat16 whi = __float2bfloat16_rn(w);
-                    const __nv_bfloat16 wlo = __float2bfloat16_rn(w - __bfloat162float(whi));
-                    const int nh = gg, nl = G + gg;
-                    *reinterpret_cast<__nv_bfloat16*>(pb + nh * 128 + (((r64 >> 3) ^ (nh & 7)) << 4) + (r64 & 7) * 2) = whi;
-                    *reinterpret_cast<__nv_bfloat16*>(pb + nl * 128 + (((r64 >> 3) ^ (nl & 7)) << 4) + (r64 & 7) * 2) = wlo;
-                    float sm = w;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-                    if (lane == 0) red[((bf * 2 + 1) * 4 + warp) * G + gg] = sm;
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(1, 128);
-                if (lane == 0) mbar_arrive(&p_ready[bf]);
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    float sm = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) sm += red[((bf * 2 + 1) * 4 + w) * G + gg];
-                    lc[gg] = sm;
-                }
-                // fold O_g (this thread's head dim, hi + lo columns) into acc
-                if (lane == 0 && !mbar_wait_bounded(&o_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
-                __syncwarp();
-                tc_fence_after();
-                float o[2 * G];
-                if constexpr (G == 8) {
-                    uint32_t rr[16];
-                    tmem_ld_x16(lane_base + 32u + bf * 16u, rr);
-                    tmem_ld_wait();
-                    tmem_regs_ready(rr);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k] = __uint_as_float(rr[k]);
-                } else {
-                    uint32_t rr[8];
-                    tmem_ld_x8(lane_base + 32u + bf * 16u, rr);
-                    tmem_ld_wait();
-                    tmem_regs_ready(rr);
-#pragma unroll
-                    for (int k = 0; k < 2 * G; ++k) o[k] = __uint_as_float(rr[k]);
-                }
-                tc_fence_before();
-                if constexpr (ES) {
-                    // early stop: every block's own (m, l, acc) partial; the merge applies the gain test
-                    constexpr int PS = G * D + 2 * G;
-                    float* bp = ws_es_part(p) + ((size_t)u * pl.esb + (size_t)(es_b0 + g)) * PS;
-                    if (tid < D) {
-#pragma unroll
-                        for (int gg = 0; gg < G; ++gg) bp[gg * D + tid] = o[gg] + o[G + gg];
+                        for (int gg = 0; gg < G; ++gg) s[gg] = __uint_as_float(rr[gg]);
                     }
-                    if (tid == 0) {
-#pragma unroll
-                        for (int gg = 0; gg < G; ++gg) {
-                            bp[G * D + gg] = mc[gg];
-                            bp[G * D + G + gg] = lc[gg];
-                        }
-                    }
-                } else {
+                    const int row = c * CF::CH + tid;
+                    const bool valid = row < nk;
+                    const float lp = valid ? clp[row] : 0.0f;
+                    float x[G];
 #pragma unroll
                     for (int gg = 0; gg < G; ++gg) {
-                        const float mn = fmaxf(m_run[gg], mc[gg]);
-                        const float ar = (m_run[gg] == -INFINITY) ? 0.0f : expf(m_run[gg] - mn);
-                        const float ac = (mc[gg] == -INFINITY) ? 0.0f : expf(mc[gg] - mn);
-                        acc[gg] = acc[gg] * ar + (o[gg] + o[G + gg]) * ac;
-                        l_run[gg] = l_run[gg] * ar + lc[gg] * ac;
-                        m_run[gg] = mn;
+                        x[gg] = valid ? s[gg] * p.scale - lp : -INFINITY;
+                        float mx = x[gg];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        if (lane == 0) red[((bf * 2 + 0) * 4 + warp) * G + gg] = mx;
                     }
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) {
+                        float mx = red[((bf * 2 + 0) * 4 + 0) * G + gg];
+#pragma unroll
+                        for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[((bf * 2 + 0) * 4 + w) * G + gg]);
+                        mc[gg] = mx;
+                    }
+                    // P = exp(x - m_chunk) as bf16 hi + lo, columns gg and G + gg of
+                    // the K-major B operand (128-byte swizzle, two 64-row planes)
+                    unsigned char* pb = smem + CF::OFF_P + bf * 2u * CF::QPLANE + (tid >> 6) * CF::QPLANE;
+                    const int r64 = tid & 63;
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) {
+                        const float w = (valid && mc[gg] != -INFINITY) ? expf(x[gg] - mc[gg]) : 0.0f;
+                        const __nv_bfloat16 whi = __float2bfloat16_rn(w);
+                        const __nv_bfloat16 wlo = __float2bfloat16_rn(w - __bfloat162float(whi));
+                        const int nh = gg, nl = G + gg;
+                        *reinterpret_cast<__nv_bfloat16*>(pb + nh * 128 + (((r64 >> 3) ^ (nh & 7)) << 4) + (r64 & 7) * 2) = whi;
+                        *reinterpret_cast<__nv_bfloat16*>(pb + nl * 128 + (((r64 >> 3) ^ (nl & 7)) << 4) + (r64 & 7) * 2) = wlo;
+                        float sm = w;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+                        if (lane == 0) red[((bf * 2 + 1) * 4 + warp) * G + gg] = sm;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_bar_sync(1, 128);
+                    if (lane == 0) mbar_arrive(&p_ready[bf]);
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) {
+                        float sm = 0.0f;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) sm += red[((bf * 2 + 1) * 4 + w) * G + gg];
+                        lc[gg] = sm;
+                    }
+                }
+                if (c > 0) {
+                    // fold O of chunk c - 1 (this thread's head dim, hi + lo columns) into acc
+                    const int g = gbase + c - 1, bf = g & 1;
+                    if (lane == 0 && !mbar_wait_bounded(&o_full[bf], (uint32_t)(g >> 1) & 1u)) flag(status, DEV_TIMEOUT);
+                    __syncwarp();
+                    tc_fence_after();
+                    float o[2 * G];
+                    if constexpr (G == 8) {
+                        uint32_t rr[16];
+                        tmem_ld_x16(lane_base + 32u + bf * 16u, rr);
+                        tmem_ld_wait();
+                        tmem_regs_ready(rr);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = __uint_as_float(rr[k]);
+                    } else {
+                        uint32_t rr[8];
+                        tmem_ld_x8(lane_base + 32u + bf * 16u, rr);
+                        tmem_ld_wait();
+                        tmem_regs_ready(rr);
+#pragma unroll
+                        for (int k = 0; k < 2 * G; ++k) o[k] = __uint_as_float(rr[k]);
+                    }
+                    tc_fence_before();
+                    if constexpr (ES) {
+                        // early stop: every block's own (m, l, acc) partial; the merge applies the gain test
+                        constexpr int PS = G * D + 2 * G;
+                        float* bp = ws_es_part(p) + ((size_t)u * pl.esb + (size_t)(es_b0 + g)) * PS;
+                        if (tid < D) {
+#pragma unroll
+                            for (int gg = 0; gg < G; ++gg) bp[gg * D + tid] = o[gg] + o[G + gg];
+                        }
+                        if (tid == 0) {
+#pragma unroll
+                            for (int gg = 0; gg < G; ++gg) {
+                                bp[G * D + gg] = mcP[gg];
+                                bp[G * D + G + gg] = lcP[gg];
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int gg = 0; gg < G; ++gg) {
+                            const float mn = fmaxf(m_run[gg], mcP[gg]);
+                            const float ar = (m_run[gg] == -INFINITY) ? 0.0f : expf(m_run[gg] - mn);
+                            const float ac = (mcP[gg] == -INFINITY) ? 0.0f : expf(mcP[gg] - mn);
+                            acc[gg] = acc[gg] * ar + (o[gg] + o[G + gg]) * ac;
+                            l_run[gg] = l_run[gg] * ar + lcP[gg] * ac;
+                            m_run[gg] = mn;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    mcP[gg] = mc[gg];
+                    lcP[gg] = lc[gg];
                 }
             }
         }

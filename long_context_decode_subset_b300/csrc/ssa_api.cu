@@ -655,7 +655,8 @@ ssa_status ssa_score(const ssa_bf16* q, const ssa_bf16* Ks, const int32_t* sel_c
     p.sel_ch = sel_ch;
     p.scale = scale;
     p.s_dst = s_hat;
-    if ((st = launch_init(p, stream)) != SSA_OK) return st;   // zeroes K1's stage queue
+    p.src_mode = 1;   // no selection follows: K0 zeroes K1's stage queue only, no histograms
+    if ((st = launch_init(p, stream)) != SSA_OK) return st;
     return launch_score(p, *shape, false, stream, true);
 }
 
