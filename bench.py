@@ -4,14 +4,16 @@
 Default workload: the Ministral-8B-shaped layer at 128K context (batch 2,
 32 query / 8 KV heads, d = 128, d_sel = 32, 50x sparsity: top-k 1311,
 budget 1310), seeded synthetic inputs resident in HBM.  A step is one
-ssa_decode call (four kernels: initialise, score, threshold bucket, attend);
+ssa_decode call (three kernels: initialise, score, and the unit kernel that
+selects, samples, attends and merges);
 the seed changes every step.  L2 is flushed (a 256 MiB write) before every
 timed step and each step is timed alone with CUDA events on its stream.
 
 Prints one JSON line (rank 0): value (us per step), graph (the median of
 graph-replayed steps, one step per CUDA graph), roofline (the score
 pass alone against the measured copy bandwidth, with the DRAM traffic
-recorded for these kernel sources), e2e (through ssa_decode_host, host
+recorded for these kernel sources and the read ceiling of the same bytes
+timed the same way), e2e (through ssa_decode_host, host
 memory in and out), append_step (ssa_decode_append, the serving form),
 secondary (the 1M-context workload), configs (the 32K workload and the 27B
 sweep points: us per step, graph-replayed median, achieved GB/s and roofline
@@ -239,6 +241,40 @@ def traffic_for(workload: str):
     except Exception:
         pass
     return None
+
+
+def read_ceiling(byte_counts):
+    """The read-only ceiling for each byte count: the same bytes read once by plain loads and by a bulk-copy
+    ring (read_ceiling.cu), each launch timed alone with CUDA events after an L2 flush, as the score pass is.
+    {bytes: (plain_us, ring_us)}, or None if the probe is missing or fails."""
+    import subprocess
+    exe = os.path.join(ROOT, "long_context_decode_subset_b300", "read_ceiling")
+    if not os.path.exists(exe):
+        return None
+    try:
+        res = subprocess.run([exe, *[str(int(b)) for b in byte_counts]], capture_output=True, text=True,
+                             timeout=120)
+        if res.returncode != 0:
+            return None
+        out = {}
+        for ln in res.stdout.splitlines():
+            d = json.loads(ln)
+            out[int(d["bytes"])] = (float(d["plain_loads_us"]), float(d["bulk_ring_us"]))
+        return out
+    except Exception:
+        return None
+
+
+def ceiling_record(ceil, nbytes: float, kernel_us: float):
+    """The score pass placed against the read ceiling of its own bytes (ceil from read_ceiling)."""
+    if not ceil or int(nbytes) not in ceil:
+        return None
+    plain, ring = ceil[int(nbytes)]
+    best = min(plain, ring)
+    return {"plain_loads_us": plain, "bulk_ring_us": ring,
+            "gbs": round(nbytes / (best * 1e-6) / 1e9, 1), "kernel_frac": round(best / kernel_us, 4),
+            "note": "the same bytes read once with nothing else to do (plain loads; a 6 x 32 KB bulk-copy ring), "
+                    "each launch timed alone after an L2 flush: kernel_frac = ceiling time / score-pass time"}
 
 
 def u16(t):
@@ -746,6 +782,13 @@ def run_ours(args):
         "clocks": m["clocks"],
         "wall_s": round(wall, 2),
     }
+    if rank == 0:
+        sizes = [score_bytes]
+        if args.secondary:
+            c2 = workloads.CONFIGS[args.secondary]
+            sizes.append(float(c2.batch * c2.n_kv_heads * c2.ctx_len * c2.d_sel * 2))
+        ceil = read_ceiling(sizes)
+        line["roofline"]["read_ceiling"] = ceiling_record(ceil, score_bytes, score_us)
     if rank == 0 and args.secondary:
         cfg2 = workloads.CONFIGS[args.secondary]
         del m
@@ -765,6 +808,10 @@ def run_ours(args):
             "frac": round(ab2 / (us2 * 1e-6) / 1e9 / peak, 4),
             "frac_of_8000": round(ab2 / (us2 * 1e-6) / 1e9 / 8000.0, 4),
             "traffic": traffic_for(cfg2.name), "clocks": m2["clocks"],
+            "score_pass": {"kernel_us": round(statistics.fmean(m2["score_us"]), 3),
+                           "read_ceiling": ceiling_record(
+                               ceil, float(cfg2.batch * cfg2.n_kv_heads * cfg2.ctx_len * cfg2.d_sel * 2),
+                               statistics.fmean(m2["score_us"]))},
             "graph": {"median_us": round(m2["graph_us"][0], 3), "mean_us": round(m2["graph_us"][1], 3),
                       "replays": m2["graph_replays"]},
         }

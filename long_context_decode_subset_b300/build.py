@@ -29,6 +29,25 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+CEILING_SRC = os.path.join(PKG, "read_ceiling.cu")
+CEILING = os.path.join(PKG, "read_ceiling")
+
+
+def build_ceiling(force: bool = False) -> str:
+    """Builds the read-ceiling probe the benchmark places the score pass against (read_ceiling.cu)."""
+    if not force and os.path.exists(CEILING) and os.path.getmtime(CEILING) >= os.path.getmtime(CEILING_SRC):
+        return CEILING
+    nvcc = os.environ.get("NVCC", "nvcc")
+    tmp = CEILING + f".tmp{os.getpid()}"
+    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", tmp, CEILING_SRC]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        sys.stderr.write(res.stderr[-4000:])
+        raise RuntimeError("nvcc failed on read_ceiling.cu")
+    os.replace(tmp, CEILING)
+    return CEILING
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
@@ -51,4 +70,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose=True)
+    build_ceiling(force="--force" in sys.argv)
     print(LIB)

@@ -119,3 +119,24 @@ def test_oracle_sample_record():
     assert "over 4 units (2 batch rows" in rec["sample"] and "6 units" in rec["sample"]
     assert rec["us_per_step"] > 0 and rec["single_thread_us_per_step"] > 0
     assert rec["threads"] == bench.cpu_threads()
+
+
+def test_read_ceiling_record():
+    """The score pass is placed against the faster of the two read-only probes of its own byte count; a size the
+    probe did not measure, or no probe at all, gives no record."""
+    ceil = {134217728: (30.0, 32.0)}
+    rec = bench.ceiling_record(ceil, 134217728.0, 40.0)
+    assert rec["plain_loads_us"] == 30.0 and rec["bulk_ring_us"] == 32.0
+    assert rec["kernel_frac"] == 0.75
+    assert abs(rec["gbs"] - 134217728 / 30e-6 / 1e9) < 0.1
+    assert bench.ceiling_record(ceil, 1024.0, 40.0) is None
+    assert bench.ceiling_record(None, 134217728.0, 40.0) is None
+
+
+def test_read_ceiling_without_a_gpu_reports_nothing():
+    import pytest
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the probe runs")
+    # the probe either is not built or finds no device: either way no figure, and no exception
+    assert bench.read_ceiling([32768]) is None
