@@ -501,16 +501,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
-            // gather: 16-byte pieces of the chunk's K and V rows into the
-            // 128-byte swizzled planes (rows past the list read as zeros).
-            // K and V buffers are released separately: a chunk's K copies go
-            // out once the S product two chunks back has read its buffer,
-            // its V copies once that chunk's O product has.  Each thread's
-            // copies arrive on k_full / v_full when they land
-            // (cp.async.mbarrier.arrive), so publishing never waits on a
-            // later chunk's buffer.
+            // gather: the chunk's K rows, then its V rows, into the 128-byte
+            // swizzled planes (rows past the list read as zeros).  An item is
+            // one row and one 16-byte piece of each of its 64-dim planes:
+            // eight consecutive threads cover a row's 128-byte plane
+            // segments, and one address computation serves both planes.  K
+            // and V buffers are released separately: a chunk's K copies go
+            // out once S of the chunk two back has read its buffer, its V
+            // copies once that chunk's O has.  Each thread's copies arrive on
+            // k_full / v_full when they land (cp.async.mbarrier.arrive), so
+            // publishing never waits on a later chunk's buffer.
             const int gt = tid - 160;   // 0 .. 32 * kUGatherWarps - 1
-            constexpr int PPR = D / 8;  // pieces per row
 #pragma unroll 1
             for (int c = 0; c < nc; ++c) {
                 const int g = gbase + c, bf = g & 1;
@@ -531,19 +532,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                 }
                 auto copy_rows = [&](unsigned char* dst, const uint16_t* src) {
 #pragma unroll 1
-                    for (int q = gt; q < CF::CH * PPR; q += 32 * kUGatherWarps) {
-                        const int i = q / PPR, pc = q % PPR;
+                    for (int it = gt; it < CF::CH * 8; it += 32 * kUGatherWarps) {
+                        const int i = it >> 3, pc = it & 7;
                         const int row = c * CF::CH + i;
                         const bool valid = row < nk;
                         int64_t j;
                         if constexpr (PAGED) j = roff[i];
                         else j = valid ? (int64_t)cidx[row] : 0;
-                        const uint32_t off = (uint32_t)(pc >> 3) * CF::PLANE + (uint32_t)i * 128u + ((uint32_t)((pc & 7) ^ (i & 7)) << 4);
-                        cp_async_16_zfill(dst + off, src + j * D + pc * 8, valid);
+                        const uint32_t off = (uint32_t)i * 128u + ((uint32_t)(pc ^ (i & 7)) << 4);
+                        const uint16_t* sp = src + j * D + pc * 8;
+                        cp_async_16_zfill(dst + off, sp, valid);
+                        if constexpr (D == 128) cp_async_16_zfill(dst + CF::PLANE + off, sp + 64, valid);
                     }
                 };
                 copy_rows(smem + CF::OFF_K + bf * CF::KV, Kb);
                 cp_async_mbar_arrive(&k_full[bf]);
+                if (warp == 5 && c < 3) SSA_MARKW(30 + c);
                 if (g >= 2) {
                     if (lane == 0 && !mbar_wait_bounded(&v_free[bf], ph)) flag(status, DEV_TIMEOUT);
                     __syncwarp();
@@ -598,11 +602,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                     const int gs = gbase + cs, go = gbase + co;
                     const bool s_next = cs < nc && cs <= co + 1;
                     if (s_next && mbar_test_wait(&k_full[gs & 1], (uint32_t)(gs >> 1) & 1u)) {
+                        if (cs < 3) SSA_MARKW(33 + cs);
                         mma_s(gs);
                         ++cs;
                         idle = false;
                     } else if (co < cs && mbar_test_wait(&p_ready[go & 1], (uint32_t)(go >> 1) & 1u) &&
                                mbar_test_wait(&v_full[go & 1], (uint32_t)(go >> 1) & 1u)) {
+                        if (co < 3) SSA_MARKW(36 + co);
                         mma_o(go);
                         ++co;
                         idle = false;
@@ -758,6 +764,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
                             m_run[gg] = mn;
                         }
                     }
+                    if (c <= 3) SSA_MARK(59 + c);
                 }
 #pragma unroll
                 for (int gg = 0; gg < G; ++gg) {
