@@ -140,3 +140,14 @@ def test_read_ceiling_without_a_gpu_reports_nothing():
         pytest.skip("a GPU is present: the probe runs")
     # the probe either is not built or finds no device: either way no figure, and no exception
     assert bench.read_ceiling([32768]) is None
+
+
+def test_read_ceiling_probe_rejects_sizes_that_are_not_whole_chunks():
+    """The probe checks its arguments before it touches a device."""
+    from long_context_decode_subset_b300 import build
+    exe = build.build_ceiling()
+    for arg in ("1000", "0", "x"):
+        r = subprocess.run([exe, arg], capture_output=True, text=True, timeout=60)
+        assert r.returncode == 2 and "multiple" in r.stderr, (arg, r.returncode, r.stderr)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 2 and "usage" in r.stderr
