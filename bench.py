@@ -248,8 +248,10 @@ def read_ceiling(byte_counts):
     ring (read_ceiling.cu), each launch timed alone with CUDA events after an L2 flush, as the score pass is.
     {bytes: (plain_us, ring_us)}, or None if the probe is missing or fails."""
     import subprocess
-    exe = os.path.join(ROOT, "long_context_decode_subset_b300", "read_ceiling")
-    if not os.path.exists(exe):
+    try:
+        from long_context_decode_subset_b300 import build
+        exe = build.build_ceiling()   # built with the library; compiled here if it is missing
+    except Exception:
         return None
     try:
         res = subprocess.run([exe, *[str(int(b)) for b in byte_counts]], capture_output=True, text=True,
