@@ -82,32 +82,44 @@ __device__ __forceinline__ int32_t pool_token_c(const Params& p, const PageCache
 // their exclusive prefix (pre[kSelWarps] = length).  With a compact list
 // requested, the kept (index, p) pairs also go to the unit's staging area at
 // stage_at.  NT threads; ends with a block barrier.
+// Copies entries [c0, c0 + n) of the tile's list (the concatenation of its
+// warp slices, pre[] their exclusive prefix) to ridx / rval with cp.async,
+// one commit group; the caller waits for it.  NT threads.
+template <int NT>
+__device__ void stage_list(const Params& p, int u, int tile, int64_t c0, int n, const uint32_t* pre,
+                           int32_t* ridx, float* rval)
+{
+    const Plan& pl = p.pl;
+    const int W2 = pl.tt / kSelWarps;
+    const int32_t* sidx = ws_sel_idx(p) + (size_t)u * pl.np;
+    const float* sp = ws_sel_p(p) + (size_t)u * pl.np;
+#pragma unroll 1
+    for (int i = threadIdx.x; i < n; i += NT) {
+        const int64_t pos = c0 + i;
+        int lo_l = 0, hi_l = kSelWarps;   // pre[lo_l] <= pos < pre[hi_l]
+        while (hi_l - lo_l > 1) {
+            const int mid = (lo_l + hi_l) >> 1;
+            if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
+        }
+        const size_t at = (size_t)tile * pl.tt + (size_t)lo_l * W2 + (size_t)(pos - pre[lo_l]);
+        cp_async_4(ridx + i, sidx + at);
+        cp_async_4(rval + i, sp + at);
+    }
+    cp_async_commit();
+}
+
 template <int LIST, int NT, bool PAGED>
 __device__ int stage_decide(const Params& p, int mode, int u, int b, int h, int tile, int64_t c0, int n,
                             int64_t stage_at, const uint32_t* pre, const UnitSel& us, int32_t* ridx, float* rval,
-                            int32_t* cidx, float* clp, uint32_t* scan, const PageCache& pc)
+                            int32_t* cidx, float* clp, uint32_t* scan, const PageCache& pc, bool prestaged)
 {
     constexpr int PER = (LIST + NT - 1) / NT;   // entries per thread at most
     static_assert(PER <= 32, "one keep bit per entry in a word");
     const Plan& pl = p.pl;
     const int tid = threadIdx.x;
-    const int W2 = pl.tt / kSelWarps;
     uint32_t* status = ws_status(p);
-    const int32_t* sidx = ws_sel_idx(p) + (size_t)u * pl.np;
-    const float* sp = ws_sel_p(p) + (size_t)u * pl.np;
     if (mode == 0) {
-#pragma unroll 1
-        for (int i = tid; i < n; i += NT) {
-            const int64_t pos = c0 + i;
-            int lo_l = 0, hi_l = kSelWarps;   // pre[lo_l] <= pos < pre[hi_l]
-            while (hi_l - lo_l > 1) {
-                const int mid = (lo_l + hi_l) >> 1;
-                if ((int64_t)pre[mid] <= pos) lo_l = mid; else hi_l = mid;
-            }
-            const size_t at = (size_t)tile * pl.tt + (size_t)lo_l * W2 + (size_t)(pos - pre[lo_l]);
-            cp_async_4(ridx + i, sidx + at);
-            cp_async_4(rval + i, sp + at);
-        }
+        if (!prestaged) stage_list<NT>(p, u, tile, c0, n, pre, ridx, rval);   // else already in flight
     } else if (mode == 2) {
 #pragma unroll 1
         for (int i = tid; i < n; i += NT) {
@@ -425,6 +437,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
     // a paged cache's unit whose stratum holds all its tokens keeps every one
     // with p = 1 (a sequence shorter than k)
     uint32_t k_unit = 0;
+    bool prestaged = false;   // the first list chunk's copies are in flight
     if (mode == 0) {
         k_unit = (p.strata == 2) ? topp_size(p, u, r, nu, sh, smem) : (uint32_t)min(p.top_k, (int64_t)0xffffffff);
         if (PAGED && (int64_t)k_unit >= nu) mode = 1;
@@ -443,6 +456,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
             atomicAdd(&ctrl->arrive, 1u);
         }
         SSA_MARK(3);
+        // the first list chunk is this CTA's own: its copies to shared memory
+        // go out now and land while the unit's other tiles finish and the
+        // resolve runs (the resolve stages in other bytes)
+        __syncthreads();
+        stage_list<kSelThreads>(p, u, r, 0, (int)min((int64_t)LIST, (int64_t)pre[kSelWarps]), pre,
+                                reinterpret_cast<int32_t*>(smem + CF::OFF_RAW),
+                                reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4));
+        prestaged = true;
         // every tile of the unit has arrived: resolve the k-th token and Z
         // (every CTA computes the same result)
         if (tid == 0 && !wait_geq_bounded(&ctrl->arrive, (uint32_t)C)) flag(status, DEV_TIMEOUT);
@@ -497,7 +518,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) unit_kernel(const __grid_const
         int32_t* ridx = reinterpret_cast<int32_t*>(smem + CF::OFF_RAW);
         float* rval = reinterpret_cast<float*>(smem + CF::OFF_RAW + LIST * 4);
         const int nk = stage_decide<LIST, kSelThreads, PAGED>(p, mode, u, b, h, r, c0, n, stage_base + kept, pre, us,
-                                                              ridx, rval, cidx, clp, scan, pc);
+                                                              ridx, rval, cidx, clp, scan, pc,
+                                                              prestaged && c0 == lo);
         kept += nk;
         const int nc = p.attend ? (nk + CF::CH - 1) / CF::CH : 0;
         if (warp >= 5) {
